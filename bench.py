@@ -1,0 +1,541 @@
+#!/usr/bin/env python
+"""Benchmark of the hybrid-head attention path on GB300.
+
+One JSON line on stdout (rank 0).  Metric: hybrid-attention prefill useful
+TFLOP/s (only unmasked (query, key) pairs count, 4*d flops each), with decode
+GB/s of the kept KV-cache bytes reported beside it.
+
+  step      one pass of the prefill path over one batch: the planner (visited
+            tiles, longest-first work queue) and the fused FA/SSA/BLOCK
+            attention kernel, on the workload named by --workload (default: the
+            Llama-3.1-8B-shaped 32K layer, 6 of 8 KV heads SSA).
+  value     useful TFLOP/s of the whole step, inputs resident in HBM; L2 is
+            flushed (256 MB memset) before every timed step, outside the
+            events.
+  e2e       the same metric through the C ABI with pinned host buffers: Q/K/V
+            and the mode mask copied in, O and LSE copied out, every step.
+  decode    B=32 x 128K-token cache, 2 FA + 6 SSA KV heads: kept K/V bytes per
+            step / step time.
+  roofline  the attention kernel alone (CUDA events around its launch):
+            visited-tile flops / its duration against the measured bf16 peak.
+
+--impl reference runs the fp64 CPU oracle (the only independent implementation
+of this method here) on a bounded row sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "hybrid-attn prefill useful TFLOP/s (% bf16 peak); decode GB/s (% HBM)"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ counting
+def kept_pairs_per_kv_head(mode, S, sink, window, bm_head=None, T=128):
+    """Unmasked causal (query, key) pairs of one KV head (closed forms)."""
+    if mode == 0:
+        return S * (S + 1) // 2
+    if mode == 1:
+        i = np.arange(S, dtype=np.int64)
+        return int((np.minimum(i + 1, window) + np.clip(np.minimum(sink, i + 1 - window), 0, None)).sum())
+    nB = (S + T - 1) // T
+    rows = np.full(nB, T, dtype=np.int64)
+    rows[-1] = S - (nB - 1) * T
+    below = np.tril(bm_head.astype(np.int64), -1).sum(axis=1)
+    diag = bm_head.diagonal().astype(np.int64)
+    return int((rows * below * T).sum() + (diag * rows * (rows + 1) // 2).sum())
+
+
+def visited_tiles_per_kv_head(mode, S, sink, window, bm_head=None, T=128):
+    nB = (S + T - 1) // T
+    if mode == 0:
+        return nB * (nB + 1) // 2
+    if mode == 1:
+        w_tiles = (window - 1 + T - 1) // T
+        s_tiles = (sink + T - 1) // T
+        tot = 0
+        for qb in range(nB):
+            lo = max(0, qb - w_tiles)
+            tot += min(s_tiles, lo) + (qb - lo + 1)
+        return tot
+    return int(np.tril(bm_head != 0).sum())
+
+
+def prefill_work(cfg, m, bm):
+    """(useful flops, visited-tile flops) of one layer."""
+    g = cfg.Hq // cfg.Hkv
+    useful = visited = 0
+    for b in range(cfg.B):
+        for h in range(cfg.Hkv):
+            mode = int(m[b, h])
+            bmh = None if bm is None else bm[b, h]
+            useful += kept_pairs_per_kv_head(mode, cfg.S, cfg.sink, cfg.window, bmh) * g
+            visited += visited_tiles_per_kv_head(mode, cfg.S, cfg.sink, cfg.window, bmh) * g
+    return 4 * cfg.d * useful, 4 * cfg.d * 128 * 128 * visited
+
+
+def decode_kept_bytes(cfg, m):
+    """K+V bytes of the kept cache entries (read once, shared by the group)."""
+    keys = 0
+    for b in range(cfg.B):
+        for h in range(cfg.Hkv):
+            L = cfg.L
+            if int(m[b, h]) == 1:
+                ns = min(cfg.sink, L)
+                keys += ns + (L - max(L - cfg.window, ns))
+            else:
+                keys += L
+    return keys * 2 * cfg.d * 2
+
+
+# ------------------------------------------------------------------ environment
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    out = {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+           "bf16_tflops_sustained": None, "source": "fallback"}
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        flat = {}
+
+        def walk(x, pre=""):
+            if isinstance(x, dict):
+                for k, v in x.items():
+                    walk(v, pre + k + ".")
+            elif isinstance(x, (int, float)):
+                flat[pre[:-1]] = float(x)
+        walk(d)
+        for k, v in flat.items():
+            kl = k.lower()
+            if "hbm" in kl and "gbs" in kl:
+                out["hbm_gbs"] = v
+            elif "bf16" in kl and "sustained" in kl:
+                out["bf16_tflops_sustained"] = v
+            elif "bf16" in kl and "tflops" in kl:
+                out["bf16_tflops"] = v
+        out["source"] = "measured"
+    except (OSError, ValueError):
+        pass
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                try:
+                    sm.append(float(p[1]))
+                    mx.append(float(p[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, p[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def profile_traffic(name, src):
+    """DRAM traffic per launch recorded by an ncu summary under profiles/, if the
+    kernel source has not changed since (else None)."""
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith(("traffic_bytes_per_launch", "source_sha256")):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != digest or "traffic_bytes_per_launch" not in vals:
+        return None
+    return float(vals["traffic_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ workloads
+def get_cfg(name):
+    from sparse_head_attention_gb300 import workloads as wl
+    table = {"llama32k": wl.LLAMA_32K, "tiny": wl.TINY, "xa256k": wl.XA_SSA_256K}
+    return table[name]
+
+
+def make_prefill_inputs(cfg, dev):
+    from sparse_head_attention_gb300 import workloads as wl
+    Q, K, V = wl.qkv(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.d, seed=cfg.seed, device=dev)
+    _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads, cfg.fa_impl, cfg.sa_impl)
+    bm = None
+    if cfg.fa_impl == 2 or cfg.sa_impl == 2:
+        bm = wl.block_mask(cfg.B, cfg.Hkv, cfg.S, density=cfg.block_density, seed=cfg.seed)
+    return Q, K, V, m, bm
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, dev):
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+
+    cfg = get_cfg(args.workload)
+    Q, K, V, m_cpu, bm_cpu = make_prefill_inputs(cfg, dev)
+    m = m_cpu.to(dev)
+    bm = None if bm_cpu is None else bm_cpu.to(dev)
+    useful_flops, tile_flops = prefill_work(cfg, m_cpu.numpy(), None if bm_cpu is None else bm_cpu.numpy())
+    O = torch.empty_like(Q)
+    LSE = torch.empty(cfg.B, cfg.Hq, cfg.S, dtype=torch.float32, device=dev)
+    ws = ea.prefill_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        ea.ea_prefill_plan(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, m, sink=cfg.sink, window=cfg.window,
+                           block_mask=bm, workspace=ws)
+        if ev is not None:
+            ev[0].record(stream)
+        ea.ea_prefill_attend(Q, K, V, m, sink=cfg.sink, window=cfg.window, block_mask=bm,
+                             O=O, LSE=LSE, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_k = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev_s[i].record(stream)
+        step(ev_k[i])
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    step_ms = sum(s.elapsed_time(e) for s, e in zip(ev_s, ev_e))
+    kern_ms = [a.elapsed_time(b) for a, b in ev_k]
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error during the timed steps")
+    if world > 1:
+        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    ms_per_step = step_ms / args.steps
+    value = world * useful_flops * args.steps / (step_ms * 1e-3) / 1e12
+
+    peaks = measured_peaks()
+    k_ms = statistics.mean(kern_ms)
+    achieved = tile_flops / (k_ms * 1e-3) / 1e12
+    traffic = profile_traffic("prefill_attention_llama32k.md",
+                              os.path.join(ROOT, "sparse_head_attention_gb300", "csrc", "ea_prefill.cu"))
+    roofline = {"bound": "tensor", "kernel": "hybrid_prefill_kernel", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "traffic": traffic, "peak_source": peaks["source"],
+                "work": "visited-tile flops 4*d*128*128 per tile per query head = %.4e per launch" % tile_flops,
+                "kernel_ms": round(k_ms, 4)}
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hQ = Q.cpu().pin_memory()
+        hK = K.cpu().pin_memory()
+        hV = V.cpu().pin_memory()
+        hm = m_cpu.pin_memory()
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        hL = torch.empty(LSE.shape, dtype=LSE.dtype, pin_memory=True)
+        dQ, dK, dV, dm = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(m)
+
+        def e2e_step():
+            dQ.copy_(hQ, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            dm.copy_(hm, non_blocking=True)
+            ea.ea_hybrid_attn_prefill(dQ, dK, dV, dm, sink=cfg.sink, window=cfg.window, block_mask=bm,
+                                      O=O, LSE=LSE, workspace=ws)
+            hO.copy_(O, non_blocking=True)
+            hL.copy_(LSE, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = 0.0
+        n_e2e = max(3, min(args.steps, 10))
+        for _ in range(n_e2e):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            e_ms += a.elapsed_time(b)
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hm))
+        d2h = sum(t.numel() * t.element_size() for t in (hO, hL))
+        e2e = {"value": round(world * useful_flops * n_e2e / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms / n_e2e, 3)}
+        del hQ, hK, hV, dQ, dK, dV
+
+    # ---- decode
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(args, dev, peaks, flush)
+
+    # ---- router latency (36-layer 64K shape: 8 KV heads, 128 -> 64 -> 2)
+    router = run_router(dev)
+
+    # ---- sparsity ratios of the timed layer (host)
+    msr, esr = ea.ea_sparsity_ratios(
+        (m_cpu.numpy() == cfg.sa_impl).astype(np.uint8), m_cpu.numpy(), cfg.S, sink=cfg.sink,
+        window=cfg.window, block_masks=None if bm_cpu is None else [bm_cpu.numpy()[0]])
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V; seeded SA-head choice)",
+        "config": {"workload": cfg.name, "B": cfg.B, "seq_len": cfg.S, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                   "d": cfg.d, "sa_heads": cfg.sa_heads, "sink": cfg.sink, "window": cfg.window,
+                   "omega_msr": msr, "omega_esr": round(esr, 6),
+                   "useful_flops_per_step": useful_flops, "visited_tile_flops_per_step": tile_flops,
+                   "pct_of_bf16_peak": round(100 * value / world / peaks["bf16_tflops"], 2),
+                   "l2": "flushed before every timed step (256 MB memset, outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        "decode": decode,
+        "router": router,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V, m_cpu, args)
+    return line
+
+
+def run_decode(args, dev, peaks, flush):
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    cfg = wl.DECODE_128K
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev)
+    _, m_cpu = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
+    m = m_cpu.to(dev)
+    nbytes = decode_kept_bytes(cfg, m_cpu.numpy())
+    ws = ea.decode_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.L, device=dev)
+    O = torch.empty_like(q)
+    LSE = torch.empty(cfg.B, cfg.Hq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m, sink=cfg.sink, window=cfg.window, O=O, LSE=LSE,
+                                 workspace=ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    n = max(args.steps, 20)
+    ms = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m, sink=cfg.sink, window=cfg.window, O=O, LSE=LSE,
+                                 workspace=ws)
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in decode")
+    t = statistics.mean(a.elapsed_time(b) for a, b in ms)
+    gbs = nbytes / (t * 1e-3) / 1e9
+    del Kc, Vc
+    return {"workload": cfg.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(t, 4),
+            "kept_kv_bytes_per_step": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_merge_kernel",
+                         "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "peak_source": peaks["source"]},
+            "gpu_launches_per_step": 2, "clocks": clk}
+
+
+def run_router(dev):
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    cfg = wl.QWEN_64K_36L
+    K = wl.randn_bf16((1, cfg.S, cfg.Hkv, cfg.d), seed=1, device=dev)
+    W, b = wl.router_weights(0, d=cfg.d, hidden=64, device=dev)
+    r = torch.empty(1, cfg.Hkv, dtype=torch.uint8, device=dev)
+    mm = torch.empty_like(r)
+    for _ in range(3):
+        ea.ea_route(K, W, b, r_out=r, m_out=mm)
+    torch.cuda.synchronize()
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 36
+    a.record()
+    for _ in range(n):
+        ea.ea_route(K, W, b, r_out=r, m_out=mm)
+    e.record()
+    torch.cuda.synchronize()
+    return {"workload": "router pre-pass, 8 KV heads, S=65536, MLP 128-64-2, per layer",
+            "us_per_layer": round(1000 * a.elapsed_time(e) / n, 2)}
+
+
+# ------------------------------------------------------------------ oracle
+def _oracle_sample(cfg, Q, K, V, m_cpu, n_rows_per_head=256):
+    """A bounded row sample: for one query head of every KV head, rows spread
+    evenly over the sequence."""
+    g = cfg.Hq // cfg.Hkv
+    idx = np.linspace(0, cfg.S - 1, n_rows_per_head).astype(np.int64)
+    rows = np.array([[0, h * g, i] for h in range(cfg.Hkv) for i in idx], dtype=np.int64)
+    flops = 0
+    for h in range(cfg.Hkv):
+        mode = int(m_cpu[0, h])
+        for i in idx:
+            if mode == 0:
+                kept = i + 1
+            else:
+                kept = min(i + 1, cfg.window) + max(0, min(cfg.sink, i + 1 - cfg.window))
+            flops += 4 * cfg.d * kept
+    return rows, flops
+
+
+def cpu_baseline(cfg, Q, K, V, m_cpu, args, rows_per_head=256):
+    import oracle
+    Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
+    rows, flops = _oracle_sample(cfg, Qc, Kc, Vc, m_cpu, rows_per_head)
+    t0 = time.perf_counter()
+    oracle.prefill_rows(Qc, Kc, Vc, m_cpu, rows, sink=cfg.sink, window=cfg.window)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d query rows (%d per KV head, evenly spaced) of %s, %.3g useful flops, %.2f s"
+                      % (len(rows), rows_per_head, cfg.name, flops, dt)}
+
+
+def run_reference(args):
+    import oracle
+    cfg = get_cfg(args.workload)
+    Q, K, V, m_cpu, _ = make_prefill_inputs(cfg, "cpu")
+    rows, flops = _oracle_sample(cfg, Q, K, V, m_cpu, 64)
+    oracle.lib()
+    for _ in range(args.warmup):
+        oracle.prefill_rows(Q, K, V, m_cpu, rows[:8], sink=cfg.sink, window=cfg.window)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.prefill_rows(Q, K, V, m_cpu, rows, sink=cfg.sink, window=cfg.window)
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    sample = ("%d query rows (64 per KV head, evenly spaced) of %s per step, %.3g useful flops"
+              % (len(rows), cfg.name, flops))
+    return {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V)", "impl": "reference",
+            "config": {"workload": cfg.name, "B": cfg.B, "seq_len": cfg.S, "Hq": cfg.Hq,
+                       "Hkv": cfg.Hkv, "d": cfg.d},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama32k", choices=["llama32k", "tiny", "xa256k"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    from sparse_head_attention_gb300 import build as ea_build
+    ea_build.build()
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

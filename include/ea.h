@@ -1,0 +1,258 @@
+/*
+ * ea.h - C ABI of the Elastic Attention hybrid-head attention library (sm_103a).
+ *
+ * Elastic Attention gives every KV head of every layer a per-input routing
+ * decision r in {0 = FA, 1 = SA} from a small Attention Router, maps r to
+ * kernel metadata m, and runs all heads of a layer, whatever their mode, in one
+ * fused launch whose output is the plain concatenation of the per-head outputs.
+ *
+ * Sources (page titles as printed):
+ *   [EN] "Paper Reading - Elastic Attention: Test-time Adaptive Sparsity Ratios"
+ *        (English reading notes of arXiv 2601.17367)
+ *   [ZH] "论文精读 - Elastic Attention" (Chinese reading notes; eqs. 4-5)
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are caller-owned device memory unless marked "host".  The library
+ *     never allocates or frees device memory; scratch space is the caller's
+ *     workspace buffer.  No state is kept between calls except what lives in
+ *     that workspace.
+ *   - Element strides are given in ELEMENTS (not bytes), outermost first.  The
+ *     innermost (head-dim) stride must be 1.
+ *   - bf16 tensors are passed as void* to raw 16-bit bf16 storage.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Device
+ *     entry points only enqueue work on it and return without synchronising.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     rejected call returns an error and enqueues nothing.  Conditions that
+ *     only the device can see (a mode value read from device memory, a wait
+ *     that ran out) set an error word in the workspace, which
+ *     ea_check_errors() reads back.
+ *   - Every function returns an ea_status; no exception or abort crosses the ABI.
+ */
+#ifndef EA_H
+#define EA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EA_OK = 0,
+    EA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, stride or alignment      */
+    EA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head dim != 128)  */
+    EA_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned        */
+    EA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed                 */
+    EA_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out                */
+    EA_ERR_DEVICE_CHECK = 6   /* the device met an invalid mode / missing mask     */
+} ea_status;
+
+/* Per-KV-head kernel metadata m ([EN] §04 Deployment, Algorithm 1(b): the
+ * routing decision r becomes metadata that each thread block branches on). */
+typedef enum {
+    EA_FULL = 0,   /* full causal attention, [EN] §02 eq. (1)                       */
+    EA_SSA = 1,    /* streaming sparse attention: key j < sink or i - j < window,   */
+                   /* [EN] §02 eq. (2), Glossary "SSA"                              */
+    EA_BLOCK = 2   /* block-sparse attention over a caller-given 128x128 block mask */
+                   /* (the compute half of XAttention), [EN] Glossary "XA"          */
+} ea_mode;
+
+/* How a routing decision maps to a mode: m = r ? sa_impl : fa_impl.
+ * "FA-SSA" = {EA_FULL, EA_SSA}; "XA-SSA" = {EA_BLOCK, EA_SSA}
+ * ([EN] §05 Experiments, "{retrieval}-{sparse}"). */
+typedef struct {
+    uint8_t fa_impl;
+    uint8_t sa_impl;
+} ea_policy;
+
+/* Router MLP: n_layers dense layers, dims[0] = head dim ... dims[n_layers] = 2,
+ * ReLU between layers (not after the last).  W[l] is a DEVICE pointer to a
+ * row-major float32 [dims[l+1]][dims[l]] matrix, b[l] a DEVICE float32
+ * [dims[l+1]] vector.  The struct and the dims/W/b pointer arrays are host
+ * memory.  Limits: 1 <= n_layers <= 4, every dims[l] <= 1024. */
+typedef struct {
+    int n_layers;
+    const int *dims;
+    const float *const *W;
+    const float *const *b;
+} ea_mlp;
+
+/* Human-readable name of a status code (static storage). */
+const char *ea_status_string(ea_status s);
+
+/*
+ * ea_route - Attention Router pre-pass ([EN] §03 Method, "Method: the Attention
+ * Router" and eq. 6; [ZH] §04 Method, "Router 怎么工作").
+ *
+ * For every (b, KV head h): mean-pool K over the first pool_head and last
+ * pool_tail tokens (100 + 100 on the pages; a token in both ranges counts
+ * once), run the MLP in fp64, take r = argmax of the two logits (ties -> 0 = FA)
+ * and m = r ? policy.sa_impl : policy.fa_impl.
+ *
+ *   K          device bf16 [B][S][Hkv][d], element strides k_strides[4]
+ *   r_out      device uint8 [B][Hkv]   routing decision (0 = FA, 1 = SA)
+ *   m_out      device uint8 [B][Hkv]   kernel metadata (an ea_mode)
+ *   logits_out device double [B][Hkv][2] or NULL
+ *
+ * Constraints: d == dims[0] <= 1024, pool_head + pool_tail >= 1, S >= 1.
+ * Errors: EA_ERR_INVALID_ARG / EA_ERR_UNSUPPORTED on the host, EA_ERR_CUDA if
+ * the launch fails.
+ */
+ea_status ea_route(const void *K, const int64_t k_strides[4], int B, int S, int Hkv, int d,
+                   int pool_head, int pool_tail, const ea_mlp *mlp, ea_policy policy,
+                   uint8_t *r_out, uint8_t *m_out, double *logits_out, void *stream);
+
+/* Bytes of device workspace ea_hybrid_attn_prefill needs for these sizes
+ * (0 on invalid sizes).  The workspace must be 256-byte aligned. */
+size_t ea_prefill_workspace_size(int B, int S, int Hq, int Hkv, int d);
+
+/*
+ * ea_hybrid_attn_prefill - fused hybrid-head attention prefill of one layer
+ * ([EN] §02 eqs. (1)-(3); §04 Deployment, Algorithm 1(b) and Figure 4).
+ *
+ * Query head qh uses KV head h = qh / (Hq / Hkv) and that head's mode m[b][h]:
+ *   EA_FULL : key j kept for query i iff j <= i
+ *   EA_SSA  : j <= i and (j < sink or i - j < window)
+ *   EA_BLOCK: j <= i and block_mask[b][h][i / 128][j / 128] != 0
+ * O[b][i][qh][:] = softmax over kept keys of scale * q_i . k_j, times V;
+ * LSE[b][qh][i] = ln sum_kept exp(scale * q_i . k_j) (natural log).
+ * A query with no kept key gets O = 0 and LSE = -inf.
+ * All heads run in one persistent launch; each head's output is written in
+ * place into its slice of O (eq. 3 concatenation, no copy).
+ *
+ *   Q            device bf16 [B][S][Hq][d],  element strides q_str[4]
+ *   K, V         device bf16 [B][S][Hkv][d], element strides kv_str[4] (shared)
+ *   O            device bf16 [B][S][Hq][d],  element strides o_str[4]
+ *   LSE          device float [B][Hq][S] contiguous, or NULL
+ *   m            device uint8 [B][Hkv] (ea_mode values)
+ *   block_mask   device uint8 [B][Hkv][nB][nB], nB = ceil(S/128), row-major;
+ *                entries above the diagonal are ignored.  May be NULL only if
+ *                no head is EA_BLOCK (checked on the device).
+ *   block_size   must be 128
+ *   workspace    device, >= ea_prefill_workspace_size(...) bytes, 256-aligned;
+ *                overwritten by the call.  Calls that share a workspace must
+ *                be ordered on one stream.
+ *   visited_bitmap  device uint32 or NULL.  When non-NULL, one bit per tile
+ *                (b, h, qb, kb) at bit index ((b*Hkv + h)*nB + qb)*nB + kb is
+ *                OR-ed in for every key tile the kernel visits; the caller
+ *                zeroes it first.  A debugging aid for tile-skipping parity.
+ *
+ * Constraints: d == 128; Hq % Hkv == 0; 1 <= S <= 2^21;
+ * sink >= 0; window >= 1; base pointers 16-byte aligned; q/kv/o strides of the
+ * b, s and h dimensions multiples of 8 elements; head-dim stride 1.
+ * Errors: EA_ERR_INVALID_ARG, EA_ERR_UNSUPPORTED, EA_ERR_WORKSPACE on the host;
+ * EA_ERR_CUDA on a failed launch; device-side problems (mode value > 2,
+ * BLOCK head with NULL block_mask, a bounded wait that ran out) are reported
+ * by ea_check_errors(workspace).
+ */
+ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                 const int64_t q_str[4], const int64_t kv_str[4],
+                                 const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                                 float scale, const uint8_t *m, int sink, int window,
+                                 const uint8_t *block_mask, int block_size, void *workspace,
+                                 size_t ws_bytes, uint32_t *visited_bitmap, void *stream);
+
+/*
+ * The two halves of ea_hybrid_attn_prefill, for callers that reuse one plan
+ * (same m, block mask and sizes) across several launches, or that time the
+ * attention kernel on its own.  ea_hybrid_attn_prefill == ea_prefill_plan
+ * followed by ea_prefill_attend with the same arguments and workspace.
+ *
+ * ea_prefill_plan enqueues the planner: per (b, KV head, 128-query block) the
+ * number of key tiles that hold at least one kept pair, then a stable
+ * longest-first work queue of (block, query-head pair) items, written to the
+ * workspace.  ea_prefill_attend enqueues the persistent attention kernel that
+ * consumes that queue; it must follow a plan made with the same m,
+ * block_mask, sink, window and sizes, on the same stream; one plan may feed
+ * any number of ea_prefill_attend launches (the kernel re-arms the queue when
+ * it has drained it).  Arguments,
+ * constraints and errors are those of ea_hybrid_attn_prefill.
+ */
+ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m, int sink,
+                          int window, const uint8_t *block_mask, int block_size, void *workspace,
+                          size_t ws_bytes, void *stream);
+
+ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                            const int64_t q_str[4], const int64_t kv_str[4],
+                            const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                            float scale, const uint8_t *m, int sink, int window,
+                            const uint8_t *block_mask, int block_size, void *workspace,
+                            size_t ws_bytes, uint32_t *visited_bitmap, void *stream);
+
+/* Bytes of device workspace ea_hybrid_attn_decode needs (0 on invalid sizes).
+ * num_splits = 0 means the automatic choice; the same value must be passed to
+ * ea_hybrid_attn_decode. */
+size_t ea_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int num_splits);
+
+/*
+ * ea_hybrid_attn_decode - one decode step of hybrid-head attention with the
+ * routing decision fixed at prefill ([EN] §08 Commentary, stated limit ③:
+ * routing happens once per request at the prefill stage).
+ *
+ * For sequence b with L = seqlens[b] cached tokens (the cache already holds
+ * the current token) and query head qh (KV head h = qh / (Hq/Hkv)):
+ *   EA_FULL : keys j in [0, L)
+ *   EA_SSA  : keys j in [0, L) with j < sink or (L - 1) - j < window
+ * O[b][qh][:] = softmax(scale * q . k_j) V over those keys; LSE[b][qh] its
+ * natural log-sum-exp.  L = 0 gives O = 0, LSE = -inf.  Work is split along
+ * the key axis and merged by log-sum-exp.
+ *
+ *   q        device bf16 [B][Hq][d], element strides q_str[3]
+ *   Kc, Vc   device bf16 [B][Lmax][Hkv][d], element strides kv_str[4] (shared)
+ *   O        device bf16 [B][Hq][d], element strides o_str[3]
+ *   LSE      device float [B][Hq] contiguous, or NULL
+ *   seqlens  device int32 [B], each in [0, Lmax] (checked on the device)
+ *   m        device uint8 [B][Hkv]; EA_BLOCK is rejected (device error word):
+ *            the pages define no decode reading of a block mask
+ *   num_splits  0 = automatic, else 1..1024 key-axis splits per (b, KV head)
+ *   workspace   device, >= ea_decode_workspace_size(...) bytes, 256-aligned
+ *
+ * Constraints: d == 128; Hq % Hkv == 0 and Hq / Hkv <= 8; sink >= 0;
+ * window >= 1; 16-byte aligned base pointers; cache strides of b, position and
+ * head dimensions multiples of 8 elements; head-dim strides 1.
+ * Errors: as for the prefill.
+ */
+ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, void *O, float *LSE,
+                                const int64_t q_str[3], const int64_t kv_str[4],
+                                const int64_t o_str[3], const int32_t *seqlens, int B, int Hq,
+                                int Hkv, int d, int Lmax, float scale, const uint8_t *m, int sink,
+                                int window, int num_splits, void *workspace, size_t ws_bytes,
+                                void *stream);
+
+/*
+ * ea_sparsity_ratios - model sparsity ratio and effective sparsity ratio of one
+ * input over L layers ([ZH] §02 Background, eqs. (4)-(5); [EN] §02).  HOST
+ * function; all pointers are host memory; nothing touches the GPU.
+ *
+ *   Omega_MSR = (1/(L Hkv)) sum_{l,h} [r[l][h] == 1]
+ *   Omega_ESR = (1/(L Hkv)) sum_{l,h} rho(l,h)
+ * where rho is the share of the S(S+1)/2 causal (query, key) pairs that the
+ * head's executed mode m[l][h] prunes (0 for EA_FULL, and e.g. 0.9 when 10%
+ * are kept).  Since all heads share the causal count, the result is computed
+ * as one division of exact integer pair counts, i.e. correctly rounded.
+ *
+ *   r, m         host uint8 [L][Hkv]
+ *   block_masks  host array of L pointers, each to uint8 [Hkv][nB][nB], or
+ *                NULL; required for layers holding EA_BLOCK heads
+ *   block_size   must be 128 when a mask is read
+ * Errors: EA_ERR_INVALID_ARG (null output, r > 1, m > 2, BLOCK without mask,
+ * S < 1).
+ */
+ea_status ea_sparsity_ratios(const uint8_t *r, const uint8_t *m, int L, int Hkv, int S, int sink,
+                             int window, const uint8_t *const *block_masks, int block_size,
+                             double *omega_msr, double *omega_esr);
+
+/*
+ * ea_check_errors - synchronise `stream`, then read and clear the device error
+ * word at the start of a prefill or decode workspace.  Returns EA_OK,
+ * EA_ERR_DEVICE_CHECK, EA_ERR_TIMEOUT, or EA_ERR_CUDA.  This is the only
+ * entry point that blocks the host.
+ */
+ea_status ea_check_errors(void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EA_H */

@@ -18,9 +18,11 @@ OUT = os.path.join(OUT_DIR, "libea_oracle.so")
 def build(force: bool = False, verbose: bool = False) -> str:
     """Build the oracle library if it is missing or older than its source."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(OUT) and os.path.getmtime(OUT) >= os.path.getmtime(SRC):
+    newest = max(os.path.getmtime(SRC), os.path.getmtime(os.path.abspath(__file__)))
+    if not force and os.path.exists(OUT) and os.path.getmtime(OUT) >= newest:
         return OUT
-    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", SRC, "-lm"]
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-fno-fast-math", "-ffp-contract=off", SRC,
+            "-lm"]
     tmp = OUT + ".tmp.%d" % os.getpid()
     for extra in (["-fopenmp"], []):
         cmd = base[:1] + extra + base[1:] + ["-o", tmp]

@@ -1,0 +1,267 @@
+"""Elastic Attention hybrid-head attention on GB300 (sm_103a).
+
+Thin Python binding over the C ABI declared in ``include/ea.h``; the names match
+the C entry points.  This module only marshals arguments (pointers, strides,
+streams) from torch tensors: every step of the computation runs in the CUDA
+library ``_lib/libea.so``.  If that library is missing, or no CUDA device is
+present, the device entry points raise instead of computing anything else.
+
+    ea_route                 router pre-pass (pool -> MLP -> argmax -> mode)
+    ea_hybrid_attn_prefill   fused FA / SSA / block-sparse prefill, one launch
+    ea_hybrid_attn_decode    split-KV decode with the prefill-time routing
+    ea_sparsity_ratios       Omega_MSR / Omega_ESR (host)
+    ea_check_errors          read back the device error word of a workspace
+"""
+import ctypes
+import math
+import os
+
+import torch
+
+FULL, SSA, BLOCK = 0, 1, 2
+TILE = 128
+EA_OK = 0
+_STATUS = {0: "EA_OK", 1: "EA_ERR_INVALID_ARG", 2: "EA_ERR_UNSUPPORTED", 3: "EA_ERR_WORKSPACE",
+           4: "EA_ERR_CUDA", 5: "EA_ERR_TIMEOUT", 6: "EA_ERR_DEVICE_CHECK"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libea.so")
+_lib = None
+
+# Function names exported by the library (the ones include/ea.h declares).
+EXPORTS = ("ea_status_string", "ea_route", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
+           "ea_prefill_plan", "ea_prefill_attend", "ea_decode_workspace_size",
+           "ea_hybrid_attn_decode", "ea_sparsity_ratios", "ea_check_errors")
+
+
+class EAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, _STATUS.get(status, status)))
+
+
+class _Mlp(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("dims", ctypes.POINTER(ctypes.c_int)),
+                ("W", ctypes.POINTER(ctypes.c_void_p)), ("b", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class _Policy(ctypes.Structure):
+    _fields_ = [("fa_impl", ctypes.c_uint8), ("sa_impl", ctypes.c_uint8)]
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libea.so is not built; run __graft_entry__.build() or "
+                               "python sparse_head_attention_gb300/build.py")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, sz, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float,
+                                ctypes.c_double)
+        L.ea_status_string.argtypes = [i32]
+        L.ea_status_string.restype = ctypes.c_char_p
+        L.ea_route.argtypes = [P, P, i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Mlp), _Policy,
+                               P, P, P, P]
+        L.ea_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.ea_prefill_workspace_size.restype = sz
+        L.ea_hybrid_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
+                                             P, i32, i32, P, i32, P, sz, P, P]
+        L.ea_prefill_plan.argtypes = [i32, i32, i32, i32, i32, P, i32, i32, P, i32, P, sz, P]
+        L.ea_prefill_attend.argtypes = list(L.ea_hybrid_attn_prefill.argtypes)
+        L.ea_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.ea_decode_workspace_size.restype = sz
+        L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
+                                            P, i32, i32, i32, P, sz, P]
+        L.ea_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
+                                         ctypes.POINTER(f64), ctypes.POINTER(f64)]
+        L.ea_check_errors.argtypes = [P, P]
+        for f in ("ea_route", "ea_hybrid_attn_prefill", "ea_prefill_plan", "ea_prefill_attend",
+                  "ea_hybrid_attn_decode",
+                  "ea_sparsity_ratios", "ea_check_errors"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(fn, status):
+    if status != EA_OK:
+        raise EAError(fn, status)
+
+
+def _dev(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+def _strides(t):
+    return (ctypes.c_int64 * t.dim())(*t.stride())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def ea_route(K, weights, biases, *, pool_head=100, pool_tail=100, policy=(FULL, SSA),
+             r_out=None, m_out=None, logits_out=None, stream=None):
+    """Router pre-pass on K [B, S, Hkv, d] (bf16, CUDA).  weights/biases: lists of
+    float32 CUDA tensors ([out, in] and [out]).  Returns (r, m, logits)."""
+    _dev(K, "K", torch.bfloat16)
+    B, S, Hkv, d = K.shape
+    dev = K.device
+    r_out = r_out if r_out is not None else torch.empty(B, Hkv, dtype=torch.uint8, device=dev)
+    m_out = m_out if m_out is not None else torch.empty(B, Hkv, dtype=torch.uint8, device=dev)
+    if logits_out is None:
+        logits_out = torch.empty(B, Hkv, 2, dtype=torch.float64, device=dev)
+    Ws = [_dev(w, "W", torch.float32).contiguous() for w in weights]
+    bs = [_dev(b, "b", torch.float32).contiguous() for b in biases]
+    dims = [Ws[0].shape[1]] + [w.shape[0] for w in Ws]
+    c_dims = (ctypes.c_int * len(dims))(*dims)
+    c_W = (ctypes.c_void_p * len(Ws))(*[w.data_ptr() for w in Ws])
+    c_b = (ctypes.c_void_p * len(bs))(*[b.data_ptr() for b in bs])
+    mlp = _Mlp(len(Ws), c_dims, c_W, c_b)
+    st = lib().ea_route(_ptr(K), _strides(K), B, S, Hkv, d, pool_head, pool_tail,
+                        ctypes.byref(mlp), _Policy(*policy), _ptr(r_out), _ptr(m_out),
+                        _ptr(logits_out), _stream(stream))
+    _check("ea_route", st)
+    return r_out, m_out, logits_out
+
+
+def ea_prefill_workspace_size(B, S, Hq, Hkv, d=128):
+    return int(lib().ea_prefill_workspace_size(B, S, Hq, Hkv, d))
+
+
+def prefill_workspace(B, S, Hq, Hkv, d=128, device="cuda"):
+    """A zeroed workspace buffer of the right size (256-byte aligned by torch)."""
+    n = ea_prefill_workspace_size(B, S, Hq, Hkv, d)
+    if n == 0:
+        raise ValueError("unsupported prefill sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ea_hybrid_attn_prefill(Q, K, V, m, *, sink, window, block_mask=None, scale=None, O=None,
+                           LSE=None, workspace=None, visited_bitmap=None, stream=None,
+                           want_lse=True, _entry="ea_hybrid_attn_prefill"):
+    """Fused hybrid-head prefill.  Q [B, S, Hq, d], K/V [B, S, Hkv, d] bf16 (CUDA),
+    m uint8 [B, Hkv] (CUDA).  Returns (O, LSE)."""
+    _dev(Q, "Q", torch.bfloat16)
+    _dev(K, "K", torch.bfloat16)
+    _dev(V, "V", torch.bfloat16)
+    _dev(m, "m", torch.uint8)
+    if K.stride() != V.stride():
+        raise ValueError("K and V must share strides")
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None and want_lse:
+        LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        workspace = prefill_workspace(B, S, Hq, Hkv, d, Q.device)
+    if block_mask is not None:
+        _dev(block_mask, "block_mask", torch.uint8)
+        if not block_mask.is_contiguous():
+            raise ValueError("block_mask must be contiguous")
+    st = getattr(lib(), _entry)(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _strides(Q), _strides(K), _strides(O),
+        B, S, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window), _ptr(block_mask), TILE,
+        _ptr(workspace), workspace.numel(), _ptr(visited_bitmap), _stream(stream))
+    _check(_entry, st)
+    return O, LSE
+
+
+def ea_prefill_plan(B, S, Hq, Hkv, m, *, sink, window, block_mask=None, workspace, d=128,
+                    stream=None):
+    """Enqueue the planner only (work queue into `workspace`)."""
+    _dev(m, "m", torch.uint8)
+    st = lib().ea_prefill_plan(B, S, Hq, Hkv, d, _ptr(m), int(sink), int(window), _ptr(block_mask),
+                               TILE, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ea_prefill_plan", st)
+
+
+def ea_prefill_attend(Q, K, V, m, *, sink, window, workspace, **kw):
+    """Enqueue the attention kernel on a plan made by ea_prefill_plan."""
+    return ea_hybrid_attn_prefill(Q, K, V, m, sink=sink, window=window, workspace=workspace,
+                                  _entry="ea_prefill_attend", **kw)
+
+
+def ea_decode_workspace_size(B, Hq, Hkv, Lmax, num_splits=0, d=128):
+    return int(lib().ea_decode_workspace_size(B, Hq, Hkv, d, Lmax, num_splits))
+
+
+def decode_workspace(B, Hq, Hkv, Lmax, num_splits=0, d=128, device="cuda"):
+    n = ea_decode_workspace_size(B, Hq, Hkv, Lmax, num_splits, d)
+    if n == 0:
+        raise ValueError("unsupported decode sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ea_hybrid_attn_decode(q, Kc, Vc, seqlens, m, *, sink, window, num_splits=0, scale=None,
+                          O=None, LSE=None, workspace=None, stream=None, want_lse=True):
+    """One decode step.  q [B, Hq, d], Kc/Vc [B, Lmax, Hkv, d] bf16 (CUDA),
+    seqlens int32 [B] (CUDA), m uint8 [B, Hkv] (CUDA).  Returns (O, LSE)."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(Kc, "Kc", torch.bfloat16)
+    _dev(Vc, "Vc", torch.bfloat16)
+    _dev(seqlens, "seqlens", torch.int32)
+    _dev(m, "m", torch.uint8)
+    if Kc.stride() != Vc.stride():
+        raise ValueError("Kc and Vc must share strides")
+    B, Hq, d = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(q)
+    if LSE is None and want_lse:
+        LSE = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, Lmax, num_splits, d, q.device)
+    st = lib().ea_hybrid_attn_decode(
+        _ptr(q), _ptr(Kc), _ptr(Vc), _ptr(O), _ptr(LSE), _strides(q), _strides(Kc), _strides(O),
+        _ptr(seqlens), B, Hq, Hkv, d, Lmax, float(scale), _ptr(m), int(sink), int(window),
+        int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ea_hybrid_attn_decode", st)
+    return O, LSE
+
+
+def ea_sparsity_ratios(r, m, S, *, sink, window, block_masks=None):
+    """Host: (Omega_MSR, Omega_ESR) for r, m uint8 [L, Hkv] (CPU tensors or arrays);
+    block_masks: None or a list of L uint8 [Hkv, nB, nB] CPU arrays (None entries
+    for layers without BLOCK heads)."""
+    import numpy as np
+    ra = np.ascontiguousarray(np.asarray(r.cpu() if isinstance(r, torch.Tensor) else r), np.uint8)
+    ma = np.ascontiguousarray(np.asarray(m.cpu() if isinstance(m, torch.Tensor) else m), np.uint8)
+    L, Hkv = ra.shape
+    keep = []
+    c_masks = None
+    if block_masks is not None:
+        c_masks = (ctypes.c_void_p * L)()
+        for l, bm in enumerate(block_masks):
+            if bm is None:
+                c_masks[l] = None
+                continue
+            a = np.ascontiguousarray(np.asarray(bm.cpu() if isinstance(bm, torch.Tensor) else bm),
+                                     np.uint8)
+            keep.append(a)
+            c_masks[l] = a.ctypes.data
+    msr, esr = ctypes.c_double(), ctypes.c_double()
+    st = lib().ea_sparsity_ratios(ra.ctypes.data, ma.ctypes.data, L, Hkv, S, sink, window,
+                                  c_masks, TILE, ctypes.byref(msr), ctypes.byref(esr))
+    _check("ea_sparsity_ratios", st)
+    return msr.value, esr.value
+
+
+def ea_check_errors(workspace, stream=None):
+    """Synchronise and read/clear the device error word; returns the status code."""
+    return lib().ea_check_errors(_ptr(workspace), _stream(stream))

@@ -1,0 +1,66 @@
+// ea_internal.h - definitions shared by the library's translation units (host
+// and device): workspace layout, device error bits, tile sizes, host helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/ea.h"
+
+// Tile edge (query rows per tile, keys per tile, block-mask block) and head dim.
+#define EA_TILE 128
+#define EA_HEAD_DIM 128
+
+// Device error bits in the workspace error word.
+#define EA_DEVERR_CHECK 1u    // invalid mode / missing block mask / bad seqlen
+#define EA_DEVERR_TIMEOUT 2u  // a bounded wait ran out
+
+// A bounded device wait gives up after this long (ns).
+#define EA_WAIT_TIMEOUT_NS 2000000000ull
+
+// Every workspace starts with this 256-byte header.
+struct ea_ws_header {
+    uint32_t error;         // EA_DEVERR_* bits
+    uint32_t work_counter;  // persistent-kernel work queue head
+    uint32_t n_items;       // number of work items in the queue
+    uint32_t drained;       // CTAs that found the queue empty (last one resets it)
+    uint32_t reserved[60];
+};
+static_assert(sizeof(ea_ws_header) == 256, "workspace header must be 256 bytes");
+
+// Largest supported prefill length: the planner's histogram lives in shared
+// memory (one int per possible tile count).
+#define EA_MAX_SEQ (1 << 21)
+
+namespace ea {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Byte offsets of the prefill workspace regions.
+struct PrefillWs {
+    size_t costs;   // int32 [B*Hkv*nB]: visited tiles per (b, KV head, q block)
+    size_t items;   // uint32 [n_items]: work items, longest first
+    size_t total;
+};
+PrefillWs prefill_ws_layout(int B, int S, int Hq, int Hkv);
+
+// Byte offsets of the decode workspace regions.
+struct DecodeWs {
+    size_t partial_o;    // float [B*Hq*splits*128]
+    size_t partial_lse;  // float [B*Hq*splits]
+    size_t total;
+};
+DecodeWs decode_ws_layout(int B, int Hq, int splits);
+int decode_auto_splits(int Lmax);
+
+// Encodes a 4-D bf16 TMA tensor map (dims innermost first: head dim, heads,
+// sequence, batch; strides in elements) with a 64 x 1 x box_rows x 1 box and
+// 128-byte swizzle (swizzle128) or none.  Returns false if the driver rejects it.
+bool encode_tmap_bf16_4d(void *tmap_out, const void *base, int d, int H, int S, int B,
+                         const int64_t strides_elems[4], int box_inner, int box_rows,
+                         bool swizzle128);
+
+int num_sms(int device);
+
+} // namespace ea

@@ -1,0 +1,899 @@
+// ea_prefill.cu - fused hybrid-head attention prefill for sm_103a.
+//
+// What it computes ("Paper Reading - Elastic Attention" (English notes), §02
+// eqs. (1)-(3); §04 Deployment, Algorithm 1(b)): every query head runs either
+// full causal attention (FA) or sparse attention (SA) over its KV head's kept
+// keys, in one launch, with each head writing its own slice of the output (the
+// eq. 3 concatenation).  The routing decision arrives as per-KV-head metadata
+// m (EA_FULL / EA_SSA / EA_BLOCK) that each work item branches on.
+//
+// How (GB300 design, not the A100/H100 Block-Sparse-Attention kernel the pages
+// name as their implementation):
+//   1. plan_costs: visited key tiles per (b, KV head, 128-query block).
+//   2. plan_sort : one CTA, stable counting sort of those rows, longest first,
+//                  into a work queue of (row, head pair) items.
+//   3. hybrid_prefill_kernel: persistent, one CTA per SM, items taken from an
+//      atomic queue head.  An item is two query heads of one GQA group over one
+//      128-query block, so each K/V tile in shared memory feeds two MMAs.
+//        warp 8     TMA producer: Q tiles, then K/V tiles in MMA order
+//        warp 9     tcgen05 issuer: S_t = Q_t K^T and O_t += P_t V into TMEM
+//        warps 0-7  two softmax warpgroups (one per head of the pair): read S
+//                   from TMEM, mask edge tiles only, online softmax in fp32
+//                   (exp2 domain, lazy rescale of O when the max grows by
+//                   more than 2^8), write P (bf16) to shared memory, and
+//                   finally normalise O and store O / LSE.
+//      TMEM: 512 columns = per head t: S_t (128 fp32 columns) + O_t (128).
+//      Shared memory: Q (2 x 32 KB), P (2 x 32 KB), a 3-stage K/V ring (3 x 32 KB).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "ea_device.cuh"
+#include "ea_internal.h"
+
+namespace ea {
+
+constexpr int T = EA_TILE;
+constexpr int D = EA_HEAD_DIM;
+constexpr int kStages = 3;
+constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale when max grows > 2^8
+constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // V is MN-major
+
+struct __align__(1024) PrefillSmem {
+    uint8_t q[2][kTileBytes];
+    uint8_t p[2][kTileBytes];
+    uint8_t kv[kStages][kTileBytes];
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t q_full, q_empty;
+    uint64_t s_full[2], s_free[2], p_ready[2], o_done[2];
+    uint64_t item_full[2], item_empty[2];
+    uint64_t teardown;
+    int item[2];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kPrefillSmemBytes = sizeof(PrefillSmem) + 1024;  // + alignment slack
+
+struct PrefillArgs {
+    __nv_bfloat16 *O;
+    int64_t o_sb, o_ss, o_sh;
+    float *LSE;
+    const uint8_t *m;
+    const uint8_t *block_mask;
+    uint32_t *visited;
+    int32_t *costs;
+    uint32_t *items;
+    ea_ws_header *hdr;
+    int B, S, Hq, Hkv, g, npairs, nB, sink, window;
+    uint32_t n_rows, n_items;
+    float scale_log2;
+};
+
+// ------------------------------------------------------------ tile sequences
+// SSA key tiles of query block qb: the sink tiles [0, n_sink) below the window,
+// then the window tiles [kb_lo, qb].  A tile is visited iff it holds at least
+// one kept (query, key) pair: a sink key (kb*T < sink), a key within the window
+// of the block's first query ((qb-kb-1)*T + 1 < window), or the diagonal.
+__device__ __forceinline__ void ssa_tiles(int qb, int sink, int window, int &n_sink, int &kb_lo)
+{
+    const int w_tiles = (window - 1 + T - 1) / T;    // ceil((window-1)/T)
+    kb_lo = qb - w_tiles > 0 ? qb - w_tiles : 0;
+    const int s_tiles = (sink + T - 1) / T;          // ceil(sink/T)
+    n_sink = s_tiles < kb_lo ? s_tiles : kb_lo;
+}
+
+// Key tile of the n-th visited tile for FULL / SSA heads.
+__device__ __forceinline__ int seq_kb(int mode, int n, int n_sink, int kb_lo)
+{
+    if (mode == EA_FULL)
+        return n;
+    return n < n_sink ? n : kb_lo + (n - n_sink);
+}
+
+// Does every (query, key) pair of tile (qb, kb) pass the head's mask?  Only
+// tiles that fail this need per-element masking.
+__device__ __forceinline__ bool tile_is_full(int mode, int qb, int kb, int sink, int window)
+{
+    if (kb >= qb)
+        return false;
+    if (mode == EA_SSA)
+        return (kb + 1) * T <= sink || (qb - kb) * T + T - 1 < window;
+    return true;
+}
+
+// ------------------------------------------------------------ planner
+// One warp per (b, KV head, q block) row: number of visited key tiles.
+__global__ void plan_costs_kernel(PrefillArgs a)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+    if (warp >= static_cast<int>(a.n_rows))
+        return;
+    const int qb = warp % a.nB;
+    const int bh = warp / a.nB;  // b * Hkv + h
+    const int mode = a.m[bh];
+    int n = 0;
+    if (mode == EA_FULL) {
+        n = qb + 1;
+    } else if (mode == EA_SSA) {
+        int n_sink, kb_lo;
+        ssa_tiles(qb, a.sink, a.window, n_sink, kb_lo);
+        n = n_sink + (qb - kb_lo + 1);
+    } else if (mode == EA_BLOCK && a.block_mask) {
+        const uint8_t *row = a.block_mask + (static_cast<int64_t>(bh) * a.nB + qb) * a.nB;
+        for (int kb = lane; kb <= qb; kb += 32)
+            n += row[kb] != 0;
+        for (int o = 16; o > 0; o >>= 1)
+            n += __shfl_xor_sync(0xffffffffu, n, o);
+    } else {
+        if (lane == 0)
+            raise_error(&a.hdr->error, EA_DEVERR_CHECK);  // bad mode, or BLOCK without a mask
+        n = 0;
+    }
+    if (lane == 0)
+        a.costs[warp] = n;
+}
+
+// One CTA: stable counting sort of the rows by visited-tile count, longest
+// first; each row contributes its npairs items back to back.  Also resets the
+// work queue head.
+__global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
+{
+    extern __shared__ int hist[];  // [nB + 2]
+    __shared__ int scan_tmp[1024];
+    const int nbins = a.nB + 1;    // costs 0..nB
+    const int tid = threadIdx.x;
+    for (int c = tid; c < nbins; c += blockDim.x)
+        hist[c] = 0;
+    __syncthreads();
+    for (uint32_t r = tid; r < a.n_rows; r += blockDim.x)
+        atomicAdd(&hist[a.costs[r]], 1);
+    __syncthreads();
+    // Exclusive scan in descending cost order: start[c] = #rows with cost > c.
+    // Bin c is visited at position nbins - 1 - c; each thread scans a segment.
+    const int per = (nbins + blockDim.x - 1) / blockDim.x;
+    const int lo = tid * per, hi = min(lo + per, nbins);
+    int local = 0;
+    for (int p = lo; p < hi; ++p)
+        local += hist[nbins - 1 - p];
+    scan_tmp[tid] = local;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        int v = tid >= off ? scan_tmp[tid - off] : 0;
+        __syncthreads();
+        scan_tmp[tid] += v;
+        __syncthreads();
+    }
+    int run = scan_tmp[tid] - local;
+    for (int p = lo; p < hi; ++p) {
+        const int c = nbins - 1 - p;
+        const int cnt = hist[c];
+        hist[c] = run;
+        run += cnt;
+    }
+    __syncthreads();
+    // Stable scatter by one warp, 32 rows at a time in row order.
+    if (tid < 32) {
+        const unsigned lt = (1u << tid) - 1u;
+        for (uint32_t base = 0; base < a.n_rows; base += 32) {
+            const uint32_t r = base + tid;
+            const bool valid = r < a.n_rows;
+            const int c = valid ? a.costs[r] : -1;
+            const unsigned active = __ballot_sync(0xffffffffu, valid);
+            const unsigned peers = __match_any_sync(0xffffffffu, c) & active;
+            int pos = 0;
+            if (valid)
+                pos = hist[c] + __popc(peers & lt);
+            __syncwarp();
+            if (valid && (peers & lt) == 0)
+                hist[c] += __popc(peers);
+            __syncwarp();
+            if (valid)
+                for (int p = 0; p < a.npairs; ++p)
+                    a.items[static_cast<uint64_t>(pos) * a.npairs + p] = r * a.npairs + p;
+        }
+    }
+    if (tid == 0) {
+        a.hdr->work_counter = 0;
+        a.hdr->drained = 0;
+        a.hdr->n_items = a.n_items;
+    }
+}
+
+// ------------------------------------------------------------ attention
+struct ItemInfo {
+    int b, h, qb, pair, row;
+};
+
+__device__ __forceinline__ ItemInfo decode_item(int item, const PrefillArgs &a)
+{
+    ItemInfo x;
+    x.pair = item % a.npairs;
+    x.row = item / a.npairs;
+    x.qb = x.row % a.nB;
+    const int bh = x.row / a.nB;
+    x.h = bh % a.Hkv;
+    x.b = bh / a.Hkv;
+    return x;
+}
+
+// Query head of tile t of an item; an odd group size pairs its last head with
+// itself (second copy computed but not stored).
+__device__ __forceinline__ int item_head(const ItemInfo &x, int t, const PrefillArgs &a, bool &store)
+{
+    const int j = 2 * x.pair + t;
+    store = j < a.g;
+    return x.h * a.g + (store ? j : 2 * x.pair);
+}
+
+// Warp-uniform generator of the kept key tiles of a BLOCK row, in ascending
+// order: each lane tests 16 mask bytes of a 512-byte window per refill.
+struct BlockScan {
+    const uint8_t *row;
+    int limit;      // qb + 1
+    int base;       // first key tile of the current window
+    int cur_lane;
+    uint32_t bits;  // remaining kept tiles of cur_lane
+    uint32_t mine;  // this lane's 16-bit mask of the current window
+
+    __device__ void refill(int lane)
+    {
+        mine = 0;
+        const int k0 = base + lane * 16;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (k0 + j < limit && row[k0 + j] != 0)
+                mine |= 1u << j;
+        cur_lane = 0;
+        bits = __shfl_sync(0xffffffffu, mine, 0);
+    }
+    __device__ void init(const uint8_t *r, int lim, int lane)
+    {
+        row = r;
+        limit = lim;
+        base = 0;
+        refill(lane);
+    }
+    // Next kept key tile, or -1.
+    __device__ int next(int lane)
+    {
+        while (true) {
+            if (bits) {
+                const int kb = base + cur_lane * 16 + (__ffs(bits) - 1);
+                bits &= bits - 1;
+                return kb;
+            }
+            if (++cur_lane < 32) {
+                bits = __shfl_sync(0xffffffffu, mine, cur_lane);
+                continue;
+            }
+            base += 512;
+            if (base >= limit)
+                return -1;
+            refill(lane);
+        }
+    }
+};
+
+__device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                              const CUtensorMap *tm_v, const PrefillArgs &a,
+                                              PrefillSmem &sm, int lane)
+{
+    uint32_t *err = &a.hdr->error;
+    uint32_t kv_it = 0, q_it = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&sm.item_empty[slot], ((it >> 1) & 1) ^ 1, &sm.abort, err))
+            break;
+        int item = -1;
+        if (lane == 0) {
+            const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
+            item = x < a.n_items ? static_cast<int>(a.items[x]) : -1;
+            // Every CTA sees the empty queue exactly once; the last one resets
+            // the head so the same plan can feed another launch.
+            if (item < 0 && atomicAdd(&a.hdr->drained, 1u) == gridDim.x - 1) {
+                a.hdr->work_counter = 0;
+                a.hdr->drained = 0;
+            }
+            sm.item[slot] = item;
+            mbar_arrive(&sm.item_full[slot]);
+        }
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item < 0)
+            break;
+        const ItemInfo x = decode_item(item, a);
+        const int N = a.costs[x.row];
+        if (N == 0)
+            continue;
+        const int mode = a.m[x.b * a.Hkv + x.h];
+        // Q tiles of both heads
+        if (!mbar_wait(&sm.q_empty, (q_it & 1) ^ 1, &sm.abort, err))
+            break;
+        ++q_it;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
+            for (int t = 0; t < 2; ++t) {
+                bool st;
+                const int qh = item_head(x, t, a, st);
+                tma_load_4d(sm.q[t], tm_q, 0, qh, x.qb * T, x.b, &sm.q_full);
+                tma_load_4d(sm.q[t] + kHalfBytes, tm_q, 64, qh, x.qb * T, x.b, &sm.q_full);
+            }
+        }
+        __syncwarp();
+        // K/V tiles in the order the MMA warp consumes them:
+        // K0, K1, V0, K2, V1, ..., K_{N-1}, V_{N-2}, V_{N-1}
+        int n_sink = 0, kb_lo = 0;
+        if (mode == EA_SSA)
+            ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
+        BlockScan scan;
+        if (mode == EA_BLOCK)
+            scan.init(a.block_mask + (static_cast<int64_t>(x.b * a.Hkv + x.h) * a.nB + x.qb) * a.nB,
+                      x.qb + 1, lane);
+        int prev_kb = -1;
+        for (int n = 0; n <= N && ok; ++n) {
+            int kb = -1;
+            if (n < N)
+                kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
+            for (int which = 0; which < 2; ++which) {
+                // which 0: K of tile n; which 1: V of tile n-1
+                const int tkb = which == 0 ? kb : prev_kb;
+                if (tkb < 0)
+                    continue;
+                const int s = kv_it % kStages;
+                if (!mbar_wait(&sm.kv_empty[s], ((kv_it / kStages) & 1) ^ 1, &sm.abort, err)) {
+                    ok = false;
+                    break;
+                }
+                ++kv_it;
+                if (lane == 0) {
+                    const CUtensorMap *tm = which == 0 ? tm_k : tm_v;
+                    mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
+                    tma_load_4d(sm.kv[s], tm, 0, x.h, tkb * T, x.b, &sm.kv_full[s]);
+                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, tkb * T, x.b, &sm.kv_full[s]);
+                    if (which == 0 && a.visited) {
+                        const uint64_t bit =
+                            (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(tkb);
+                        atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
+                    }
+                }
+                __syncwarp();
+            }
+            prev_kb = kb;
+        }
+    }
+    // Before leaving on an abort, let the copies already issued land.
+    if (sm.abort) {
+        for (uint32_t k = kv_it > kStages ? kv_it - kStages : 0; k < kv_it; ++k) {
+            volatile int no_abort = 0;
+            mbar_wait(&sm.kv_full[k % kStages], (k / kStages) & 1, &no_abort, nullptr);
+        }
+    }
+}
+
+__device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem, int lane)
+{
+    uint32_t *err = &a.hdr->error;
+    uint32_t kv_it = 0, q_it = 0;
+    uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
+    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
+    const uint32_t p_addr[2] = {smem_u32(sm.p[0]), smem_u32(sm.p[1])};
+    bool ok = true;
+
+    auto wait_kv = [&](int &s) -> bool {
+        s = kv_it % kStages;
+        if (!mbar_wait(&sm.kv_full[s], (kv_it / kStages) & 1, &sm.abort, err))
+            return false;
+        ++kv_it;
+        tc_fence_after();
+        return true;
+    };
+    auto issue_qk = [&](int sK) -> bool {
+        const uint32_t kaddr = smem_u32(sm.kv[sK]);
+        for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait(&sm.s_free[t], (s_cnt[t] & 1) ^ 1, &sm.abort, err))
+                return false;
+            ++s_cnt[t];
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                    tc_mma(tmem + t * 256, sdesc_sw128(q_addr[t] + off, 16, 1024),
+                           sdesc_sw128(kaddr + off, 16, 1024), kIdescQK, k > 0);
+                }
+                tc_commit(&sm.s_full[t]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            tc_commit(&sm.kv_empty[sK]);
+        __syncwarp();
+        return true;
+    };
+    auto issue_pv = [&](int sV, bool acc) -> bool {
+        const uint32_t vaddr = smem_u32(sm.kv[sV]);
+        for (int t = 0; t < 2; ++t) {
+            if (!mbar_wait(&sm.p_ready[t], p_cnt[t] & 1, &sm.abort, err))
+                return false;
+            ++p_cnt[t];
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < T / 16; ++k) {
+                    const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                    tc_mma(tmem + t * 256 + 128, sdesc_sw128(p_addr[t] + aoff, 16, 1024),
+                           sdesc_sw128(vaddr + k * 2048, kHalfBytes, 1024), kIdescPV,
+                           (acc || k > 0) ? 1u : 0u);
+                }
+                tc_commit(&sm.o_done[t]);
+            }
+            __syncwarp();
+        }
+        if (lane == 0)
+            tc_commit(&sm.kv_empty[sV]);
+        __syncwarp();
+        return true;
+    };
+
+    for (int it = 0; ok; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it >> 1) & 1, &sm.abort, err))
+            break;
+        const int item = sm.item[slot];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.item_empty[slot]);
+        if (item < 0)
+            break;
+        const ItemInfo x = decode_item(item, a);
+        const int N = a.costs[x.row];
+        if (N == 0)
+            continue;
+        if (!mbar_wait(&sm.q_full, q_it & 1, &sm.abort, err))
+            break;
+        ++q_it;
+        tc_fence_after();
+        int sK, sV;
+        if (!wait_kv(sK) || !issue_qk(sK)) {
+            ok = false;
+            break;
+        }
+        if (N == 1 && lane == 0)
+            tc_commit(&sm.q_empty);
+        for (int n = 0; n < N && ok; ++n) {
+            if (n + 1 < N) {
+                if (!wait_kv(sK) || !issue_qk(sK)) {
+                    ok = false;
+                    break;
+                }
+                if (n + 2 == N && lane == 0)
+                    tc_commit(&sm.q_empty);
+            }
+            if (!wait_kv(sV) || !issue_pv(sV, n > 0)) {
+                ok = false;
+                break;
+            }
+        }
+        __syncwarp();
+    }
+    // All MMAs must have completed before TMEM is released.
+    if (lane == 0)
+        tc_commit(&sm.teardown);
+    __syncwarp();
+    volatile int no_abort = 0;
+    mbar_wait(&sm.teardown, 0, &no_abort, err);
+}
+
+__device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem,
+                                             int warp)
+{
+    uint32_t *err = &a.hdr->error;
+    const int t = warp >> 2;                    // head of the pair handled by this warpgroup
+    const int r = threadIdx.x & 127;            // query row within the 128-row tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 256;
+    const uint32_t tO = tS + 128;
+    uint8_t *pbuf = sm.p[t];
+    uint32_t s_cnt = 0, o_cnt = 0;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&sm.item_full[slot], (it >> 1) & 1, &sm.abort, err))
+            break;
+        const int item = sm.item[slot];
+        mbar_arrive(&sm.item_empty[slot]);
+        if (item < 0)
+            break;
+        const ItemInfo x = decode_item(item, a);
+        bool store;
+        const int qh = item_head(x, t, a, store);
+        const int N = a.costs[x.row];
+        const int mode = a.m[x.b * a.Hkv + x.h];
+        int n_sink = 0, kb_lo = 0;
+        if (mode == EA_SSA)
+            ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
+        bool diag_kept = false;
+        if (mode == EA_BLOCK && N > 0)
+            diag_kept = a.block_mask[(static_cast<int64_t>(x.b * a.Hkv + x.h) * a.nB + x.qb) * a.nB +
+                                     x.qb] != 0;
+        const int i = x.qb * T + r;
+        float m_run = NEG_INF, l_run = 0.f;
+        bool ok = true;
+
+        for (int n = 0; n < N; ++n) {
+            int kb;
+            if (mode == EA_BLOCK)
+                kb = (n == N - 1 && diag_kept) ? x.qb : -1;  // only the diagonal needs its index
+            else
+                kb = seq_kb(mode, n, n_sink, kb_lo);
+            if (!mbar_wait(&sm.s_full[t], s_cnt & 1, &sm.abort, err)) {
+                ok = false;
+                break;
+            }
+            ++s_cnt;
+            tc_fence_after();
+            uint32_t s[128];
+            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&sm.s_free[t]);
+
+            // mask edge tiles only
+            const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
+            if (edge) {
+                const int j0 = kb * T;
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int j = j0 + c;
+                    const bool keep =
+                        j <= i && (mode != EA_SSA || j < a.sink || i - j < a.window);
+                    if (!keep)
+                        s[c] = __float_as_uint(NEG_INF);
+                }
+            }
+            float mx = NEG_INF;
+#pragma unroll
+            for (int c = 0; c < 128; ++c)
+                mx = fmaxf(mx, __uint_as_float(s[c]));
+            mx *= a.scale_log2;
+            const float m_new = fmaxf(m_run, mx);
+            float factor = 1.f;
+            bool rescale_o = false;
+            if (m_new > m_run + kRescaleThreshold) {
+                if (m_run > NEG_INF) {
+                    factor = ex2(m_run - m_new);
+                    l_run *= factor;
+                    rescale_o = n > 0;
+                }
+                m_run = m_new;
+            }
+            const float mb = m_run > NEG_INF ? m_run : 0.f;
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const float p = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mb));
+                lsum += p;
+                s[c] = __float_as_uint(p);
+            }
+            l_run += lsum;
+
+            // PV of the previous tile must be done before O is rescaled and
+            // before the P buffer is overwritten.
+            if (n > 0) {
+                if (!mbar_wait(&sm.o_done[t], o_cnt & 1, &sm.abort, err)) {
+                    ok = false;
+                    break;
+                }
+                ++o_cnt;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, rescale_o)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + ch * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
+                        tmem_st32(tO + ch * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P (bf16) -> shared memory, 128-byte swizzled K-major layout
+#pragma unroll
+            for (int c16 = 0; c16 < 16; ++c16) {
+                const int half = c16 >> 3, cc = c16 & 7;
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(s[c16 * 8 + 0]), __uint_as_float(s[c16 * 8 + 1]));
+                v.y = pack_bf16x2(__uint_as_float(s[c16 * 8 + 2]), __uint_as_float(s[c16 * 8 + 3]));
+                v.z = pack_bf16x2(__uint_as_float(s[c16 * 8 + 4]), __uint_as_float(s[c16 * 8 + 5]));
+                v.w = pack_bf16x2(__uint_as_float(s[c16 * 8 + 6]), __uint_as_float(s[c16 * 8 + 7]));
+                *reinterpret_cast<uint4 *>(pbuf + half * kHalfBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&sm.p_ready[t]);
+        }
+        if (!ok)
+            break;
+
+        // epilogue: O / l -> bf16, LSE = ln(2^m * l)
+        if (N > 0) {
+            if (!mbar_wait(&sm.o_done[t], o_cnt & 1, &sm.abort, err))
+                break;
+            ++o_cnt;
+            tc_fence_after();
+        }
+        const bool row_ok = store && i < a.S;
+        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        __nv_bfloat16 *orow = a.O + x.b * a.o_sb + static_cast<int64_t>(i) * a.o_ss + qh * a.o_sh;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t o[32];
+            if (N > 0) {
+                tmem_ld32(tO + ch * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    o[c] = 0u;
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
+                    v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
+                    v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
+                    v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
+                    *reinterpret_cast<uint4 *>(orow + ch * 32 + q4 * 8) = v;
+                }
+            }
+        }
+        if (row_ok && a.LSE)
+            a.LSE[(static_cast<int64_t>(x.b) * a.Hq + qh) * a.S + i] =
+                l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
+        tc_fence_before();
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    hybrid_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.kv_full[s], 1);
+            mbar_init(&sm.kv_empty[s], 1);
+        }
+        mbar_init(&sm.q_full, 1);
+        mbar_init(&sm.q_empty, 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.s_free[t], 128);
+            mbar_init(&sm.p_ready[t], 128);
+            mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.item_full[t], 1);
+            mbar_init(&sm.item_empty[t], 1 + 256);
+        }
+        mbar_init(&sm.teardown, 1);
+        sm.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sm.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+
+    if (warp == kProducerWarp)
+        producer_role(&tm_q, &tm_k, &tm_v, a, sm, lane);
+    else if (warp == kMmaWarp)
+        mma_role(a, sm, tmem, lane);
+    else
+        softmax_role(a, sm, tmem, warp);
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+} // namespace ea
+
+using namespace ea;
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by the planner and the attention launch; fills the kernel
+// arguments that do not depend on the tensors.
+static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint8_t *m, int sink,
+                                int window, const uint8_t *block_mask, int block_size,
+                                void *workspace, size_t ws_bytes, PrefillArgs &a)
+{
+    if (!m)
+        return EA_ERR_INVALID_ARG;
+    if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || sink < 0 || window < 1 ||
+        block_size != EA_TILE)
+        return EA_ERR_INVALID_ARG;
+    if (d != EA_HEAD_DIM || S > EA_MAX_SEQ || B > 65535)
+        return EA_ERR_UNSUPPORTED;
+    const PrefillWs L = prefill_ws_layout(B, S, Hq, Hkv);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < L.total)
+        return EA_ERR_WORKSPACE;
+    const int64_t nB = ceil_div(S, T);
+    const int64_t n_rows = static_cast<int64_t>(B) * Hkv * nB;
+    const int g = Hq / Hkv;
+    const int npairs = (g + 1) / 2;
+    if (n_rows * npairs >= (int64_t(1) << 31))
+        return EA_ERR_UNSUPPORTED;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a = PrefillArgs{};
+    a.m = m;
+    a.block_mask = block_mask;
+    a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
+    a.items = reinterpret_cast<uint32_t *>(ws + L.items);
+    a.hdr = reinterpret_cast<ea_ws_header *>(ws);
+    a.B = B;
+    a.S = S;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.npairs = npairs;
+    a.nB = static_cast<int>(nB);
+    a.sink = sink < S ? sink : S;        // sink or window beyond S keep the same pairs
+    a.window = window < S ? window : S;
+    a.n_rows = static_cast<uint32_t>(n_rows);
+    a.n_items = static_cast<uint32_t>(n_rows * npairs);
+    return EA_OK;
+}
+
+static bool g_attr_done[64] = {};
+
+static ea_status ensure_attributes()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return EA_ERR_CUDA;
+    if (dev < 64 && g_attr_done[dev])
+        return EA_OK;
+    if (cudaFuncSetAttribute(hybrid_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPrefillSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(int) * (EA_MAX_SEQ / T + 2))) != cudaSuccess)
+        return EA_ERR_CUDA;
+    if (dev < 64)
+        g_attr_done[dev] = true;
+    return EA_OK;
+}
+
+extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
+                                     int sink, int window, const uint8_t *block_mask,
+                                     int block_size, void *workspace, size_t ws_bytes, void *stream)
+{
+    PrefillArgs a;
+    ea_status s = prefill_common(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size,
+                                 workspace, ws_bytes, a);
+    if (s != EA_OK)
+        return s;
+    if ((s = ensure_attributes()) != EA_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int warps_per_cta = 8;
+    const unsigned cost_blocks = static_cast<unsigned>(ceil_div(a.n_rows, warps_per_cta));
+    plan_costs_kernel<<<cost_blocks, warps_per_cta * 32, 0, st>>>(a);
+    plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O,
+                                       float *LSE, const int64_t q_str[4], const int64_t kv_str[4],
+                                       const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                                       float scale, const uint8_t *m, int sink, int window,
+                                       const uint8_t *block_mask, int block_size, void *workspace,
+                                       size_t ws_bytes, uint32_t *visited_bitmap, void *stream)
+{
+    if (!Q || !K || !V || !O || !q_str || !kv_str || !o_str || !(scale > 0.f))
+        return EA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    ea_status s = prefill_common(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size,
+                                 workspace, ws_bytes, a);
+    if (s != EA_OK)
+        return s;
+    if (q_str[3] != 1 || kv_str[3] != 1 || o_str[3] != 1)
+        return EA_ERR_INVALID_ARG;
+    for (int k = 0; k < 3; ++k)
+        if (q_str[k] <= 0 || kv_str[k] <= 0 || o_str[k] <= 0 || q_str[k] % 8 || kv_str[k] % 8 ||
+            o_str[k] % 8)
+            return EA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return EA_ERR_INVALID_ARG;
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, S, B, q_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tk, K, d, Hkv, S, B, kv_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tv, V, d, Hkv, S, B, kv_str, 64, T, true))
+        return EA_ERR_INVALID_ARG;
+    a.O = static_cast<__nv_bfloat16 *>(O);
+    a.o_sb = o_str[0];
+    a.o_ss = o_str[1];
+    a.o_sh = o_str[2];
+    a.LSE = LSE;
+    a.visited = visited_bitmap;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if ((s = ensure_attributes()) != EA_OK)
+        return s;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return EA_ERR_CUDA;
+    const int sms = num_sms(dev);
+    if (sms <= 0)
+        return EA_ERR_CUDA;
+    const unsigned grid =
+        static_cast<unsigned>(a.n_items < static_cast<uint32_t>(sms) ? a.n_items : sms);
+    hybrid_prefill_kernel<<<grid, kThreads, kPrefillSmemBytes, static_cast<cudaStream_t>(stream)>>>(
+        tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, void *O,
+                                            float *LSE, const int64_t q_str[4],
+                                            const int64_t kv_str[4], const int64_t o_str[4], int B,
+                                            int S, int Hq, int Hkv, int d, float scale,
+                                            const uint8_t *m, int sink, int window,
+                                            const uint8_t *block_mask, int block_size,
+                                            void *workspace, size_t ws_bytes,
+                                            uint32_t *visited_bitmap, void *stream)
+{
+    // Validate everything (tensors included) before enqueueing the planner.
+    if (!Q || !K || !V || !O || !q_str || !kv_str || !o_str || !(scale > 0.f))
+        return EA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    ea_status s = prefill_common(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size,
+                                 workspace, ws_bytes, a);
+    if (s != EA_OK)
+        return s;
+    if (q_str[3] != 1 || kv_str[3] != 1 || o_str[3] != 1)
+        return EA_ERR_INVALID_ARG;
+    for (int k = 0; k < 3; ++k)
+        if (q_str[k] <= 0 || kv_str[k] <= 0 || o_str[k] <= 0 || q_str[k] % 8 || kv_str[k] % 8 ||
+            o_str[k] % 8)
+            return EA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return EA_ERR_INVALID_ARG;
+    s = ea_prefill_plan(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size, workspace,
+                        ws_bytes, stream);
+    if (s != EA_OK)
+        return s;
+    return ea_prefill_attend(Q, K, V, O, LSE, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale, m,
+                             sink, window, block_mask, block_size, workspace, ws_bytes,
+                             visited_bitmap, stream);
+}

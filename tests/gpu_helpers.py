@@ -1,0 +1,62 @@
+"""Shared helpers of the GPU parity tests (imported by tests/test_*_gpu.py)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import build as ea_build
+
+# Tolerances: bf16 output max abs error 1e-2, LSE abs error 1e-3 (fp32 vs fp64).
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def gpu_device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ea_build.build()
+    oracle.lib()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def assert_close(O, LSE, Oref, Lref, what=""):
+    """O: bf16/float array vs float64 reference; LSE: -inf must match -inf."""
+    O = np.asarray(O, dtype=np.float64)
+    LSE = np.asarray(LSE, dtype=np.float64)
+    assert O.shape == Oref.shape, (O.shape, Oref.shape)
+    assert np.isfinite(O).all(), what + ": non-finite output"
+    err_o = np.abs(O - Oref).max() if O.size else 0.0
+    ninf = np.isneginf(Lref)
+    assert (np.isneginf(LSE) == ninf).all(), what + ": -inf LSE pattern differs"
+    err_l = np.abs(LSE[~ninf] - Lref[~ninf]).max() if (~ninf).any() else 0.0
+    assert err_o <= O_TOL, "%s: max |O - oracle| = %g" % (what, err_o)
+    assert err_l <= LSE_TOL, "%s: max |LSE - oracle| = %g" % (what, err_l)
+    return err_o, err_l
+
+
+def check_no_device_error(ws):
+    st = ea.ea_check_errors(ws)
+    assert st == 0, "device error word: status %d" % st
+
+
+def bitmap_to_tiles(bitmap, B, Hkv, nB):
+    """Unpack the visited-tile bitmap (uint32 words) to uint8 [B, Hkv, nB, nB]."""
+    words = bitmap.cpu().numpy().view(np.uint32)
+    bits = np.unpackbits(words.view(np.uint8), bitorder="little")
+    return bits[: B * Hkv * nB * nB].reshape(B, Hkv, nB, nB)
+
+
+def sample_rows(S, sink, window, T=128, block_mask_row0=None, n_random=128, seed=0, edge=128):
+    """Deterministic query-row sample of a long sequence: the first and last
+    `edge` rows, rows around the sink / window / sink+window boundaries (and
+    their tile edges), and seeded random rows."""
+    rows = set(range(min(edge, S))) | set(range(max(0, S - edge), S))
+    for x in (sink, window, sink + window, T, 2 * T):
+        for t in (x - 1, x, x + 1, (x // T) * T, (x // T) * T + T - 1):
+            if 0 <= t < S:
+                rows.add(t)
+    g = np.random.default_rng(seed)
+    rows |= set(int(v) for v in g.integers(0, S, size=n_random))
+    return np.array(sorted(rows), dtype=np.int64)

@@ -1,0 +1,189 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads and exports
+every entry point include/ea.h declares, argument validation rejects bad calls
+before anything is enqueued, workspace sizing, and the host-only sparsity
+ratios, which must equal the oracle's bit for bit."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import build as ea_build
+from sparse_head_attention_gb300 import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    ea_build.build()
+    return ea.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "ea.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ea_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    names = _declared_functions()
+    assert set(names) == set(ea.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = L.ea_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert L.ea_status_string(0) == b"ok"
+
+
+def test_workspace_sizes(L):
+    assert L.ea_prefill_workspace_size(1, 1024, 8, 2, 128) > 256
+    assert L.ea_prefill_workspace_size(1, 1024, 8, 2, 64) == 0       # head dim 128 only
+    assert L.ea_prefill_workspace_size(1, 1024, 8, 3, 128) == 0      # Hq % Hkv != 0
+    assert L.ea_prefill_workspace_size(0, 1024, 8, 2, 128) == 0
+    assert L.ea_decode_workspace_size(32, 32, 8, 128, 131072, 0) > 256
+    assert L.ea_decode_workspace_size(32, 32, 8, 128, 131072, 2000) == 0
+    # bigger problems never need less
+    assert L.ea_prefill_workspace_size(1, 32768, 32, 8, 128) > L.ea_prefill_workspace_size(1, 1024, 32, 8, 128)
+
+
+def _fake(n=0x1000):
+    return ctypes.c_void_p(n)
+
+
+def _str(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+def _prefill(L, **kw):
+    a = dict(Q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None,
+             qs=_str(8 * 1024 * 128, 8 * 128, 128, 1), kvs=_str(2 * 1024 * 128, 2 * 128, 128, 1),
+             os_=_str(8 * 1024 * 128, 8 * 128, 128, 1), B=1, S=1024, Hq=8, Hkv=2, d=128, scale=0.088,
+             m=_fake(), sink=64, window=256, bm=None, bs=128, ws=_fake(0x100000), wsb=1 << 30,
+             vis=None, stream=None)
+    a.update(kw)
+    return L.ea_hybrid_attn_prefill(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["qs"], a["kvs"], a["os_"],
+                                    a["B"], a["S"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["m"],
+                                    a["sink"], a["window"], a["bm"], a["bs"], a["ws"], a["wsb"],
+                                    a["vis"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Q=None), 1), (dict(m=None), 1), (dict(B=0), 1), (dict(Hkv=3), 1), (dict(window=0), 1),
+    (dict(sink=-1), 1), (dict(scale=0.0), 1), (dict(bs=64), 1), (dict(d=64), 2),
+    (dict(S=(1 << 21) + 1), 2), (dict(qs=_str(8 * 1024 * 128, 8 * 128, 128, 2)), 1),
+    (dict(kvs=_str(2 * 1024 * 128, 2 * 128, 100, 1)), 1), (dict(Q=_fake(0x1008)), 1),
+    (dict(ws=None), 3), (dict(ws=_fake(0x100010)), 3), (dict(wsb=16), 3),
+])
+def test_prefill_rejects_bad_arguments_on_host(L, kw, expect):
+    assert _prefill(L, **kw) == expect
+
+
+def _decode(L, **kw):
+    a = dict(q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None, qs=_str(32 * 128, 128, 1),
+             kvs=_str(4096 * 8 * 128, 8 * 128, 128, 1), os_=_str(32 * 128, 128, 1), sl=_fake(),
+             B=4, Hq=32, Hkv=8, d=128, Lmax=4096, scale=0.088, m=_fake(), sink=128, window=4096,
+             ns=0, ws=_fake(0x100000), wsb=1 << 30, stream=None)
+    a.update(kw)
+    return L.ea_hybrid_attn_decode(a["q"], a["K"], a["V"], a["O"], a["LSE"], a["qs"], a["kvs"], a["os_"],
+                                   a["sl"], a["B"], a["Hq"], a["Hkv"], a["d"], a["Lmax"], a["scale"], a["m"],
+                                   a["sink"], a["window"], a["ns"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(sl=None), 1), (dict(Hq=30), 1), (dict(ns=-1), 1), (dict(ns=1025), 1),
+    (dict(window=0), 1), (dict(Hkv=2), 2), (dict(d=96), 2), (dict(kvs=_str(4096 * 8 * 128, 8 * 128, 128, 2)), 1),
+    (dict(ws=None), 3), (dict(wsb=1024), 3),
+])
+def test_decode_rejects_bad_arguments_on_host(L, kw, expect):
+    assert _decode(L, **kw) == expect
+
+
+def test_route_rejects_bad_mlp(L):
+    dims = (ctypes.c_int * 3)(128, 64, 3)          # last layer must have 2 outputs
+    W = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    b = (ctypes.c_void_p * 2)(0x3000, 0x4000)
+    mlp = ea._Mlp(2, dims, W, b)
+    st = L.ea_route(_fake(), _str(65536 * 8 * 128, 8 * 128, 128, 1), 1, 65536, 8, 128, 100, 100,
+                    ctypes.byref(mlp), ea._Policy(0, 1), _fake(), _fake(), None, None)
+    assert st == 1
+    mlp5 = ea._Mlp(5, dims, W, b)
+    st = L.ea_route(_fake(), _str(65536 * 8 * 128, 8 * 128, 128, 1), 1, 65536, 8, 128, 100, 100,
+                    ctypes.byref(mlp5), ea._Policy(0, 1), _fake(), _fake(), None, None)
+    assert st == 2
+
+
+# ---------------------------------------------------------------- ratios
+def test_sparsity_ratios_equal_oracle_on_hand_cases(L):
+    import json
+    cases = json.load(open(os.path.join(ROOT, "tests", "golden", "sparsity_ratio_hand_examples.json")))
+    for c in cases["cases"]:
+        if c["T"] != 128:
+            continue  # the library's block size is fixed at 128
+        msr, esr = ea.ea_sparsity_ratios(np.array(c["r"], np.uint8), np.array(c["m"], np.uint8), c["S"],
+                                         sink=c["sink"], window=c["window"])
+        assert msr == c["msr"]
+        assert esr == c["esr_num"] / c["esr_den"]
+
+
+@pytest.mark.parametrize("S,sink,window", [(1000, 64, 256), (257, 0, 1), (1300, 200, 129), (129, 128, 1)])
+def test_sparsity_ratios_bit_exact_vs_oracle(L, S, sink, window):
+    Lyr, Hkv = 3, 4
+    g = torch.Generator().manual_seed(S)
+    r = (torch.rand(Lyr, Hkv, generator=g) < 0.6).to(torch.uint8).numpy()
+    pol = np.array([[ea.FULL, ea.SSA], [ea.BLOCK, ea.SSA]], np.uint8)
+    m = np.where(r == 1, ea.SSA, np.where(np.arange(Hkv)[None, :] % 2 == 0, ea.FULL, ea.BLOCK)).astype(np.uint8)
+    bms = wl.block_mask(Lyr, Hkv, S, density=0.3, seed=S).numpy()           # [L, Hkv, nB, nB]
+    bms[0, 1, -1, -1] = 0
+    msr_o, esr_o, _ = oracle.sparsity_ratios(r, m, S, sink=sink, window=window, block_masks=bms)
+    msr, esr = ea.ea_sparsity_ratios(r, m, S, sink=sink, window=window, block_masks=list(bms))
+    assert msr == msr_o
+    assert esr == esr_o
+
+
+def test_sparsity_ratios_at_256k_match_closed_forms(L):
+    # XA-SSA 256K workload: 2 BLOCK heads (r = 0) and 6 SSA heads (sink 128, window 4096).
+    cfg = wl.XA_SSA_256K
+    S, T = cfg.S, 128
+    r, m = wl.routing_from_sa_heads(1, cfg.Hkv, cfg.sa_heads, fa_impl=ea.BLOCK, sa_impl=ea.SSA)
+    bm = wl.block_mask(1, cfg.Hkv, S, density=cfg.block_density, seed=cfg.seed).numpy()[0]
+    msr, esr = ea.ea_sparsity_ratios(r.numpy(), m.numpy(), S, sink=cfg.sink, window=cfg.window,
+                                     block_masks=[bm])
+    assert msr == 0.75
+    causal = S * (S + 1) // 2
+    i = np.arange(S, dtype=np.int64)
+    ssa_kept = int((np.minimum(i + 1, cfg.window) +
+                    np.maximum(0, np.minimum(cfg.sink, i + 1 - cfg.window))).sum())
+    pruned = 0
+    for h in range(cfg.Hkv):
+        if m[0, h] == ea.SSA:
+            pruned += causal - ssa_kept
+        else:
+            # rows of query block qb keep 128 keys per kept block below the diagonal
+            # plus (t + 1) keys of the diagonal block for row t
+            nB = S // T
+            below = np.tril(bm[h], -1).sum(axis=1).astype(np.int64)
+            kept = int((below * T * T).sum()) + int(bm[h].diagonal().sum()) * (T * (T + 1) // 2)
+            pruned += causal - kept
+    assert esr == pruned / (1 * cfg.Hkv * causal)
+    assert 0.9 < esr < 0.96
+
+
+def test_device_entry_points_fail_loudly_without_gpu():
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    Q = torch.zeros(1, 128, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ea.ea_hybrid_attn_prefill(Q, Q[:, :, :2], Q[:, :, :2], torch.zeros(1, 2, dtype=torch.uint8),
+                                  sink=0, window=1)

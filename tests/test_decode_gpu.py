@@ -1,0 +1,93 @@
+"""Parity of the split-KV hybrid decode (CUDA, through the C ABI) with the fp64
+oracle, split-count invariance, edge cases, and the full B=32 / 128K workload
+on sampled sequences."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import workloads as wl
+from gpu_helpers import assert_close, check_no_device_error, gpu_device
+
+pytestmark = pytest.mark.gpu
+FULL, SSA, BLOCK = ea.FULL, ea.SSA, ea.BLOCK
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return gpu_device()
+
+
+def run(dev, q, Kc, Vc, sl, modes, sink, window, num_splits=0):
+    B, Hq, _ = q.shape
+    Lmax, Hkv = Kc.shape[1], Kc.shape[2]
+    ws = ea.decode_workspace(B, Hq, Hkv, Lmax, num_splits, device=dev)
+    O, LSE = ea.ea_hybrid_attn_decode(q.to(dev), Kc.to(dev), Vc.to(dev), sl.to(dev),
+                                      torch.as_tensor(modes, dtype=torch.uint8).to(dev),
+                                      sink=sink, window=window, num_splits=num_splits, workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    return O, LSE
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 7, 64])
+def test_small_batch_all_heads(dev, num_splits):
+    cfg = wl.DecodeConfig("t", B=4, Hq=8, Hkv=2, d=128, L=5000, sink=128, window=1000)
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=[5000, 1, 4097, 1129])
+    modes = np.array([[FULL, SSA], [SSA, FULL], [SSA, SSA], [FULL, FULL]], np.uint8)
+    O, LSE = run(dev, q, Kc, Vc, sl, modes, cfg.sink, cfg.window, num_splits)
+    Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=cfg.sink, window=cfg.window)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "splits=%d" % num_splits)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (16, 2), (6, 2), (12, 4)])
+def test_group_sizes(dev, Hq, Hkv):
+    cfg = wl.DecodeConfig("t", B=2, Hq=Hq, Hkv=Hkv, d=128, L=3000, sink=7, window=333)
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=[3000, 2049])
+    modes = np.where(np.arange(Hkv)[None, :] % 2 == 0, FULL, SSA).repeat(2, 0).astype(np.uint8)
+    O, LSE = run(dev, q, Kc, Vc, sl, modes, cfg.sink, cfg.window)
+    Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=cfg.sink, window=cfg.window)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "g=%d" % (Hq // Hkv))
+
+
+def test_empty_sequence_and_block_rejection(dev):
+    cfg = wl.DecodeConfig("t", B=2, Hq=8, Hkv=2, d=128, L=256, sink=4, window=16)
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=[0, 256])
+    O, LSE = run(dev, q, Kc, Vc, sl, [[FULL, SSA], [FULL, SSA]], cfg.sink, cfg.window)
+    assert (O[0].float() == 0).all()
+    assert torch.isneginf(LSE[0]).all()
+    ws = ea.decode_workspace(2, 8, 2, 256, device=dev)
+    ea.ea_hybrid_attn_decode(q.to(dev), Kc.to(dev), Vc.to(dev), sl.to(dev),
+                             torch.tensor([[BLOCK, SSA], [FULL, SSA]], dtype=torch.uint8, device=dev),
+                             sink=4, window=16, workspace=ws)
+    assert ea.ea_check_errors(ws) == 6
+
+
+def test_decode_equals_last_prefill_row_on_gpu(dev):
+    B, S, Hq, Hkv, sink, window = 1, 1500, 8, 2, 64, 300
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=12)
+    modes = torch.tensor([[FULL, SSA]], dtype=torch.uint8, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Q.to(dev), K.to(dev), V.to(dev), modes, sink=sink, window=window)
+    Od, Ld = ea.ea_hybrid_attn_decode(Q[:, S - 1].contiguous().to(dev), K.to(dev), V.to(dev),
+                                      torch.tensor([S], dtype=torch.int32, device=dev), modes,
+                                      sink=sink, window=window)
+    torch.cuda.synchronize()
+    assert (Od[0].float() - O[0, S - 1].float()).abs().max().item() <= 1.6e-2
+    assert (Ld[0] - LSE[0, :, S - 1]).abs().max().item() <= 1e-3
+
+
+def test_full_workload_sampled_sequences(dev):
+    cfg = wl.DECODE_128K
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev)
+    _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
+    ws = ea.decode_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.L, device=dev)
+    O, LSE = ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m.to(dev), sink=cfg.sink, window=cfg.window,
+                                      workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    for b in (0, 13, cfg.B - 1):
+        Oref, Lref = oracle.decode(q[b:b + 1].cpu(), Kc[b:b + 1].cpu(), Vc[b:b + 1].cpu(),
+                                   sl[b:b + 1].cpu(), m[b:b + 1], sink=cfg.sink, window=cfg.window)
+        assert_close(O[b:b + 1].float().cpu().numpy(), LSE[b:b + 1].cpu().numpy(), Oref, Lref,
+                     "b=%d" % b)

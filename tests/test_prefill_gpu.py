@@ -1,0 +1,181 @@
+"""Parity of the fused hybrid-head prefill (CUDA, through the C ABI) with the
+fp64 oracle: element by element on small and ragged shapes, on sampled rows at
+the full workload sizes, bit-exact visited-tile sets, and the device checks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import workloads as wl
+from gpu_helpers import (assert_close, bitmap_to_tiles, check_no_device_error, gpu_device,
+                         sample_rows)
+
+pytestmark = pytest.mark.gpu
+FULL, SSA, BLOCK = ea.FULL, ea.SSA, ea.BLOCK
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return gpu_device()
+
+
+def run(dev, Q, K, V, modes, sink, window, bm=None, visited=False, **kw):
+    B, S, Hq, _ = Q.shape
+    Hkv = K.shape[2]
+    nB = (S + 127) // 128
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    vis = None
+    if visited:
+        vis = torch.zeros((B * Hkv * nB * nB + 31) // 32, dtype=torch.int32, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Q.to(dev), K.to(dev), V.to(dev),
+                                       torch.as_tensor(modes, dtype=torch.uint8).to(dev),
+                                       sink=sink, window=window,
+                                       block_mask=None if bm is None else torch.as_tensor(bm).to(dev),
+                                       workspace=ws, visited_bitmap=vis, **kw)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    return O, LSE, vis
+
+
+def test_tiny_workload_all_rows(dev):
+    cfg = wl.TINY
+    Q, K, V = wl.qkv(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.d, seed=cfg.seed)
+    _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
+    O, LSE, vis = run(dev, Q, K, V, m, cfg.sink, cfg.window, visited=True)
+    Oref, Lref = oracle.prefill_full(Q, K, V, m, sink=cfg.sink, window=cfg.window)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "tiny")
+    nB = cfg.S // 128
+    tiles = bitmap_to_tiles(vis, cfg.B, cfg.Hkv, nB)
+    ref = oracle.visited(cfg.B, cfg.S, cfg.Hkv, m, sink=cfg.sink, window=cfg.window)
+    np.testing.assert_array_equal(tiles, ref)
+    assert tiles[0, 0].sum() == 36 and tiles[0, 1].sum() == 26   # FA / SSA tiles per head
+
+
+SHAPES = [
+    # B, S, Hq, Hkv, modes, sink, window
+    (3, 129, 8, 2, [[FULL, SSA], [SSA, FULL], [SSA, SSA]], 5, 17),
+    (1, 1000, 4, 1, [[SSA]], 0, 1),
+    (1, 1, 8, 2, [[FULL, SSA]], 64, 256),
+    (2, 300, 6, 2, [[FULL, SSA], [SSA, FULL]], 100, 3),          # odd group size 3
+    (1, 513, 4, 4, [[FULL, SSA, FULL, SSA]], 130, 129),          # one query head per KV head
+    (1, 700, 8, 2, [[SSA, SSA]], 2000, 1),                       # sink covers everything
+    (1, 640, 8, 2, [[SSA, FULL]], 128, 128),                     # tile-aligned sink / window
+]
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,modes,sink,window", SHAPES)
+def test_ragged_shapes_all_rows(dev, B, S, Hq, Hkv, modes, sink, window):
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=S + Hq)
+    O, LSE, vis = run(dev, Q, K, V, modes, sink, window, visited=True)
+    Oref, Lref = oracle.prefill_full(Q, K, V, np.array(modes, np.uint8), sink=sink, window=window)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "S=%d" % S)
+    nB = (S + 127) // 128
+    tiles = bitmap_to_tiles(vis, B, Hkv, nB)
+    np.testing.assert_array_equal(tiles, oracle.visited(B, S, Hkv, np.array(modes, np.uint8),
+                                                        sink=sink, window=window))
+
+
+def test_block_masks_with_empty_rows(dev):
+    B, S, Hq, Hkv = 2, 1000, 12, 3
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=5)
+    bm = wl.block_mask(B, Hkv, S, density=0.3, seed=9).numpy()
+    bm[0, 0, 3, :] = 0                   # query block 3 of (b0, h0) keeps nothing
+    bm[1, 2, 5, 5] = 0                   # diagonal dropped
+    bm[1, 1] = np.tril(np.ones_like(bm[1, 1]))   # all kept: equals FA
+    modes = [[BLOCK, SSA, BLOCK], [FULL, BLOCK, BLOCK]]
+    O, LSE, vis = run(dev, Q, K, V, modes, 64, 300, bm=bm, visited=True)
+    Oref, Lref = oracle.prefill_full(Q, K, V, np.array(modes, np.uint8), sink=64, window=300,
+                                     block_mask=bm)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "block")
+    assert np.isneginf(LSE[0, 0, 3 * 128:4 * 128].cpu().numpy()).all()
+    assert (O[0, 3 * 128:4 * 128, 0:4].float().cpu().numpy() == 0).all()
+    nB = (S + 127) // 128
+    np.testing.assert_array_equal(
+        bitmap_to_tiles(vis, B, Hkv, nB),
+        oracle.visited(B, S, Hkv, np.array(modes, np.uint8), sink=64, window=300, block_mask=bm))
+
+
+def test_strided_views_and_concatenation(dev):
+    # Q, K, V as views of one packed projection [B, S, Hq + 2 Hkv, d]; O written
+    # into the first Hq heads of a wider buffer (eq. 3 concatenation in place).
+    B, S, Hq, Hkv, d = 2, 333, 8, 2, 128
+    packed = wl.randn_bf16((B, S, Hq + 2 * Hkv, d), seed=77)
+    Q, K, V = packed[:, :, :Hq], packed[:, :, Hq:Hq + Hkv], packed[:, :, Hq + Hkv:]
+    modes = np.array([[SSA, FULL], [FULL, SSA]], np.uint8)
+    pg = packed.to(dev)
+    Ob = torch.full((B, S, Hq + 8, d), 7.0, dtype=torch.bfloat16, device=dev)
+    Oview = Ob[:, :, :Hq]
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    ea.ea_hybrid_attn_prefill(pg[:, :, :Hq], pg[:, :, Hq:Hq + Hkv], pg[:, :, Hq + Hkv:],
+                              torch.as_tensor(modes).to(dev), sink=3, window=50, O=Oview,
+                              workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Oref, _ = oracle.prefill_full(Q, K, V, modes, sink=3, window=50)
+    err = np.abs(Oview.float().cpu().numpy() - Oref).max()
+    assert err <= 1e-2, err
+    assert (Ob[:, :, Hq:].float() == 7.0).all()       # neighbours untouched
+
+
+def test_repeated_calls_are_bitwise_identical(dev):
+    B, S, Hq, Hkv = 1, 2000, 8, 2
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=3)
+    O1, L1, _ = run(dev, Q, K, V, [[FULL, SSA]], 64, 256)
+    O2, L2, _ = run(dev, Q, K, V, [[FULL, SSA]], 64, 256)
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+def test_device_checks_report_bad_modes_and_missing_masks(dev):
+    B, S, Hq, Hkv = 1, 256, 4, 2
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=1)
+    for modes in ([[FULL, 7]], [[BLOCK, SSA]]):       # unknown mode; BLOCK without a mask
+        ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+        ea.ea_hybrid_attn_prefill(Q.to(dev), K.to(dev), V.to(dev),
+                                  torch.tensor(modes, dtype=torch.uint8, device=dev),
+                                  sink=0, window=16, workspace=ws)
+        assert ea.ea_check_errors(ws) == 6
+        assert ea.ea_check_errors(ws) == 0            # the word is cleared by the read
+
+
+def _full_size(dev, cfg, m, bm=None, n_random=64):
+    """Run one layer of a full-size workload and check sampled rows."""
+    Qd, Kd, Vd = wl.qkv(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.d, seed=cfg.seed, device=dev)
+    nB = (cfg.S + 127) // 128
+    vis = torch.zeros((cfg.B * cfg.Hkv * nB * nB + 31) // 32, dtype=torch.int32, device=dev)
+    ws = ea.prefill_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Qd, Kd, Vd, m.to(dev), sink=cfg.sink, window=cfg.window,
+                                       block_mask=None if bm is None else bm.to(dev),
+                                       workspace=ws, visited_bitmap=vis)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Q, K, V = Qd.cpu(), Kd.cpu(), Vd.cpu()
+    del Qd, Kd, Vd
+    srows = sample_rows(cfg.S, cfg.sink, cfg.window, n_random=n_random, edge=64)
+    rows = np.array([[b, qh, i] for b in range(cfg.B) for qh in range(cfg.Hq) for i in srows])
+    Oref, Lref = oracle.prefill_rows(Q, K, V, m, rows, sink=cfg.sink, window=cfg.window,
+                                     block_mask=bm)
+    idx = torch.from_numpy(rows).to(O.device)
+    Og = O[idx[:, 0], idx[:, 2], idx[:, 1]].float().cpu().numpy()
+    Lg = LSE[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy()
+    assert_close(Og, Lg, Oref, Lref, cfg.name)
+    # visited tiles of a few query blocks, bit-exact
+    tiles = bitmap_to_tiles(vis, cfg.B, cfg.Hkv, nB)
+    for qb in (0, 1, nB // 2, nB - 1):
+        ref = oracle.visited(cfg.B, cfg.S, cfg.Hkv, m, sink=cfg.sink, window=cfg.window,
+                             block_mask=bm, qb_begin=qb, qb_end=qb + 1)
+        np.testing.assert_array_equal(tiles[:, :, qb:qb + 1], ref)
+    return O, LSE
+
+
+def test_llama_32k_layer_sampled_rows(dev):
+    cfg = wl.LLAMA_32K
+    _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
+    _full_size(dev, cfg, m)
+
+
+def test_xa_ssa_256k_sampled_rows(dev):
+    cfg = wl.XA_SSA_256K
+    _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads, fa_impl=BLOCK, sa_impl=SSA)
+    bm = wl.block_mask(cfg.B, cfg.Hkv, cfg.S, density=cfg.block_density, seed=cfg.seed)
+    _full_size(dev, cfg, m, bm=bm, n_random=32)
