@@ -39,7 +39,16 @@ constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;   // warpgroups: softmax head 0, softmax head 1, producer + MMA
+// Register split: launched at kLaunchRegs per thread (12 warps: 3 per SM sub-
+// partition); the producer/MMA warpgroup drops to kCtrlRegs and the two softmax
+// warpgroups grow to kSoftmaxRegs.  2 * kSoftmaxRegs + kCtrlRegs must not
+// exceed 3 * kLaunchRegs, or the increase would wait forever; the host
+// launcher checks the compiled register count before every launch.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kCtrlRegs = 96;
+constexpr uint32_t kSoftmaxRegs = 200;
+static_assert(2 * kSoftmaxRegs + kCtrlRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale when max grows > 2^8
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
@@ -396,6 +405,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
     };
     auto issue_qk = [&](int sK) -> bool {
         const uint32_t kaddr = smem_u32(sm.kv[sK]);
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!mbar_wait(&sm.s_free[t], (s_cnt[t] & 1) ^ 1, &sm.abort, err))
                 return false;
@@ -419,6 +429,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
     };
     auto issue_pv = [&](int sV, bool acc) -> bool {
         const uint32_t vaddr = smem_u32(sm.kv[sV]);
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
             if (!mbar_wait(&sm.p_ready[t], p_cnt[t] & 1, &sm.abort, err))
                 return false;
@@ -562,10 +573,18 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                         s[c] = __float_as_uint(NEG_INF);
                 }
             }
-            float mx = NEG_INF;
+            // row max: eight independent 3-input chains
+            float mxa[8];
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-                mx = fmaxf(mx, __uint_as_float(s[c]));
+            for (int k = 0; k < 8; ++k)
+                mxa[k] = max3f(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]), NEG_INF);
+#pragma unroll
+            for (int c = 16; c < 128; c += 16)
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mxa[k] = max3f(mxa[k], __uint_as_float(s[c + 2 * k]), __uint_as_float(s[c + 2 * k + 1]));
+            float mx = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
+                             fmaxf(mxa[6], mxa[7]));
             mx *= a.scale_log2;
             const float m_new = fmaxf(m_run, mx);
             float factor = 1.f;
@@ -579,14 +598,25 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                 m_run = m_new;
             }
             const float mb = m_run > NEG_INF ? m_run : 0.f;
-            float lsum = 0.f;
+            // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
+            // the row sum in four independent packed accumulators
+            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+            const uint64_t nm2 = f2_pack(-mb, -mb);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float p = ex2(fmaf(__uint_as_float(s[c]), a.scale_log2, -mb));
-                lsum += p;
-                s[c] = __float_as_uint(p);
+            for (int c = 0; c < 128; c += 2) {
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2),
+                          x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
+                s[c] = __float_as_uint(p0);
+                s[c + 1] = __float_as_uint(p1);
             }
-            l_run += lsum;
+            float l0, l1, l2, l3;
+            f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
+            f2_unpack(f2_add(acc[2], acc[3]), l2, l3);
+            l_run += (l0 + l1) + (l2 + l3);
 
             // PV of the previous tile must be done before O is rescaled and
             // before the P buffer is overwritten.
@@ -713,12 +743,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
 
-    if (warp == kProducerWarp)
-        producer_role(&tm_q, &tm_k, &tm_v, a, sm, lane);
-    else if (warp == kMmaWarp)
-        mma_role(a, sm, tmem, lane);
-    else
+    if (warp >= 8) {
+        regs_dec<kCtrlRegs>();
+        if (warp == kProducerWarp)
+            producer_role(&tm_q, &tm_k, &tm_v, a, sm, lane);
+        else if (warp == kMmaWarp)
+            mma_role(a, sm, tmem, lane);
+    } else {
+        regs_inc<kSoftmaxRegs>();
         softmax_role(a, sm, tmem, warp);
+    }
 
     tc_fence_before();
     __syncthreads();
@@ -851,6 +885,16 @@ extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void 
     a.scale_log2 = scale * 1.4426950408889634f;
     if ((s = ensure_attributes()) != EA_OK)
         return s;
+    // The register split inside the kernel assumes this launch size.
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, hybrid_prefill_kernel) != cudaSuccess)
+            return EA_ERR_CUDA;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs != kLaunchRegs)
+        return EA_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return EA_ERR_CUDA;
