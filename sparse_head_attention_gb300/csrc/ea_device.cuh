@@ -157,6 +157,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, K packed two bf16 per 32-bit
+// column, one row per lane) is read from tensor memory.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void tc_commit(uint64_t *bar)

@@ -5,7 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/ea.h"
+#include "ea.h"
 
 // Tile edge (query rows per tile, keys per tile, block-mask block) and head dim.
 #define EA_TILE 128

@@ -16,14 +16,16 @@
 //      atomic queue head.  An item is two query heads of one GQA group over one
 //      128-query block, so each K/V tile in shared memory feeds two MMAs.
 //        warp 8     TMA producer: Q tiles, then K/V tiles in MMA order
-//        warp 9     tcgen05 issuer: S_t = Q_t K^T and O_t += P_t V into TMEM
+//        warp 9     tcgen05 issuer: S_t = Q_t K^T (smem x smem) and O_t += P_t V
+//                   (P from TMEM, V from smem) into TMEM
 //        warps 0-7  two softmax warpgroups (one per head of the pair): read S
 //                   from TMEM, mask edge tiles only, online softmax in fp32
 //                   (exp2 domain, lazy rescale of O when the max grows by
-//                   more than 2^8), write P (bf16) to shared memory, and
+//                   more than 2^8), write P (bf16) back into TMEM over S, and
 //                   finally normalise O and store O / LSE.
-//      TMEM: 512 columns = per head t: S_t (128 fp32 columns) + O_t (128).
-//      Shared memory: Q (2 x 32 KB), P (2 x 32 KB), a 3-stage K/V ring (3 x 32 KB).
+//      TMEM: 512 columns = per head t: S_t / P_t (128 fp32 columns) + O_t (128);
+//      the PV MMA reads P straight from TMEM, so P never touches shared memory.
+//      Shared memory: Q (2 x 32 KB) and a 5-stage K/V ring (5 x 32 KB).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,7 +36,7 @@ namespace ea {
 
 constexpr int T = EA_TILE;
 constexpr int D = EA_HEAD_DIM;
-constexpr int kStages = 3;
+constexpr int kStages = 5;
 constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
 constexpr int kProducerWarp = 8;
@@ -46,8 +48,8 @@ constexpr int kThreads = 384;   // warpgroups: softmax head 0, softmax head 1, p
 // exceed 3 * kLaunchRegs, or the increase would wait forever; the host
 // launcher checks the compiled register count before every launch.
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kCtrlRegs = 96;
-constexpr uint32_t kSoftmaxRegs = 200;
+constexpr uint32_t kCtrlRegs = 88;
+constexpr uint32_t kSoftmaxRegs = 208;
 static_assert(2 * kSoftmaxRegs + kCtrlRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale when max grows > 2^8
@@ -56,12 +58,11 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // V is M
 
 struct __align__(1024) PrefillSmem {
     uint8_t q[2][kTileBytes];
-    uint8_t p[2][kTileBytes];
     uint8_t kv[kStages][kTileBytes];
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], s_free[2], p_ready[2], o_done[2];
+    uint64_t s_full[2], p_ready[2], pv_done[2], o_done[2];
     uint64_t item_full[2], item_empty[2];
     uint64_t teardown;
     int item[2];
@@ -336,8 +337,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
             }
         }
         __syncwarp();
-        // K/V tiles in the order the MMA warp consumes them:
-        // K0, K1, V0, K2, V1, ..., K_{N-1}, V_{N-2}, V_{N-1}
+        // K/V tiles in the order the MMA warp consumes them: K0, V0, K1, V1, ...
         int n_sink = 0, kb_lo = 0;
         if (mode == EA_SSA)
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
@@ -345,16 +345,10 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
         if (mode == EA_BLOCK)
             scan.init(a.block_mask + (static_cast<int64_t>(x.b * a.Hkv + x.h) * a.nB + x.qb) * a.nB,
                       x.qb + 1, lane);
-        int prev_kb = -1;
-        for (int n = 0; n <= N && ok; ++n) {
-            int kb = -1;
-            if (n < N)
-                kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
+        for (int n = 0; n < N && ok; ++n) {
+            const int kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
+#pragma unroll 1
             for (int which = 0; which < 2; ++which) {
-                // which 0: K of tile n; which 1: V of tile n-1
-                const int tkb = which == 0 ? kb : prev_kb;
-                if (tkb < 0)
-                    continue;
                 const int s = kv_it % kStages;
                 if (!mbar_wait(&sm.kv_empty[s], ((kv_it / kStages) & 1) ^ 1, &sm.abort, err)) {
                     ok = false;
@@ -364,17 +358,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
                 if (lane == 0) {
                     const CUtensorMap *tm = which == 0 ? tm_k : tm_v;
                     mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
-                    tma_load_4d(sm.kv[s], tm, 0, x.h, tkb * T, x.b, &sm.kv_full[s]);
-                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, tkb * T, x.b, &sm.kv_full[s]);
+                    tma_load_4d(sm.kv[s], tm, 0, x.h, kb * T, x.b, &sm.kv_full[s]);
+                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, kb * T, x.b, &sm.kv_full[s]);
                     if (which == 0 && a.visited) {
                         const uint64_t bit =
-                            (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(tkb);
+                            (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(kb);
                         atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
                     }
                 }
                 __syncwarp();
             }
-            prev_kb = kb;
         }
     }
     // Before leaving on an abort, let the copies already issued land.
@@ -386,13 +379,18 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
     }
 }
 
+// MMA issue order per item (head t in {0, 1}):
+//   QK_0(0), QK_0(1), then for every tile n:
+//   PV_n(0), QK_{n+1}(0), PV_n(1), QK_{n+1}(1).
+// P_n(t) lives in TMEM over S_t, so QK_{n+1}(t) is issued only once PV_n(t)
+// has completed (pv_done); the other head's work keeps the tensor core busy
+// meanwhile.
 __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem, int lane)
 {
     uint32_t *err = &a.hdr->error;
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t s_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
-    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
-    const uint32_t p_addr[2] = {smem_u32(sm.p[0]), smem_u32(sm.p[1])};
+    uint32_t pv_cnt0 = 0, pv_cnt1 = 0, p_cnt0 = 0, p_cnt1 = 0;
+    const uint32_t q_addr0 = smem_u32(sm.q[0]), q_addr1 = smem_u32(sm.q[1]);
     bool ok = true;
 
     auto wait_kv = [&](int &s) -> bool {
@@ -403,53 +401,49 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
         tc_fence_after();
         return true;
     };
-    auto issue_qk = [&](int sK) -> bool {
-        const uint32_t kaddr = smem_u32(sm.kv[sK]);
+    // S_t = Q_t K^T once P_{n-1}(t) has been consumed
+    auto issue_qk = [&](int t, int sK) -> bool {
+        const uint32_t pv_cnt = t ? pv_cnt1 : pv_cnt0;
+        if (pv_cnt > 0 && !mbar_wait(&sm.pv_done[t], (pv_cnt - 1) & 1, &sm.abort, err))
+            return false;
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t kaddr = smem_u32(sm.kv[sK]);
+            const uint32_t qaddr = t ? q_addr1 : q_addr0;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(&sm.s_free[t], (s_cnt[t] & 1) ^ 1, &sm.abort, err))
-                return false;
-            ++s_cnt[t];
-            tc_fence_after();
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                    tc_mma(tmem + t * 256, sdesc_sw128(q_addr[t] + off, 16, 1024),
-                           sdesc_sw128(kaddr + off, 16, 1024), kIdescQK, k > 0);
-                }
-                tc_commit(&sm.s_full[t]);
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                tc_mma(tmem + t * 256, sdesc_sw128(qaddr + off, 16, 1024),
+                       sdesc_sw128(kaddr + off, 16, 1024), kIdescQK, k > 0);
             }
-            __syncwarp();
+            tc_commit(&sm.s_full[t]);
         }
-        if (lane == 0)
-            tc_commit(&sm.kv_empty[sK]);
         __syncwarp();
         return true;
     };
-    auto issue_pv = [&](int sV, bool acc) -> bool {
-        const uint32_t vaddr = smem_u32(sm.kv[sV]);
+    // O_t += P_t V once the softmax has written P_t
+    auto issue_pv = [&](int t, int sV, bool acc, bool last) -> bool {
+        uint32_t &p_cnt = t ? p_cnt1 : p_cnt0;
+        if (!mbar_wait(&sm.p_ready[t], p_cnt & 1, &sm.abort, err))
+            return false;
+        ++p_cnt;
+        tc_fence_after();
+        if (lane == 0) {
+            const uint32_t vaddr = smem_u32(sm.kv[sV]);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            if (!mbar_wait(&sm.p_ready[t], p_cnt[t] & 1, &sm.abort, err))
-                return false;
-            ++p_cnt[t];
-            tc_fence_after();
-            if (lane == 0) {
-#pragma unroll
-                for (int k = 0; k < T / 16; ++k) {
-                    const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                    tc_mma(tmem + t * 256 + 128, sdesc_sw128(p_addr[t] + aoff, 16, 1024),
-                           sdesc_sw128(vaddr + k * 2048, kHalfBytes, 1024), kIdescPV,
-                           (acc || k > 0) ? 1u : 0u);
-                }
+            for (int k = 0; k < T / 16; ++k)
+                tc_mma_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8,
+                          sdesc_sw128(vaddr + k * 2048, kHalfBytes, 1024), kIdescPV,
+                          (acc || k > 0) ? 1u : 0u);
+            tc_commit(&sm.pv_done[t]);
+            if (last)
                 tc_commit(&sm.o_done[t]);
-            }
-            __syncwarp();
         }
-        if (lane == 0)
-            tc_commit(&sm.kv_empty[sV]);
         __syncwarp();
+        if (t)
+            ++pv_cnt1;
+        else
+            ++pv_cnt0;
         return true;
     };
 
@@ -472,24 +466,44 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
         ++q_it;
         tc_fence_after();
         int sK, sV;
-        if (!wait_kv(sK) || !issue_qk(sK)) {
+        if (!wait_kv(sK) || !issue_qk(0, sK) || !issue_qk(1, sK)) {
             ok = false;
             break;
         }
-        if (N == 1 && lane == 0)
-            tc_commit(&sm.q_empty);
+        if (lane == 0) {
+            tc_commit(&sm.kv_empty[sK]);
+            if (N == 1)
+                tc_commit(&sm.q_empty);
+        }
+        __syncwarp();
         for (int n = 0; n < N && ok; ++n) {
-            if (n + 1 < N) {
-                if (!wait_kv(sK) || !issue_qk(sK)) {
+            const bool more = n + 1 < N;
+            if (!wait_kv(sV) || !issue_pv(0, sV, n > 0, !more)) {
+                ok = false;
+                break;
+            }
+            if (more && (!wait_kv(sK) || !issue_qk(0, sK))) {
+                ok = false;
+                break;
+            }
+            if (!issue_pv(1, sV, n > 0, !more)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0)
+                tc_commit(&sm.kv_empty[sV]);
+            __syncwarp();
+            if (more) {
+                if (!issue_qk(1, sK)) {
                     ok = false;
                     break;
                 }
-                if (n + 2 == N && lane == 0)
-                    tc_commit(&sm.q_empty);
-            }
-            if (!wait_kv(sV) || !issue_pv(sV, n > 0)) {
-                ok = false;
-                break;
+                if (lane == 0) {
+                    tc_commit(&sm.kv_empty[sK]);
+                    if (n + 2 == N)
+                        tc_commit(&sm.q_empty);
+                }
+                __syncwarp();
             }
         }
         __syncwarp();
@@ -502,6 +516,11 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
     mbar_wait(&sm.teardown, 0, &no_abort, err);
 }
 
+// One warpgroup per head of the pair; thread r owns query row r of the tile.
+// Per visited tile: S (fp32, 128 TMEM columns) -> registers, edge-tile mask,
+// online softmax in the exp2 domain, P (bf16) written back over the first 64
+// columns of S for the PV MMA.  S_n(t) being ready implies PV_{n-1}(t) has
+// completed, so O_t can be rescaled in place without another wait.
 __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem,
                                              int warp)
 {
@@ -511,7 +530,6 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 256;
     const uint32_t tO = tS + 128;
-    uint8_t *pbuf = sm.p[t];
     uint32_t s_cnt = 0, o_cnt = 0;
     const float NEG_INF = -__int_as_float(0x7f800000);
 
@@ -557,8 +575,6 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
             tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(&sm.s_free[t]);
 
             // mask edge tiles only
             const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
@@ -599,7 +615,8 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             }
             const float mb = m_run > NEG_INF ? m_run : 0.f;
             // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
-            // the row sum in four independent packed accumulators
+            // the row sum in four independent packed accumulators, P packed to
+            // bf16 pairs in place (s[c/2] once s[c], s[c+1] are consumed)
             const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
             const uint64_t nm2 = f2_pack(-mb, -mb);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -610,49 +627,31 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                           x0, x1);
                 const float p0 = ex2(x0), p1 = ex2(x1);
                 acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
-                s[c] = __float_as_uint(p0);
-                s[c + 1] = __float_as_uint(p1);
+                s[c >> 1] = pack_bf16x2(p0, p1);
             }
             float l0, l1, l2, l3;
             f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
             f2_unpack(f2_add(acc[2], acc[3]), l2, l3);
             l_run += (l0 + l1) + (l2 + l3);
 
-            // PV of the previous tile must be done before O is rescaled and
-            // before the P buffer is overwritten.
-            if (n > 0) {
-                if (!mbar_wait(&sm.o_done[t], o_cnt & 1, &sm.abort, err)) {
-                    ok = false;
-                    break;
-                }
-                ++o_cnt;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale_o)) {
+            // O rescale (PV_{n-1} is complete: it preceded QK_n in issue order
+            // and QK_n waited for it)
+            if (__any_sync(0xffffffffu, rescale_o)) {
 #pragma unroll 1
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint32_t o[32];
-                        tmem_ld32(tO + ch * 32, o);
-                        tmem_wait_ld();
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + ch * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c)
-                            o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
-                        tmem_st32(tO + ch * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int c = 0; c < 32; ++c)
+                        o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
+                    tmem_st32(tO + ch * 32, o);
                 }
             }
-            // P (bf16) -> shared memory, 128-byte swizzled K-major layout
-#pragma unroll
-            for (int c16 = 0; c16 < 16; ++c16) {
-                const int half = c16 >> 3, cc = c16 & 7;
-                uint4 v;
-                v.x = pack_bf16x2(__uint_as_float(s[c16 * 8 + 0]), __uint_as_float(s[c16 * 8 + 1]));
-                v.y = pack_bf16x2(__uint_as_float(s[c16 * 8 + 2]), __uint_as_float(s[c16 * 8 + 3]));
-                v.z = pack_bf16x2(__uint_as_float(s[c16 * 8 + 4]), __uint_as_float(s[c16 * 8 + 5]));
-                v.w = pack_bf16x2(__uint_as_float(s[c16 * 8 + 6]), __uint_as_float(s[c16 * 8 + 7]));
-                *reinterpret_cast<uint4 *>(pbuf + half * kHalfBytes + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
-            }
-            fence_proxy_async_smem();
+            // P (bf16 pairs) over the first 64 columns of S
+            tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&sm.p_ready[t]);
         }
@@ -718,8 +717,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&sm.q_empty, 1);
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.s_free[t], 128);
             mbar_init(&sm.p_ready[t], 128);
+            mbar_init(&sm.pv_done[t], 1);
             mbar_init(&sm.o_done[t], 1);
             mbar_init(&sm.item_full[t], 1);
             mbar_init(&sm.item_empty[t], 1 + 256);
