@@ -27,28 +27,35 @@ PrefillWs prefill_ws_layout(int B, int S, int Hq, int Hkv)
     return w;
 }
 
-DecodeWs decode_ws_layout(int B, int Hq, int splits)
+DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits)
 {
     DecodeWs w{};
-    const size_t n = static_cast<size_t>(B) * Hq * splits;
+    const size_t units = static_cast<size_t>(B) * Hkv;
+    const size_t chunks = units * max_splits;
+    const size_t g = Hq / Hkv;
     size_t off = sizeof(ea_ws_header);
+    w.unit_first = off;
+    off = align_up(off + sizeof(int32_t) * units, 256);
+    w.unit_splits = off;
+    off = align_up(off + sizeof(int32_t) * units, 256);
+    w.chunks = off;
+    off = align_up(off + sizeof(int32_t) * chunks, 256);
     w.partial_o = off;
-    off = align_up(off + sizeof(float) * n * EA_HEAD_DIM, 256);
+    off = align_up(off + sizeof(float) * chunks * g * EA_HEAD_DIM, 256);
     w.partial_lse = off;
-    off = align_up(off + sizeof(float) * n, 256);
+    off = align_up(off + sizeof(float) * chunks * g, 256);
     w.total = off;
     return w;
 }
 
-// Automatic split count: about 2048 keys per split for the longest sequence.
-int decode_auto_splits(int Lmax)
+// Chunks per unit: the caller's count, or one per EA_DECODE_AUTO_CHUNK keys of
+// the longest possible sequence.
+int decode_max_splits(int Lmax, int num_splits)
 {
-    int64_t s = ceil_div(Lmax, 2048);
-    if (s < 1)
-        s = 1;
-    if (s > 1024)
-        s = 1024;
-    return static_cast<int>(s);
+    if (num_splits > 0)
+        return num_splits;
+    int64_t s = ceil_div(Lmax, EA_DECODE_AUTO_CHUNK);
+    return static_cast<int>(s < 1 ? 1 : (s > 1024 ? 1024 : s));
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn()
@@ -128,8 +135,7 @@ extern "C" size_t ea_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lm
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d != EA_HEAD_DIM || Lmax < 1 ||
         num_splits < 0 || num_splits > 1024)
         return 0;
-    const int splits = num_splits == 0 ? decode_auto_splits(Lmax) : num_splits;
-    return decode_ws_layout(B, Hq, splits).total;
+    return decode_ws_layout(B, Hq, Hkv, decode_max_splits(Lmax, num_splits)).total;
 }
 
 extern "C" ea_status ea_check_errors(void *workspace, void *stream)

@@ -45,14 +45,20 @@ struct PrefillWs {
 };
 PrefillWs prefill_ws_layout(int B, int S, int Hq, int Hkv);
 
-// Byte offsets of the decode workspace regions.
+// Byte offsets of the decode workspace regions.  A chunk is one split of one
+// (b, KV head) unit; every unit has at most max_splits chunks.
 struct DecodeWs {
-    size_t partial_o;    // float [B*Hq*splits*128]
-    size_t partial_lse;  // float [B*Hq*splits]
+    size_t unit_first;   // int32 [B*Hkv]: index of the unit's first chunk
+    size_t unit_splits;  // int32 [B*Hkv]: number of chunks of the unit
+    size_t chunks;       // int32 [B*Hkv*max_splits]: unit << 11 | split
+    size_t partial_o;    // float [B*Hkv*max_splits][g][128]
+    size_t partial_lse;  // float [B*Hkv*max_splits][g]
     size_t total;
 };
-DecodeWs decode_ws_layout(int B, int Hq, int splits);
-int decode_auto_splits(int Lmax);
+DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits);
+// Keys per chunk when the split count is automatic.
+#define EA_DECODE_AUTO_CHUNK 2048
+int decode_max_splits(int Lmax, int num_splits);
 
 // Encodes a 4-D bf16 TMA tensor map (dims innermost first: head dim, heads,
 // sequence, batch; strides in elements) with a 64 x 1 x box_rows x 1 box and
