@@ -411,11 +411,11 @@ def run_decode(args, dev, peaks, flush):
     del Kc, Vc
     return {"workload": cfg.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(t, 4),
             "kept_kv_bytes_per_step": nbytes,
-            "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_merge_kernel",
+            "roofline": {"bound": "hbm", "kernel": "decode_plan_kernel + decode_split_kernel + decode_merge_kernel",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
                          "peak_source": peaks["source"]},
-            "gpu_launches_per_step": 2, "clocks": clk}
+            "gpu_launches_per_step": 3, "clocks": clk}
 
 
 def run_router(dev):

@@ -26,11 +26,12 @@
 
 namespace ea {
 
-constexpr int kDecKeys = 64;                           // keys per TMA box
-constexpr int kDecStages = 4;
-constexpr int kDecRowBytes = EA_HEAD_DIM * 2;          // 256
-constexpr int kDecBoxBytes = kDecKeys * kDecRowBytes;  // 16 KB
-constexpr int kDecThreads = 256;                       // 8 warps x 4 groups of 8 lanes
+constexpr int kDecKeys = 64;                           // keys per tile
+constexpr int kDecStages = 6;
+constexpr int kDecHalfBytes = kDecKeys * 128;          // one 64-dim swizzled box: 8 KB
+constexpr int kDecTileBytes = 2 * kDecHalfBytes;       // K or V of one tile: 16 KB
+constexpr int kDecWarps = 4;                           // compute warps: 16 keys each per tile
+constexpr int kDecThreads = (kDecWarps + 1) * 32;      // + one producer warp
 constexpr int kSplitBits = 11;                         // chunk code: unit << 11 | split
 
 struct DecodeArgs {
@@ -51,13 +52,15 @@ struct DecodeArgs {
     float scale_log2;
 };
 
-template <int G>
-struct DecSmem {
-    uint8_t kv[kDecStages][2][kDecBoxBytes];
-    float red_o[8][G][EA_HEAD_DIM];
-    float red_m[8][G];
-    float red_l[8][G];
+struct __align__(1024) DecSmem {
+    uint8_t k[kDecStages][kDecTileBytes];
+    uint8_t v[kDecStages][kDecTileBytes];
+    float red_o[kDecWarps][8][EA_HEAD_DIM];
+    float red_m[kDecWarps][8];
+    float red_l[kDecWarps][8];
     uint64_t full[kDecStages];
+    uint64_t empty[kDecStages];
+    int abort;   // set by a timed-out wait; every warp then leaves without further barriers
 };
 
 // Kept keys of one (b, KV head) unit as at most two contiguous ranges:
@@ -172,195 +175,232 @@ __device__ __forceinline__ void tile_rows(const ChunkInfo &ci, int t, int &key0,
     }
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
-
-__device__ __forceinline__ void unpack16(const uint4 &u0, const uint4 &u1, float (&f)[16])
+// ---------------------------------------------------------------- mma.sync
+// m16n8k16 bf16 -> fp32.  Fragment layouts (lane = 4 * row_in_group + quad):
+//   A 16x16: a0 = (r, 2q..2q+1), a1 = (r + 8, ..), a2 = (r, 2q + 8..), a3 = (r + 8, 2q + 8..)
+//   B 16x8 : b0 = (k = 2q..2q+1, n = r), b1 = (k = 2q + 8.., n = r)
+//   C 16x8 : c0, c1 = (r, 2q..2q+1), c2, c3 = (r + 8, ..)
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    f[0] = bf_lo(u0.x); f[1] = bf_hi(u0.x); f[2] = bf_lo(u0.y); f[3] = bf_hi(u0.y);
-    f[4] = bf_lo(u0.z); f[5] = bf_hi(u0.z); f[6] = bf_lo(u0.w); f[7] = bf_hi(u0.w);
-    f[8] = bf_lo(u1.x); f[9] = bf_hi(u1.x); f[10] = bf_lo(u1.y); f[11] = bf_hi(u1.y);
-    f[12] = bf_lo(u1.z); f[13] = bf_hi(u1.z); f[14] = bf_lo(u1.w); f[15] = bf_hi(u1.w);
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Persistent: CTA x handles chunks x, x + grid, x + 2 grid, ...  Thread 0
-// keeps kDecStages K/V tile pairs in flight, running ahead across chunk
-// boundaries, so a chunk's epilogue overlaps the next chunk's loads.
-template <int G>
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// Barrier over the compute warps only (named barrier 1).
+__device__ __forceinline__ void compute_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecWarps * 32) : "memory");
+}
+
+// Byte offset of the 16-byte chunk holding (row, 8-element column block cb)
+// of a [64 rows][128 dims] tile stored as two 128-byte-swizzled 64-dim boxes.
+__device__ __forceinline__ uint32_t sw_off(int row, int cb)
+{
+    return (cb >> 3) * kDecHalfBytes + row * 128 + (((cb & 7) ^ (row & 7)) << 4);
+}
+
+// Persistent: CTA x handles chunks x, x + grid, x + 2 grid, ...
+// Warp w (of 4) owns keys [16w, 16w + 16) of every 64-key tile; the query
+// heads of the GQA group are the rows of the MMA (padded to 16 with zeros):
+//   S (16 x 16 keys) = Q K^T : 2 key blocks x 8 head-dim steps
+//   O (16 x 128)    += P V   : P straight from the S fragments, 16 dim blocks
+// The producer warp keeps kDecStages tiles in flight across chunk boundaries;
+// each compute warp releases a stage through its arrival on `empty`.
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    DecSmem<G> &sm = *reinterpret_cast<DecSmem<G> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    DecSmem &sm = *reinterpret_cast<DecSmem *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int grp = lane >> 3, j = lane & 7;
+    const int r = lane >> 2, qd = lane & 3;   // fragment row / quad position
     const float NEG_INF = -__int_as_float(0x7f800000);
     const int total = static_cast<int>(a.hdr->n_items);
+    volatile int *abort = &sm.abort;
 
     if (tid == 0) {
-        for (int s = 0; s < kDecStages; ++s)
+        sm.abort = 0;
+        for (int s = 0; s < kDecStages; ++s) {
             mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], kDecWarps);
+        }
         fence_barrier_init();
         fence_proxy_async_smem();
     }
     __syncthreads();
 
-    // producer cursor (thread 0 only)
-    int pc = blockIdx.x, pt = 0;
-    ChunkInfo pci;
-    if (tid == 0 && pc < total)
-        pci = chunk_info(a, pc);
-    uint32_t issued = 0;
-    auto issue_next = [&]() {
-        while (pc < total && pt >= pci.n_tiles) {
-            pc += gridDim.x;
-            pt = 0;
-            if (pc < total)
-                pci = chunk_info(a, pc);
+    if (warp == kDecWarps) {
+        // ------------------------------------------------------------ producer
+        // The whole warp walks the tile sequence (converged waits); lane 0
+        // issues the copies.  It takes part in no block-wide barrier: the
+        // compute warps synchronise among themselves with a named barrier.
+        uint32_t issued = 0;
+        for (int c = blockIdx.x; c < total; c += gridDim.x) {
+            const ChunkInfo ci = chunk_info(a, c);
+            for (int t = 0; t < ci.n_tiles; ++t) {
+                const int s = issued % kDecStages;
+                if (!mbar_wait(&sm.empty[s], ((issued / kDecStages) & 1) ^ 1, abort, &a.hdr->error))
+                    return;
+                if (lane == 0) {
+                    int key0, nv;
+                    tile_rows(ci, t, key0, nv);
+                    mbar_arrive_expect_tx(&sm.full[s], 2 * kDecTileBytes);
+                    tma_load_4d(sm.k[s], &tm_k, 0, ci.h, key0, ci.b, &sm.full[s]);
+                    tma_load_4d(sm.k[s] + kDecHalfBytes, &tm_k, 64, ci.h, key0, ci.b, &sm.full[s]);
+                    tma_load_4d(sm.v[s], &tm_v, 0, ci.h, key0, ci.b, &sm.full[s]);
+                    tma_load_4d(sm.v[s] + kDecHalfBytes, &tm_v, 64, ci.h, key0, ci.b, &sm.full[s]);
+                }
+                __syncwarp();
+                ++issued;
+            }
         }
-        if (pc >= total)
-            return;
-        int key0, nv;
-        tile_rows(pci, pt, key0, nv);
-        const int s = issued % kDecStages;
-        mbar_arrive_expect_tx(&sm.full[s], 2 * kDecBoxBytes);
-        tma_load_4d(sm.kv[s][0], &tm_k, 0, pci.h, key0, pci.b, &sm.full[s]);
-        tma_load_4d(sm.kv[s][1], &tm_v, 0, pci.h, key0, pci.b, &sm.full[s]);
-        ++issued;
-        ++pt;
-    };
-    if (tid == 0)
-        for (int k = 0; k < kDecStages; ++k)
-            issue_next();
+        return;
+    }
 
-    volatile int no_abort = 0;
+    // ---------------------------------------------------------------- compute
     uint32_t consumed = 0;
     for (int c = blockIdx.x; c < total; c += gridDim.x) {
         const ChunkInfo ci = chunk_info(a, c);
-        // query slices of this lane: d in {8j..8j+7} and {64+8j..64+8j+7}
-        float q[G][16];
+        // Q as the A operand: rows r < g are query heads, the rest zero
+        uint32_t qa[8][2];   // per head-dim step j: (r, 16j + 2q..), (r, 16j + 8 + 2q..)
+        {
+            const bool real = r < a.g;
+            const __nv_bfloat16 *qrow = a.q + ci.b * a.q_sb + (ci.h * a.g + (real ? r : 0)) * a.q_sh;
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            const int qh = ci.h * a.g + (hh < a.g ? hh : 0);
-            const uint4 *qp = reinterpret_cast<const uint4 *>(a.q + ci.b * a.q_sb + qh * a.q_sh);
-            unpack16(qp[j], qp[8 + j], q[hh]);
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t *p0 = reinterpret_cast<const uint32_t *>(qrow + 16 * j + 2 * qd);
+                const uint32_t *p1 = reinterpret_cast<const uint32_t *>(qrow + 16 * j + 8 + 2 * qd);
+                qa[j][0] = real ? *p0 : 0u;
+                qa[j][1] = real ? *p1 : 0u;
+            }
         }
-        float m_run[G], l_run[G], o[G][16];
+        float o[16][4];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-            m_run[hh] = NEG_INF;
-            l_run[hh] = 0.f;
+        for (int n = 0; n < 16; ++n)
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                o[hh][e] = 0.f;
-        }
+            for (int e = 0; e < 4; ++e)
+                o[n][e] = 0.f;
+        float m_run = NEG_INF, l_part = 0.f;   // row r statistics (l summed over the quad at the end)
+
         for (int t = 0; t < ci.n_tiles; ++t) {
             const int s = consumed % kDecStages;
-            if (!mbar_wait(&sm.full[s], (consumed / kDecStages) & 1, &no_abort, &a.hdr->error))
-                return;  // timed out: the error word is set
+            if (!mbar_wait(&sm.full[s], (consumed / kDecStages) & 1, abort, &a.hdr->error))
+                return;  // timed out (error word set) or another warp did
             ++consumed;
             int key0, nv;
             tile_rows(ci, t, key0, nv);
-            const uint8_t *kt = sm.kv[s][0];
-            const uint8_t *vt = sm.kv[s][1];
+            const uint32_t kb = smem_u32(sm.k[s]), vb = smem_u32(sm.v[s]);
+            const int kw = warp * 16;   // this warp's first key in the tile
+
+            // S = Q K^T for keys kw..kw+15 (two 8-key blocks)
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int krow = kw + (lane >> 4) * 8 + (lane & 7);   // key this lane addresses
+                const int csel = (lane >> 3) & 1;                      // 0: first 8 dims, 1: next 8
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const int key = warp * 8 + grp * 2 + kk;
-                const uint4 *kr = reinterpret_cast<const uint4 *>(kt + key * kDecRowBytes);
-                float kf[16];
-                unpack16(kr[j], kr[8 + j], kf);
-                float sc[G];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        acc = fmaf(q[hh][e], kf[e], acc);
-                    sc[hh] = acc;
-                }
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 1);
-                    sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 2);
-                    sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 4);
-                }
-                if (key < nv) {
-                    const uint4 *vr = reinterpret_cast<const uint4 *>(vt + key * kDecRowBytes);
-                    float vf[16];
-                    unpack16(vr[j], vr[8 + j], vf);
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        const float x = sc[hh] * a.scale_log2;
-                        if (x > m_run[hh]) {
-                            const float f = ex2(m_run[hh] - x);
-                            l_run[hh] *= f;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                o[hh][e] *= f;
-                            m_run[hh] = x;
-                        }
-                        const float p = ex2(x - m_run[hh]);
-                        l_run[hh] += p;
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            o[hh][e] = fmaf(p, vf[e], o[hh][e]);
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4(kb + sw_off(krow, 2 * j + csel), b00, b01, b10, b11);
+                    mma_bf16(sc[0], qa[j][0], 0u, qa[j][1], 0u, b00, b01);
+                    mma_bf16(sc[1], qa[j][0], 0u, qa[j][1], 0u, b10, b11);
                 }
             }
-            __syncthreads();  // every warp is done with stage s: refill it
-            if (tid == 0)
-                issue_next();
+            // online softmax over this warp's 16 keys, row r
+            float x[4] = {sc[0][0] * a.scale_log2, sc[0][1] * a.scale_log2,
+                          sc[1][0] * a.scale_log2, sc[1][1] * a.scale_log2};
+            const int kcol[4] = {kw + 2 * qd, kw + 2 * qd + 1, kw + 8 + 2 * qd, kw + 9 + 2 * qd};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (kcol[e] >= nv)
+                    x[e] = NEG_INF;
+            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            if (m_new > m_run) {
+                const float f = m_run == NEG_INF ? 0.f : ex2(m_run - m_new);
+                l_part *= f;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) {
+                    o[n][0] *= f;
+                    o[n][1] *= f;
+                }
+                m_run = m_new;
+            }
+            const float mb = m_run == NEG_INF ? 0.f : m_run;
+            float p[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p[e] = ex2(x[e] - mb);
+                l_part += p[e];
+            }
+            const uint32_t pa0 = pack_bf16x2(p[0], p[1]);   // (r, keys 2q..)
+            const uint32_t pa2 = pack_bf16x2(p[2], p[3]);   // (r, keys 8 + 2q..)
+
+            // O += P V: 16 head-dim blocks of 8, two per ldmatrix
+            {
+                const int vrow = kw + ((lane >> 3) & 1) * 8 + (lane & 7);
+                const int cadd = lane >> 4;
+#pragma unroll
+                for (int n = 0; n < 16; n += 2) {
+                    uint32_t b00, b01, b10, b11;
+                    ldsm_x4_t(vb + sw_off(vrow, n + cadd), b00, b01, b10, b11);
+                    mma_bf16(o[n], pa0, 0u, pa2, 0u, b00, b01);
+                    mma_bf16(o[n + 1], pa0, 0u, pa2, 0u, b10, b11);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&sm.empty[s]);
         }
 
-        // combine the 4 groups of each warp (lanes j, j+8, j+16, j+24 hold the same d)
+        // per-warp results of the rows r < g -> shared memory, then merge warps
+        l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+        l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+        if (r < a.g) {
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-            for (int off = 8; off <= 16; off <<= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, m_run[hh], off);
-                const float lo = __shfl_xor_sync(0xffffffffu, l_run[hh], off);
-                const float mn = fmaxf(m_run[hh], mo);
-                const float fa = mn == NEG_INF ? 0.f : ex2(m_run[hh] - mn);
-                const float fb = mn == NEG_INF ? 0.f : ex2(mo - mn);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float oo = __shfl_xor_sync(0xffffffffu, o[hh][e], off);
-                    o[hh][e] = o[hh][e] * fa + oo * fb;
-                }
-                l_run[hh] = l_run[hh] * fa + lo * fb;
-                m_run[hh] = mn;
+            for (int n = 0; n < 16; ++n) {
+                sm.red_o[warp][r][8 * n + 2 * qd] = o[n][0];
+                sm.red_o[warp][r][8 * n + 2 * qd + 1] = o[n][1];
+            }
+            if (qd == 0) {
+                sm.red_m[warp][r] = m_run;
+                sm.red_l[warp][r] = l_part;
             }
         }
-        // combine the 8 warps through shared memory
-        if (grp == 0) {
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int dd = e < 8 ? 8 * j + e : 64 + 8 * j + (e - 8);
-                    sm.red_o[warp][hh][dd] = o[hh][e];
-                }
-                if (j == 0) {
-                    sm.red_m[warp][hh] = m_run[hh];
-                    sm.red_l[warp][hh] = l_run[hh];
-                }
-            }
-        }
-        __syncthreads();
-        for (int idx = tid; idx < G * EA_HEAD_DIM; idx += kDecThreads) {
+        if (*abort)
+            return;
+        compute_sync();
+        for (int idx = tid; idx < a.g * EA_HEAD_DIM; idx += kDecWarps * 32) {
             const int hh = idx / EA_HEAD_DIM, dd = idx % EA_HEAD_DIM;
-            if (hh >= a.g)
-                continue;
             float M = NEG_INF;
 #pragma unroll
-            for (int w = 0; w < 8; ++w)
+            for (int w = 0; w < kDecWarps; ++w)
                 M = fmaxf(M, sm.red_m[w][hh]);
             float lsum = 0.f, osum = 0.f;
             if (M > NEG_INF)
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
+                for (int w = 0; w < kDecWarps; ++w) {
                     const float f = ex2(sm.red_m[w][hh] - M);
                     lsum += sm.red_l[w][hh] * f;
                     osum += sm.red_o[w][hh][dd] * f;
@@ -370,7 +410,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             if (dd == 0)
                 a.part_lse[pidx] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
         }
-        __syncthreads();  // the reduction buffers are reused by the next chunk
+        if (*abort)
+            return;
+        compute_sync();  // the reduction buffers are reused by the next chunk
     }
 }
 
@@ -398,21 +440,20 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a)
         a.LSE[static_cast<int64_t>(b) * a.Hq + qh] = wsum > 0.f ? M + __logf(wsum) : NEG_INF;
 }
 
-template <int G>
 static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
                                  int grid, cudaStream_t st)
 {
-    const size_t smem = sizeof(DecSmem<G>) + 128;
+    const size_t smem = sizeof(DecSmem) + 1024;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G>,
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
         attr = true;
     }
-    decode_split_kernel<G><<<grid, kDecThreads, smem, st>>>(tk, tv, a);
+    decode_split_kernel<<<grid, kDecThreads, smem, st>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
@@ -456,8 +497,8 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
         return EA_ERR_WORKSPACE;
 
     alignas(64) CUtensorMap tk, tv;
-    if (!encode_tmap_bf16_4d(&tk, Kc, d, Hkv, Lmax, B, kv_str, EA_HEAD_DIM, kDecKeys, false) ||
-        !encode_tmap_bf16_4d(&tv, Vc, d, Hkv, Lmax, B, kv_str, EA_HEAD_DIM, kDecKeys, false))
+    if (!encode_tmap_bf16_4d(&tk, Kc, d, Hkv, Lmax, B, kv_str, 64, kDecKeys, true) ||
+        !encode_tmap_bf16_4d(&tv, Vc, d, Hkv, Lmax, B, kv_str, 64, kDecKeys, true))
         return EA_ERR_INVALID_ARG;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -498,15 +539,7 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
     const int64_t max_chunks = static_cast<int64_t>(B) * Hkv * max_splits;
     const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
     decode_plan_kernel<<<1, 1024, 0, st>>>(a);
-    cudaError_t e;
-    if (a.g == 1)
-        e = launch_decode<1>(tk, tv, a, grid, st);
-    else if (a.g == 2)
-        e = launch_decode<2>(tk, tv, a, grid, st);
-    else if (a.g <= 4)
-        e = launch_decode<4>(tk, tv, a, grid, st);
-    else
-        e = launch_decode<8>(tk, tv, a, grid, st);
+    const cudaError_t e = launch_decode(tk, tv, a, grid, st);
     if (e != cudaSuccess)
         return EA_ERR_CUDA;
     decode_merge_kernel<<<dim3(Hq, B), EA_HEAD_DIM, 0, st>>>(a);
