@@ -375,9 +375,13 @@ def run_ours(args, rank, world, dev):
 
 
 def run_decode(args, dev, peaks, flush):
+    import dataclasses
+
     import sparse_head_attention_gb300 as ea
     from sparse_head_attention_gb300 import workloads as wl
     cfg = wl.DECODE_128K
+    if args.decode_batch != cfg.B:
+        cfg = dataclasses.replace(cfg, B=args.decode_batch, name="%s_b%d" % (cfg.name, args.decode_batch))
     q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev)
     _, m_cpu = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
     m = m_cpu.to(dev)
@@ -508,6 +512,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode workload (profiling helper; prints its object)")
+    ap.add_argument("--decode-batch", type=int, default=32,
+                    help="decode batch (32 is the benchmark workload; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -529,6 +537,11 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     from sparse_head_attention_gb300 import build as ea_build
     ea_build.build()
+    if args.decode_only:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        if rank == 0:
+            print(json.dumps(run_decode(args, dev, measured_peaks(), flush)), flush=True)
+        return 0
     line = run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
