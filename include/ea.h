@@ -180,6 +180,39 @@ ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O
                             const uint8_t *block_mask, int block_size, void *workspace,
                             size_t ws_bytes, uint32_t *visited_bitmap, void *stream);
 
+/*
+ * ea_hybrid_attn_prefill_noalloc - ea_hybrid_attn_prefill for callers that
+ * cannot provide a workspace, e.g. an engine whose device memory is owned by
+ * its own allocator and that forbids allocations once it is running, or a
+ * latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation.  The pages have no counterpart of this entry point; it is
+ * an interface convenience of this library.
+ *
+ * Same arguments, results and constraints as ea_hybrid_attn_prefill, minus the
+ * workspace.  The planner's scratch lives in a fixed 4 MiB device array
+ * inside the library (one per device that loads it, kept until the process
+ * exits).  It holds the plan of any problem with
+ * ea_prefill_workspace_size(B, S, Hq, Hkv, d) <= 4 MiB (for example B = 1,
+ * 8 KV heads, 32 query heads, S up to 1M); larger problems return
+ * EA_ERR_UNSUPPORTED without enqueueing anything.  Nothing is allocated.
+ *
+ * The first call on a device looks up that array's device address (with the
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call reuses the same array and clears its header first, so
+ * calls whose executions overlap on the GPU (different streams, or different
+ * host threads without ordering) race and must be serialised by the caller.
+ * Device-side checks (invalid mode, missing block mask, a timed-out wait)
+ * leave their error word in that internal array, which no entry point reads
+ * back; diagnose such inputs with ea_hybrid_attn_prefill and a workspace.
+ */
+ea_status ea_hybrid_attn_prefill_noalloc(const void *Q, const void *K, const void *V, void *O,
+                                         float *LSE, const int64_t q_str[4],
+                                         const int64_t kv_str[4], const int64_t o_str[4], int B,
+                                         int S, int Hq, int Hkv, int d, float scale,
+                                         const uint8_t *m, int sink, int window,
+                                         const uint8_t *block_mask, int block_size,
+                                         uint32_t *visited_bitmap, void *stream);
+
 /* Bytes of device workspace ea_hybrid_attn_decode needs (0 on invalid sizes).
  * num_splits = 0 means the automatic choice; the same value must be passed to
  * ea_hybrid_attn_decode. */

@@ -30,7 +30,8 @@ _lib = None
 
 # Function names exported by the library (the ones include/ea.h declares).
 EXPORTS = ("ea_status_string", "ea_route", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
-           "ea_prefill_plan", "ea_prefill_attend", "ea_decode_workspace_size",
+           "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
+           "ea_decode_workspace_size",
            "ea_hybrid_attn_decode", "ea_sparsity_ratios", "ea_check_errors")
 
 
@@ -69,6 +70,9 @@ def lib():
                                              P, i32, i32, P, i32, P, sz, P, P]
         L.ea_prefill_plan.argtypes = [i32, i32, i32, i32, i32, P, i32, i32, P, i32, P, sz, P]
         L.ea_prefill_attend.argtypes = list(L.ea_hybrid_attn_prefill.argtypes)
+        L.ea_hybrid_attn_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                     i32, f32, P, i32, i32, P, i32, P, P]
+        L.ea_hybrid_attn_prefill_noalloc.restype = ctypes.c_int
         L.ea_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ea_decode_workspace_size.restype = sz
         L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
@@ -193,6 +197,34 @@ def ea_prefill_attend(Q, K, V, m, *, sink, window, workspace, **kw):
     """Enqueue the attention kernel on a plan made by ea_prefill_plan."""
     return ea_hybrid_attn_prefill(Q, K, V, m, sink=sink, window=window, workspace=workspace,
                                   _entry="ea_prefill_attend", **kw)
+
+
+def ea_hybrid_attn_prefill_noalloc(Q, K, V, m, *, sink, window, block_mask=None, scale=None,
+                                   O=None, LSE=None, visited_bitmap=None, stream=None,
+                                   want_lse=True):
+    """ea_hybrid_attn_prefill without a workspace: for callers that cannot
+    allocate device memory for the library (the planner's scratch is a fixed
+    4 MiB array inside it; see include/ea.h).  Returns (O, LSE)."""
+    _dev(Q, "Q", torch.bfloat16)
+    _dev(K, "K", torch.bfloat16)
+    _dev(V, "V", torch.bfloat16)
+    _dev(m, "m", torch.uint8)
+    if K.stride() != V.stride():
+        raise ValueError("K and V must share strides")
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None and want_lse:
+        LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=Q.device)
+    st = lib().ea_hybrid_attn_prefill_noalloc(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _strides(Q), _strides(K), _strides(O),
+        B, S, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window), _ptr(block_mask), TILE,
+        _ptr(visited_bitmap), _stream(stream))
+    _check("ea_hybrid_attn_prefill_noalloc", st)
+    return O, LSE
 
 
 def ea_decode_workspace_size(B, Hq, Hkv, Lmax, num_splits=0, d=128):

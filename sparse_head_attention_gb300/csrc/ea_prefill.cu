@@ -29,6 +29,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "ea_device.cuh"
 #include "ea_internal.h"
 
@@ -939,4 +941,60 @@ extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const 
     return ea_prefill_attend(Q, K, V, O, LSE, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale, m,
                              sink, window, block_mask, block_size, workspace, ws_bytes,
                              visited_bitmap, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill.  Some callers cannot hand the library a workspace:
+// an engine whose device memory is owned end to end by its own allocator and
+// that forbids allocations after start-up, or a latency-critical path that
+// cannot afford cudaMalloc's implicit device synchronisation.  This entry point
+// keeps the planner's scratch (work queue and per-block tile counts) in a
+// file-scope device array instead, so the caller passes only inputs and
+// outputs.  The array is EA_NOALLOC_PREFILL_SCRATCH_BYTES long and lives on
+// every device that loads the library until the process exits.
+#define EA_NOALLOC_PREFILL_SCRATCH_BYTES (4u << 20)
+
+static __device__ __align__(256) uint8_t g_noalloc_prefill_scratch[EA_NOALLOC_PREFILL_SCRATCH_BYTES];
+
+// Device address of the array, resolved once per device (host code only sees a
+// host-side stand-in under that name).
+static void *g_noalloc_scratch_ptr[64] = {};
+static std::mutex g_noalloc_mutex;
+
+extern "C" ea_status ea_hybrid_attn_prefill_noalloc(const void *Q, const void *K, const void *V,
+                                                    void *O, float *LSE, const int64_t q_str[4],
+                                                    const int64_t kv_str[4],
+                                                    const int64_t o_str[4], int B, int S, int Hq,
+                                                    int Hkv, int d, float scale, const uint8_t *m,
+                                                    int sink, int window,
+                                                    const uint8_t *block_mask, int block_size,
+                                                    uint32_t *visited_bitmap, void *stream)
+{
+    const size_t need = ea_prefill_workspace_size(B, S, Hq, Hkv, d);
+    if (need == 0)
+        return (d != EA_HEAD_DIM || S > EA_MAX_SEQ) ? EA_ERR_UNSUPPORTED : EA_ERR_INVALID_ARG;
+    if (need > EA_NOALLOC_PREFILL_SCRATCH_BYTES)
+        return EA_ERR_UNSUPPORTED;  // plan would not fit the fixed scratch array
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return EA_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        if (!g_noalloc_scratch_ptr[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_prefill_scratch) != cudaSuccess || !p)
+                return EA_ERR_CUDA;
+            g_noalloc_scratch_ptr[dev] = p;
+        }
+        scratch = g_noalloc_scratch_ptr[dev];
+    }
+    // The array keeps the previous call's contents: clear the header (error
+    // word and queue counters) before planning.
+    if (cudaMemsetAsync(scratch, 0, sizeof(ea_ws_header), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return EA_ERR_CUDA;
+    return ea_hybrid_attn_prefill(Q, K, V, O, LSE, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale,
+                                  m, sink, window, block_mask, block_size, scratch,
+                                  EA_NOALLOC_PREFILL_SCRATCH_BYTES, visited_bitmap, stream);
 }
