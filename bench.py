@@ -370,7 +370,7 @@ def run_ours(args, rank, world, dev):
         "router": router,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V, m_cpu, args)
+        line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V, m_cpu, bm_cpu, args)
     return line
 
 
@@ -417,7 +417,10 @@ def run_decode(args, dev, peaks, flush):
             "kept_kv_bytes_per_step": nbytes,
             "roofline": {"bound": "hbm", "kernel": "decode_plan_kernel + decode_split_kernel + decode_merge_kernel",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": None,
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "traffic": profile_traffic("decode_split_b4_l128k.md", os.path.join(
+                             ROOT, "sparse_head_attention_gb300", "csrc", "ea_decode.cu"))
+                         if cfg.B == 32 else None,
                          "peak_source": peaks["source"]},
             "gpu_launches_per_step": 3, "clocks": clk}
 
@@ -445,47 +448,62 @@ def run_router(dev):
 
 
 # ------------------------------------------------------------------ oracle
-def _oracle_sample(cfg, Q, K, V, m_cpu, n_rows_per_head=256):
-    """A bounded row sample: for one query head of every KV head, rows spread
-    evenly over the sequence."""
+def _oracle_rows(cfg, m_cpu, bm_cpu, offset, n_rows_per_head):
+    """A bounded row sample: one query head of every KV head, rows spread evenly
+    over the sequence (shifted by `offset` so repeated samples differ), with the
+    useful flops of those rows."""
     g = cfg.Hq // cfg.Hkv
-    idx = np.linspace(0, cfg.S - 1, n_rows_per_head).astype(np.int64)
+    idx = (np.linspace(0, cfg.S - 1, n_rows_per_head).astype(np.int64) + offset) % cfg.S
     rows = np.array([[0, h * g, i] for h in range(cfg.Hkv) for i in idx], dtype=np.int64)
     flops = 0
     for h in range(cfg.Hkv):
         mode = int(m_cpu[0, h])
+        bmh = None if bm_cpu is None else bm_cpu[0, h]
         for i in idx:
             if mode == 0:
                 kept = i + 1
-            else:
+            elif mode == 1:
                 kept = min(i + 1, cfg.window) + max(0, min(cfg.sink, i + 1 - cfg.window))
+            else:
+                qb = i // 128
+                kept = int(bmh[qb, :qb].sum()) * 128 + (int(i % 128) + 1) * int(bmh[qb, qb])
             flops += 4 * cfg.d * kept
     return rows, flops
 
 
-def cpu_baseline(cfg, Q, K, V, m_cpu, args, rows_per_head=256):
+def cpu_baseline(cfg, Q, K, V, m_cpu, bm_cpu, args, budget_s=10.0):
+    """The fp64 oracle on this machine's cores over a time-bounded row sample."""
     import oracle
     Qc, Kc, Vc = Q.cpu(), K.cpu(), V.cpu()
-    rows, flops = _oracle_sample(cfg, Qc, Kc, Vc, m_cpu, rows_per_head)
+    bm = None if bm_cpu is None else bm_cpu.numpy()
+    oracle.lib()
     t0 = time.perf_counter()
-    oracle.prefill_rows(Qc, Kc, Vc, m_cpu, rows, sink=cfg.sink, window=cfg.window)
+    done_rows = done_flops = 0
+    k = 0
+    while time.perf_counter() - t0 < budget_s and k < 64:
+        rows, flops = _oracle_rows(cfg, m_cpu, bm, 7919 * k, 256)
+        oracle.prefill_rows(Qc, Kc, Vc, m_cpu, rows, sink=cfg.sink, window=cfg.window, block_mask=bm)
+        done_rows += len(rows)
+        done_flops += flops
+        k += 1
     dt = time.perf_counter() - t0
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": "%d query rows (%d per KV head, evenly spaced) of %s, %.3g useful flops, %.2f s"
-                      % (len(rows), rows_per_head, cfg.name, flops, dt)}
+    return {"value": done_flops / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "%d query rows of %s (%d batches of 256 evenly spaced rows per KV head), "
+                      "%.3g useful flops in %.1f s" % (done_rows, cfg.name, k, done_flops, dt)}
 
 
 def run_reference(args):
     import oracle
     cfg = get_cfg(args.workload)
-    Q, K, V, m_cpu, _ = make_prefill_inputs(cfg, "cpu")
-    rows, flops = _oracle_sample(cfg, Q, K, V, m_cpu, 64)
+    Q, K, V, m_cpu, bm_cpu = make_prefill_inputs(cfg, "cpu")
+    bm = None if bm_cpu is None else bm_cpu.numpy()
+    rows, flops = _oracle_rows(cfg, m_cpu, bm, 0, 64)
     oracle.lib()
     for _ in range(args.warmup):
-        oracle.prefill_rows(Q, K, V, m_cpu, rows[:8], sink=cfg.sink, window=cfg.window)
+        oracle.prefill_rows(Q, K, V, m_cpu, rows[:8], sink=cfg.sink, window=cfg.window, block_mask=bm)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.prefill_rows(Q, K, V, m_cpu, rows, sink=cfg.sink, window=cfg.window)
+        oracle.prefill_rows(Q, K, V, m_cpu, rows, sink=cfg.sink, window=cfg.window, block_mask=bm)
     dt = time.perf_counter() - t0
     value = flops * args.steps / dt / 1e12
     sample = ("%d query rows (64 per KV head, evenly spaced) of %s per step, %.3g useful flops"
