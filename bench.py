@@ -520,6 +520,80 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+# ------------------------------------------------------------------ Algorithm 1(a) comparison
+def serial_dispatch(ea, Q, K, V, m_cpu, sink, window, O, LSE, ws_fa, ws_sa):
+    """Serial Dispatch ("Paper Reading - Elastic Attention" (English notes),
+    §04 Deployment, Algorithm 1(a)): split the KV heads into the FA and the SA
+    group, copy each group's Q/K/V into tensors of their own, run one
+    single-mode attention launch per group, and copy the outputs back into
+    place.  Same kernels as the fused path; only the dispatch differs."""
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    g = Hq // Hkv
+    dev = Q.device
+    for mode, ws in ((0, ws_fa), (1, ws_sa)):
+        kv = [h for h in range(Hkv) if int(m_cpu[0, h]) == mode]
+        if not kv:
+            continue
+        kv_t = torch.tensor(kv, device=dev)
+        q_t = torch.tensor([h * g + j for h in kv for j in range(g)], device=dev)
+        Qs = Q.index_select(2, q_t)
+        Ks = K.index_select(2, kv_t)
+        Vs = V.index_select(2, kv_t)
+        ms = torch.full((B, len(kv)), mode, dtype=torch.uint8, device=dev)
+        Os, Ls = ea.ea_hybrid_attn_prefill(Qs, Ks, Vs, ms, sink=sink, window=window, workspace=ws)
+        O.index_copy_(2, q_t, Os)
+        LSE.index_copy_(1, q_t, Ls)
+
+
+def run_serial_sweep(args, dev):
+    """Fused single launch vs Serial Dispatch over the layer sparsity ratio
+    (1..7 of 8 KV heads SSA, sink 128 / window 2048) and sequence length, on
+    the Llama-3.1-8B attention shape; one JSON line per point."""
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    B, Hq, Hkv, d, sink, window = 1, 32, 8, 128, 128, 2048
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for S in args.serial_lengths:
+        Q, K, V = wl.qkv(B, S, Hq, Hkv, d, seed=0, device=dev)
+        O = torch.empty_like(Q)
+        LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+        ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+        ws_fa = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+        ws_sa = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+        for n_sa in range(1, Hkv):
+            sa = wl.sa_heads_randperm(Hkv, n_sa, 0)
+            _, m_cpu = wl.routing_from_sa_heads(B, Hkv, sa)
+            m = m_cpu.to(dev)
+            runs = {
+                "fused": lambda: ea.ea_hybrid_attn_prefill(Q, K, V, m, sink=sink, window=window,
+                                                           O=O, LSE=LSE, workspace=ws),
+                "serial": lambda: serial_dispatch(ea, Q, K, V, m_cpu, sink, window, O, LSE,
+                                                  ws_fa, ws_sa),
+            }
+            res = {}
+            for name, fn in runs.items():
+                for _ in range(2):
+                    fn()
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(max(3, args.steps // 5)):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b))
+                res[name] = statistics.median(ts)
+            print(json.dumps({"comparison": "fused vs serial dispatch", "seq_len": S,
+                              "omega_msr_layer": n_sa / Hkv, "fused_ms": round(res["fused"], 4),
+                              "serial_ms": round(res["serial"], 4),
+                              "speedup": round(res["serial"] / res["fused"], 3)}), flush=True)
+        del Q, K, V, O, LSE
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -532,6 +606,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workload (profiling helper; prints its object)")
+    ap.add_argument("--serial-sweep", action="store_true",
+                    help="fused single launch vs Serial Dispatch (Algorithm 1(a)) sweep instead of the benchmark")
+    ap.add_argument("--serial-lengths", type=int, nargs="+", default=[16384, 32768, 65536, 131072])
     ap.add_argument("--decode-batch", type=int, default=32,
                     help="decode batch (32 is the benchmark workload; smaller for profiling)")
     args = ap.parse_args()
@@ -555,6 +632,10 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     from sparse_head_attention_gb300 import build as ea_build
     ea_build.build()
+    if args.serial_sweep:
+        if rank == 0:
+            run_serial_sweep(args, dev)
+        return 0
     if args.decode_only:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
         if rank == 0:

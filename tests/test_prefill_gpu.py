@@ -179,3 +179,20 @@ def test_xa_ssa_256k_sampled_rows(dev):
     _, m = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads, fa_impl=BLOCK, sa_impl=SSA)
     bm = wl.block_mask(cfg.B, cfg.Hkv, cfg.S, density=cfg.block_density, seed=cfg.seed)
     _full_size(dev, cfg, m, bm=bm, n_random=32)
+
+
+def test_serial_dispatch_matches_fused_launch(dev):
+    # Algorithm 1(a) (split heads, one launch per group, scatter back) must give
+    # exactly what the single fused launch gives: every head's computation is
+    # the same, only the dispatch differs.
+    import bench
+    B, S, Hq, Hkv = 1, 1500, 16, 4
+    Q, K, V = (t.to(dev) for t in wl.qkv(B, S, Hq, Hkv, 128, seed=31))
+    m_cpu = torch.tensor([[SSA, FULL, SSA, SSA]], dtype=torch.uint8)
+    O1, L1 = ea.ea_hybrid_attn_prefill(Q, K, V, m_cpu.to(dev), sink=64, window=300)
+    O2 = torch.empty_like(O1)
+    L2 = torch.empty_like(L1)
+    wss = [ea.prefill_workspace(B, S, Hq, Hkv, device=dev) for _ in range(2)]
+    bench.serial_dispatch(ea, Q, K, V, m_cpu, 64, 300, O2, L2, *wss)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
