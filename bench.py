@@ -520,6 +520,88 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+# ------------------------------------------------------------------ 36-layer routed workload
+def run_routed_layers(args, dev):
+    """Qwen3-8B-shaped attention stack: 36 layers, S=65536, 32/8 heads, SSA
+    128/2048.  One step = for every layer: the router pre-pass on that layer's K
+    (pool -> 128-64-2 MLP -> argmax -> mode), the planner and the fused prefill
+    driven by those modes.  The output bias beta of the router is set once,
+    before timing, by bisection on the device so that the model-level share of
+    SA heads is 0.75 (the pages report 0.63-0.85 at test time)."""
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    cfg = wl.QWEN_64K_36L
+    L = cfg.layers if args.layers is None else args.layers
+    layers = []
+    for l in range(L):
+        K = wl.randn_bf16((cfg.B, cfg.S, cfg.Hkv, cfg.d), seed=3 * (cfg.seed + l) + 1, device=dev)
+        layers.append(K)
+    # beta: bisect on the device router so that 75% of the L*8 decisions are SA
+    def sa_share(beta):
+        tot = 0
+        for l in range(L):
+            W, b = wl.router_weights(l, d=cfg.d, hidden=64, seed=cfg.seed, beta=beta, device=dev)
+            r, _, _ = ea.ea_route(layers[l], W, b)
+            tot += int(r.sum().item())
+        return tot / (L * cfg.Hkv)
+    lo, hi = -0.05, 0.05
+    for _ in range(40):
+        mid = 0.5 * (lo + hi)
+        if sa_share(mid) < 0.75:
+            lo = mid
+        else:
+            hi = mid
+    beta = hi
+    weights = [wl.router_weights(l, d=cfg.d, hidden=64, seed=cfg.seed, beta=beta, device=dev) for l in range(L)]
+    Qs, Vs = [], []
+    for l in range(L):
+        Qs.append(wl.randn_bf16((cfg.B, cfg.S, cfg.Hq, cfg.d), seed=3 * (cfg.seed + l), device=dev))
+        Vs.append(wl.randn_bf16((cfg.B, cfg.S, cfg.Hkv, cfg.d), seed=3 * (cfg.seed + l) + 2, device=dev))
+    O = torch.empty_like(Qs[0])
+    LSE = torch.empty(cfg.B, cfg.Hq, cfg.S, dtype=torch.float32, device=dev)
+    ws = ea.prefill_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, device=dev)
+    r_buf = [torch.empty(cfg.B, cfg.Hkv, dtype=torch.uint8, device=dev) for _ in range(L)]
+    m_buf = [torch.empty(cfg.B, cfg.Hkv, dtype=torch.uint8, device=dev) for _ in range(L)]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for l in range(L):
+            W, b = weights[l]
+            ea.ea_route(layers[l], W, b, r_out=r_buf[l], m_out=m_buf[l])
+            ea.ea_hybrid_attn_prefill(Qs[l], layers[l], Vs[l], m_buf[l], sink=cfg.sink,
+                                      window=cfg.window, O=O, LSE=LSE, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in the routed workload")
+    m_all = torch.stack([m.cpu()[0] for m in m_buf]).numpy()
+    r_all = torch.stack([r.cpu()[0] for r in r_buf]).numpy()
+    useful = tile = 0
+    for l in range(L):
+        u, t = prefill_work(cfg, m_all[l:l + 1], None)
+        useful += u
+        tile += t
+    msr, esr = ea.ea_sparsity_ratios(r_all, m_all, cfg.S, sink=cfg.sink, window=cfg.window)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ts = []
+    for _ in range(max(1, args.steps // 10)):
+        flush.zero_()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(e))
+    ms = statistics.median(ts)
+    return {"workload": cfg.name, "layers": L, "ms_per_step": round(ms, 3),
+            "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 1),
+            "visited_tile_tflops": round(tile / (ms * 1e-3) / 1e12, 1),
+            "omega_msr": msr, "omega_esr": round(esr, 4), "router_output_bias_beta": beta,
+            "step": "per layer: ea_route -> ea_hybrid_attn_prefill (planner + fused kernel)",
+            "gpu_launches_per_step": 4 * L}
+
+
 # ------------------------------------------------------------------ Algorithm 1(a) comparison
 def serial_dispatch(ea, Q, K, V, m_cpu, sink, window, O, LSE, ws_fa, ws_sa):
     """Serial Dispatch ("Paper Reading - Elastic Attention" (English notes),
@@ -606,6 +688,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workload (profiling helper; prints its object)")
+    ap.add_argument("--routed-layers", action="store_true",
+                    help="time the 36-layer router-driven 64K workload instead of the benchmark")
+    ap.add_argument("--layers", type=int, default=None, help="layers of --routed-layers (default 36)")
     ap.add_argument("--serial-sweep", action="store_true",
                     help="fused single launch vs Serial Dispatch (Algorithm 1(a)) sweep instead of the benchmark")
     ap.add_argument("--serial-lengths", type=int, nargs="+", default=[16384, 32768, 65536, 131072])
@@ -632,6 +717,10 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=dev)
     from sparse_head_attention_gb300 import build as ea_build
     ea_build.build()
+    if args.routed_layers:
+        if rank == 0:
+            print(json.dumps(run_routed_layers(args, dev)), flush=True)
+        return 0
     if args.serial_sweep:
         if rank == 0:
             run_serial_sweep(args, dev)

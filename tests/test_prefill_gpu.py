@@ -196,3 +196,24 @@ def test_serial_dispatch_matches_fused_launch(dev):
     bench.serial_dispatch(ea, Q, K, V, m_cpu, 64, 300, O2, L2, *wss)
     torch.cuda.synchronize()
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
+
+
+def test_qwen3_64k_routed_layer_sampled_rows(dev):
+    # One layer of the 36-layer 64K workload: the modes come from the oracle
+    # router on that layer's K (boundary tokens), then the fused prefill runs
+    # with them at full size; sampled rows are checked.  The first layer whose
+    # routing is mixed (some FA and some SA heads) is used.
+    import dataclasses
+    cfg = wl.QWEN_64K_36L
+    for layer in range(cfg.layers):
+        Kd = wl.randn_bf16((cfg.B, cfg.S, cfg.Hkv, cfg.d), seed=3 * (cfg.seed + layer) + 1, device=dev)
+        W, b = wl.router_weights(layer, d=cfg.d, hidden=64, seed=cfg.seed, beta=0.0015)
+        Kb = torch.cat([Kd[:, :100], Kd[:, -100:]], dim=1).cpu()
+        r, m, _, _ = oracle.route(Kb, W, b, pool_head=100, pool_tail=100)
+        if 0 < int(r.sum()) < cfg.Hkv:
+            break
+    else:
+        pytest.skip("no layer with mixed routing at this output bias")
+    del Kd
+    c = dataclasses.replace(cfg, seed=cfg.seed + layer)
+    _full_size(dev, c, torch.from_numpy(m), n_random=32)
