@@ -64,7 +64,7 @@ struct __align__(1024) PrefillSmem {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], p_ready[2], pv_done[2], o_done[2];
+    uint64_t s_full[2], p_ready[2], o_done[2];
     uint64_t item_full[2], item_empty[2];
     uint64_t teardown;
     int item[2];
@@ -384,14 +384,16 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
 // MMA issue order per item (head t in {0, 1}):
 //   QK_0(0), QK_0(1), then for every tile n:
 //   PV_n(0), QK_{n+1}(0), PV_n(1), QK_{n+1}(1).
-// P_n(t) lives in TMEM over S_t, so QK_{n+1}(t) is issued only once PV_n(t)
-// has completed (pv_done); the other head's work keeps the tensor core busy
-// meanwhile.
+// P_n(t) lives in TMEM over S_t and QK_{n+1}(t) overwrites those columns.  It
+// is issued right behind PV_n(t) by the same thread, relying on tcgen05.mma
+// operations of one thread executing in issue order (PV_n(t) has read its A
+// operand before QK_{n+1}(t) writes its accumulator); the GPU parity tests
+// cover every tile of this hand-off.
 __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem, int lane)
 {
     uint32_t *err = &a.hdr->error;
     uint32_t kv_it = 0, q_it = 0;
-    uint32_t pv_cnt0 = 0, pv_cnt1 = 0, p_cnt0 = 0, p_cnt1 = 0;
+    uint32_t p_cnt0 = 0, p_cnt1 = 0;
     const uint32_t q_addr0 = smem_u32(sm.q[0]), q_addr1 = smem_u32(sm.q[1]);
     bool ok = true;
 
@@ -403,12 +405,8 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
         tc_fence_after();
         return true;
     };
-    // S_t = Q_t K^T once P_{n-1}(t) has been consumed
+    // S_t = Q_t K^T (behind PV_{n-1}(t) in issue order)
     auto issue_qk = [&](int t, int sK) -> bool {
-        const uint32_t pv_cnt = t ? pv_cnt1 : pv_cnt0;
-        if (pv_cnt > 0 && !mbar_wait(&sm.pv_done[t], (pv_cnt - 1) & 1, &sm.abort, err))
-            return false;
-        tc_fence_after();
         if (lane == 0) {
             const uint32_t kaddr = smem_u32(sm.kv[sK]);
             const uint32_t qaddr = t ? q_addr1 : q_addr0;
@@ -437,15 +435,10 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
                 tc_mma_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8,
                           sdesc_sw128(vaddr + k * 2048, kHalfBytes, 1024), kIdescPV,
                           (acc || k > 0) ? 1u : 0u);
-            tc_commit(&sm.pv_done[t]);
             if (last)
                 tc_commit(&sm.o_done[t]);
         }
         __syncwarp();
-        if (t)
-            ++pv_cnt1;
-        else
-            ++pv_cnt0;
         return true;
     };
 
@@ -720,7 +713,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
             mbar_init(&sm.s_full[t], 1);
             mbar_init(&sm.p_ready[t], 128);
-            mbar_init(&sm.pv_done[t], 1);
             mbar_init(&sm.o_done[t], 1);
             mbar_init(&sm.item_full[t], 1);
             mbar_init(&sm.item_empty[t], 1 + 256);
