@@ -416,26 +416,58 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 }
 
-// One CTA of 128 threads per (q head, b): log-sum-exp merge of the unit's chunks.
+// One CTA of 128 threads per (q head, b): log-sum-exp merge of the unit's
+// chunks.  Warp 0 computes the maximum and the weight sum of the partial LSEs
+// (lanes over chunks); then each thread (one head dimension) sums the
+// weighted partial outputs with eight loads in flight.
 __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a)
 {
-    const int qh = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+    __shared__ float stat[2];
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const float LOG2E = 1.4426950408889634f;
+    const int qh = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
     const int u = b * a.Hkv + qh / a.g, hh = qh % a.g;
     const int first = a.unit_first[u], ns = a.unit_splits[u];
-    float M = NEG_INF;
-    for (int s = 0; s < ns; ++s)
-        M = fmaxf(M, a.part_lse[static_cast<int64_t>(first + s) * a.g + hh]);
-    float wsum = 0.f, osum = 0.f;
-    if (M > NEG_INF)
-        for (int s = 0; s < ns; ++s) {
-            const int64_t pidx = static_cast<int64_t>(first + s) * a.g + hh;
-            const float w = __expf(a.part_lse[pidx] - M);
-            wsum += w;
-            osum += w * a.part_o[pidx * EA_HEAD_DIM + dd];
+    const int64_t base = static_cast<int64_t>(first) * a.g + hh;
+    if (dd < 32) {
+        float M = NEG_INF;
+        for (int s = dd; s < ns; s += 32)
+            M = fmaxf(M, a.part_lse[base + static_cast<int64_t>(s) * a.g]);
+        for (int o = 16; o > 0; o >>= 1)
+            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float wsum = 0.f;
+        if (M > NEG_INF)
+            for (int s = dd; s < ns; s += 32)
+                wsum += ex2((a.part_lse[base + static_cast<int64_t>(s) * a.g] - M) * LOG2E);
+        for (int o = 16; o > 0; o >>= 1)
+            wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        if (dd == 0) {
+            stat[0] = M;
+            stat[1] = wsum;
         }
-    const float out = wsum > 0.f ? osum / wsum : 0.f;
-    a.O[b * a.o_sb + qh * a.o_sh + dd] = __float2bfloat16_rn(out);
+    }
+    __syncthreads();
+    const float M = stat[0], wsum = stat[1];
+    float osum = 0.f;
+    if (M > NEG_INF) {
+        int s = 0;
+        for (; s + 8 <= ns; s += 8) {
+            float l[8], o[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                l[k] = a.part_lse[base + static_cast<int64_t>(s + k) * a.g];
+                o[k] = a.part_o[(base + static_cast<int64_t>(s + k) * a.g) * EA_HEAD_DIM + dd];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                osum += ex2((l[k] - M) * LOG2E) * o[k];
+        }
+        for (; s < ns; ++s) {
+            const int64_t pidx = base + static_cast<int64_t>(s) * a.g;
+            osum += ex2((a.part_lse[pidx] - M) * LOG2E) * a.part_o[pidx * EA_HEAD_DIM + dd];
+        }
+    }
+    a.O[b * a.o_sb + qh * a.o_sh + dd] = __float2bfloat16_rn(wsum > 0.f ? osum / wsum : 0.f);
     if (dd == 0 && a.LSE)
         a.LSE[static_cast<int64_t>(b) * a.Hq + qh] = wsum > 0.f ? M + __logf(wsum) : NEG_INF;
 }
