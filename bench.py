@@ -103,6 +103,17 @@ def decode_kept_bytes(cfg, m):
     return keys * 2 * cfg.d * 2
 
 
+def job_throughput(local_ms, world, work_per_rank_step, steps, device):
+    """Whole-job throughput of N replicas: the timed region is the slowest
+    rank's (max over ranks), the work is every rank's (weak scaling, each rank
+    processes its own batch).  Returns (max ms, work units per second / 1e12)."""
+    if world > 1:
+        t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        local_ms = float(t.item())
+    return local_ms, world * work_per_rank_step * steps / (local_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ environment
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -279,12 +290,8 @@ def run_ours(args, rank, world, dev):
     kern_ms = [a.elapsed_time(b) for a, b in ev_k]
     if ea.ea_check_errors(ws) != 0:
         raise RuntimeError("device error during the timed steps")
-    if world > 1:
-        t = torch.tensor([step_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms, value = job_throughput(step_ms, world, useful_flops, args.steps, dev)
     ms_per_step = step_ms / args.steps
-    value = world * useful_flops * args.steps / (step_ms * 1e-3) / 1e12
 
     peaks = measured_peaks()
     k_ms = statistics.mean(kern_ms)

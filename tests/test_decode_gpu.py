@@ -91,3 +91,26 @@ def test_full_workload_sampled_sequences(dev):
                                    sl[b:b + 1].cpu(), m[b:b + 1], sink=cfg.sink, window=cfg.window)
         assert_close(O[b:b + 1].float().cpu().numpy(), LSE[b:b + 1].cpu().numpy(), Oref, Lref,
                      "b=%d" % b)
+
+
+def test_strided_query_cache_and_output(dev):
+    # q as a slice of a wider projection, the cache as a view of a larger
+    # [B, Lmax, heads, d] buffer, O written into a slice of a wider output.
+    B, Hq, Hkv, d, Lmax = 2, 8, 2, 128, 1500
+    proj = wl.randn_bf16((B, Hq + 4, d), seed=61)
+    cache = wl.randn_bf16((B, Lmax, Hkv + 2, d), seed=62)
+    q = proj[:, 2:2 + Hq]
+    Kc, Vc = cache[:, :, :Hkv], cache[:, :, 2:]
+    seqlens = torch.tensor([1500, 777], dtype=torch.int32)
+    modes = np.array([[FULL, SSA], [SSA, FULL]], np.uint8)
+    pd, cd = proj.to(dev), cache.to(dev)
+    Ob = torch.full((B, Hq + 3, d), 5.0, dtype=torch.bfloat16, device=dev)
+    ws = ea.decode_workspace(B, Hq, Hkv, Lmax, device=dev)
+    ea.ea_hybrid_attn_decode(pd[:, 2:2 + Hq], cd[:, :, :Hkv], cd[:, :, 2:], seqlens.to(dev),
+                             torch.as_tensor(modes).to(dev), sink=32, window=400, O=Ob[:, 1:1 + Hq],
+                             workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Oref, _ = oracle.decode(q, Kc, Vc, seqlens, modes, sink=32, window=400)
+    assert np.abs(Ob[:, 1:1 + Hq].float().cpu().numpy() - Oref).max() <= 1e-2
+    assert (Ob[:, 0].float() == 5.0).all() and (Ob[:, 1 + Hq:].float() == 5.0).all()

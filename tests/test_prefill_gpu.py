@@ -217,3 +217,20 @@ def test_qwen3_64k_routed_layer_sampled_rows(dev):
     del Kd
     c = dataclasses.replace(cfg, seed=cfg.seed + layer)
     _full_size(dev, c, torch.from_numpy(m), n_random=32)
+
+
+def test_one_plan_feeds_several_launches(dev):
+    # ea_prefill_plan once, ea_prefill_attend twice on other inputs: the queue
+    # re-arms itself after each launch and both results match the oracle.
+    B, S, Hq, Hkv = 1, 700, 8, 2
+    modes = torch.tensor([[FULL, SSA]], dtype=torch.uint8, device=dev)
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    ea.ea_prefill_plan(B, S, Hq, Hkv, modes, sink=16, window=200, workspace=ws)
+    for seed in (41, 42):
+        Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=seed)
+        O, LSE = ea.ea_prefill_attend(Q.to(dev), K.to(dev), V.to(dev), modes, sink=16, window=200,
+                                      workspace=ws)
+        torch.cuda.synchronize()
+        check_no_device_error(ws)
+        Oref, Lref = oracle.prefill_full(Q, K, V, modes.cpu(), sink=16, window=200)
+        assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "seed %d" % seed)
