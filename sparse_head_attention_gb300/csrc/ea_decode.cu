@@ -476,14 +476,18 @@ static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, c
                                  int grid, cudaStream_t st)
 {
     const size_t smem = sizeof(DecSmem) + 1024;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    static bool attr_done[64] = {};   // the attribute is set once per device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev >= 64 || !attr_done[dev]) {
+        e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
         if (e != cudaSuccess)
             return e;
-        attr = true;
+        if (dev < 64)
+            attr_done[dev] = true;
     }
     decode_split_kernel<<<grid, kDecThreads, smem, st>>>(tk, tv, a);
     return cudaGetLastError();

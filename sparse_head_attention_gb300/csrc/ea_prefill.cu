@@ -879,14 +879,10 @@ extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void 
     if ((s = ensure_attributes()) != EA_OK)
         return s;
     // The register split inside the kernel assumes this launch size.
-    static int launch_regs = -1;
-    if (launch_regs < 0) {
-        cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, hybrid_prefill_kernel) != cudaSuccess)
-            return EA_ERR_CUDA;
-        launch_regs = fa.numRegs;
-    }
-    if (launch_regs != kLaunchRegs)
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, hybrid_prefill_kernel) != cudaSuccess)
+        return EA_ERR_CUDA;
+    if (fa.numRegs != kLaunchRegs)
         return EA_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
