@@ -234,3 +234,49 @@ def test_one_plan_feeds_several_launches(dev):
         check_no_device_error(ws)
         Oref, Lref = oracle.prefill_full(Q, K, V, modes.cpu(), sink=16, window=200)
         assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "seed %d" % seed)
+
+
+def test_random_small_configurations(dev):
+    # Seeded sweep over ragged lengths, group sizes, mixed modes per head,
+    # sink/window settings and block masks; every row against the oracle.
+    rng = np.random.default_rng(2024)
+    for case in range(12):
+        B = int(rng.integers(1, 3))
+        S = int(rng.integers(1, 700))
+        Hkv = int(rng.integers(1, 4))
+        g = int(rng.integers(1, 5))
+        Hq = Hkv * g
+        sink = int(rng.integers(0, 200))
+        window = int(rng.integers(1, 400))
+        modes = rng.integers(0, 3, size=(B, Hkv)).astype(np.uint8)
+        Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=1000 + case)
+        bm = wl.block_mask(B, Hkv, S, density=float(rng.uniform(0.1, 0.9)), seed=case).numpy()
+        bm[rng.random(bm.shape) < 0.1] = 0            # drop some diagonal / first blocks too
+        O, LSE, vis = run(dev, Q, K, V, modes, sink, window, bm=bm, visited=True)
+        Oref, Lref = oracle.prefill_full(Q, K, V, modes, sink=sink, window=window, block_mask=bm)
+        what = "case %d (B=%d S=%d Hq=%d Hkv=%d sink=%d window=%d modes=%s)" % (
+            case, B, S, Hq, Hkv, sink, window, modes.tolist())
+        assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, what)
+        nB = (S + 127) // 128
+        np.testing.assert_array_equal(
+            bitmap_to_tiles(vis, B, Hkv, nB),
+            oracle.visited(B, S, Hkv, modes, sink=sink, window=window, block_mask=bm), err_msg=what)
+
+
+def test_longest_supported_sequence(dev):
+    # S = 2^21 (the planner's limit): streaming heads only, sampled rows.
+    B, S, Hq, Hkv, sink, window = 1, 1 << 21, 2, 1, 128, 300
+    Qd, Kd, Vd = wl.qkv(B, S, Hq, Hkv, 128, seed=77, device=dev)
+    m = torch.tensor([[SSA]], dtype=torch.uint8)
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Qd, Kd, Vd, m.to(dev), sink=sink, window=window, workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    rows_i = np.array([0, 1, 127, 128, 299, 300, 301, 4095, S // 2, S - 129, S - 1], dtype=np.int64)
+    rows = np.array([[0, qh, i] for qh in range(Hq) for i in rows_i])
+    Oref, Lref = oracle.prefill_rows(Qd.cpu(), Kd.cpu(), Vd.cpu(), m, rows, sink=sink, window=window)
+    idx = torch.from_numpy(rows).to(dev)
+    assert_close(O[idx[:, 0], idx[:, 2], idx[:, 1]].float().cpu().numpy(),
+                 LSE[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy(), Oref, Lref, "S=2^21")
+    with pytest.raises(ValueError):
+        ea.prefill_workspace(B, S + 1, Hq, Hkv, device=dev)
