@@ -433,25 +433,73 @@ def run_decode(args, dev, peaks, flush):
 
 
 def run_router(dev):
+    """Router pre-pass timings: all 36 layers of the 64K workload in one
+    ea_route_layers launch (the form the pre-pass takes when a model's K states
+    are at hand), the same 36 layers as 36 ea_route launches, and one layer at
+    S = 4K / 64K / 1M to show that the cost does not grow with length."""
     import sparse_head_attention_gb300 as ea
     from sparse_head_attention_gb300 import workloads as wl
     cfg = wl.QWEN_64K_36L
+    L = cfg.layers
+    # the router reads only the boundary tokens, so one resident K serves
+    # every layer; each layer has its own weights
     K = wl.randn_bf16((1, cfg.S, cfg.Hkv, cfg.d), seed=1, device=dev)
-    W, b = wl.router_weights(0, d=cfg.d, hidden=64, device=dev)
-    r = torch.empty(1, cfg.Hkv, dtype=torch.uint8, device=dev)
+    wb = [wl.router_weights(l, d=cfg.d, hidden=64, device=dev) for l in range(L)]
+    Ks = [K] * L
+    r = torch.empty(L, 1, cfg.Hkv, dtype=torch.uint8, device=dev)
     mm = torch.empty_like(r)
-    for _ in range(3):
-        ea.ea_route(K, W, b, r_out=r, m_out=mm)
-    torch.cuda.synchronize()
-    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = 36
-    a.record()
-    for _ in range(n):
-        ea.ea_route(K, W, b, r_out=r, m_out=mm)
-    e.record()
-    torch.cuda.synchronize()
-    return {"workload": "router pre-pass, 8 KV heads, S=65536, MLP 128-64-2, per layer",
-            "us_per_layer": round(1000 * a.elapsed_time(e) / n, 2)}
+    lg = torch.empty(L, 1, cfg.Hkv, 2, dtype=torch.float64, device=dev)
+
+    def timed(fn, n=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        e.record()
+        torch.cuda.synchronize()
+        return 1000 * a.elapsed_time(e) / n
+
+    def one_launch():
+        ea.ea_route_layers(Ks, [w for w, _ in wb], [b for _, b in wb], r_out=r, m_out=mm,
+                           logits_out=lg)
+
+    def per_layer():
+        for l in range(L):
+            ea.ea_route(K, *wb[l], r_out=r[l], m_out=mm[l], logits_out=lg[l])
+
+    def graphed(fn):
+        # device time alone: the calls replayed from a CUDA graph
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return timed(g.replay)
+
+    us_all = timed(one_launch)
+    us_per = timed(per_layer)
+    us_all_dev = graphed(one_launch)
+    us_per_dev = graphed(per_layer)
+    by_len = {}
+    for S in (4096, 65536, 1 << 20):
+        Kl = wl.randn_bf16((1, S, cfg.Hkv, cfg.d), seed=2, device=dev)
+        by_len[str(S)] = round(timed(lambda: ea.ea_route(Kl, *wb[0], r_out=r[0], m_out=mm[0],
+                                                         logits_out=lg[0])), 2)
+        del Kl
+    return {"workload": "router pre-pass, 8 KV heads, boundary 100+100 tokens, MLP 128-64-2",
+            "us_36_layers_one_launch": round(us_all, 2),
+            "us_36_layers_per_layer_launches": round(us_per, 2),
+            "us_36_layers_one_launch_graph": round(us_all_dev, 2),
+            "us_36_layers_per_layer_launches_graph": round(us_per_dev, 2),
+            "us_one_layer_by_seq_len": by_len,
+            "note": "eager figures include the host-side call (argument marshalling); "
+                    "graph figures are device time of the same calls replayed from a CUDA graph"}
 
 
 # ------------------------------------------------------------------ oracle
@@ -545,12 +593,10 @@ def run_routed_layers(args, dev):
         layers.append(K)
     # beta: bisect on the device router so that 75% of the L*8 decisions are SA
     def sa_share(beta):
-        tot = 0
-        for l in range(L):
-            W, b = wl.router_weights(l, d=cfg.d, hidden=64, seed=cfg.seed, beta=beta, device=dev)
-            r, _, _ = ea.ea_route(layers[l], W, b)
-            tot += int(r.sum().item())
-        return tot / (L * cfg.Hkv)
+        wb = [wl.router_weights(l, d=cfg.d, hidden=64, seed=cfg.seed, beta=beta, device=dev)
+              for l in range(L)]
+        r, _, _ = ea.ea_route_layers(layers, [w for w, _ in wb], [b for _, b in wb])
+        return int(r.sum().item()) / (L * cfg.Hkv)
     lo, hi = -0.05, 0.05
     for _ in range(40):
         mid = 0.5 * (lo + hi)

@@ -103,6 +103,25 @@ ea_status ea_route(const void *K, const int64_t k_strides[4], int B, int S, int 
                    int pool_head, int pool_tail, const ea_mlp *mlp, ea_policy policy,
                    uint8_t *r_out, uint8_t *m_out, double *logits_out, void *stream);
 
+/*
+ * ea_route_layers - ea_route for L layers in one launch (all layers' routing
+ * decisions of one input at once; the router reads only the boundary tokens,
+ * so the whole pre-pass of a model is one short kernel).
+ *
+ *   K_layers   host array of L device pointers, layer l's K as in ea_route
+ *              (all layers share k_strides, B, S, Hkv, d)
+ *   mlps       host array of L ea_mlp (per-layer weights; same shapes rules)
+ *   r_out, m_out  device uint8 [L][B][Hkv]; logits_out device double
+ *              [L][B][Hkv][2] or NULL
+ * Up to 64 layers take one kernel launch (more take one per 64 layers).
+ * Limits: 1 <= L <= 1024.  Errors as for ea_route; every layer's arguments
+ * are checked before anything is enqueued, so an error launches nothing.
+ */
+ea_status ea_route_layers(const void *const *K_layers, int L, const int64_t k_strides[4], int B,
+                          int S, int Hkv, int d, int pool_head, int pool_tail, const ea_mlp *mlps,
+                          ea_policy policy, uint8_t *r_out, uint8_t *m_out, double *logits_out,
+                          void *stream);
+
 /* Bytes of device workspace ea_hybrid_attn_prefill needs for these sizes
  * (0 on invalid sizes).  The workspace must be 256-byte aligned. */
 size_t ea_prefill_workspace_size(int B, int S, int Hq, int Hkv, int d);

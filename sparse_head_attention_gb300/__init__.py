@@ -7,6 +7,7 @@ library ``_lib/libea.so``.  If that library is missing, or no CUDA device is
 present, the device entry points raise instead of computing anything else.
 
     ea_route                 router pre-pass (pool -> MLP -> argmax -> mode)
+    ea_route_layers          the router pre-pass of many model layers in one launch
     ea_hybrid_attn_prefill   fused FA / SSA / block-sparse prefill, one launch
     ea_hybrid_attn_decode    split-KV decode with the prefill-time routing
     ea_sparsity_ratios       Omega_MSR / Omega_ESR (host)
@@ -29,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libea.so")
 _lib = None
 
 # Function names exported by the library (the ones include/ea.h declares).
-EXPORTS = ("ea_status_string", "ea_route", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
+EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
            "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
            "ea_decode_workspace_size",
            "ea_hybrid_attn_decode", "ea_sparsity_ratios", "ea_check_errors")
@@ -64,6 +65,8 @@ def lib():
         L.ea_status_string.restype = ctypes.c_char_p
         L.ea_route.argtypes = [P, P, i32, i32, i32, i32, i32, i32, ctypes.POINTER(_Mlp), _Policy,
                                P, P, P, P]
+        L.ea_route_layers.argtypes = [P, i32, P, i32, i32, i32, i32, i32, i32, P, _Policy,
+                                      P, P, P, P]
         L.ea_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         L.ea_prefill_workspace_size.restype = sz
         L.ea_hybrid_attn_prefill.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
@@ -80,7 +83,7 @@ def lib():
         L.ea_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
                                          ctypes.POINTER(f64), ctypes.POINTER(f64)]
         L.ea_check_errors.argtypes = [P, P]
-        for f in ("ea_route", "ea_hybrid_attn_prefill", "ea_prefill_plan", "ea_prefill_attend",
+        for f in ("ea_route", "ea_route_layers", "ea_hybrid_attn_prefill", "ea_prefill_plan", "ea_prefill_attend",
                   "ea_hybrid_attn_decode",
                   "ea_sparsity_ratios", "ea_check_errors"):
             getattr(L, f).restype = ctypes.c_int
@@ -114,6 +117,17 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+def _mlp_struct(weights, biases):
+    """(ea_mlp, keep-alive list) for float32 CUDA weights [out, in] and biases [out]."""
+    Ws = [_dev(w, "W", torch.float32).contiguous() for w in weights]
+    bs = [_dev(b, "b", torch.float32).contiguous() for b in biases]
+    dims = [Ws[0].shape[1]] + [w.shape[0] for w in Ws]
+    c_dims = (ctypes.c_int * len(dims))(*dims)
+    c_W = (ctypes.c_void_p * len(Ws))(*[w.data_ptr() for w in Ws])
+    c_b = (ctypes.c_void_p * len(bs))(*[b.data_ptr() for b in bs])
+    return _Mlp(len(Ws), c_dims, c_W, c_b), [Ws, bs, c_dims, c_W, c_b]
+
+
 def ea_route(K, weights, biases, *, pool_head=100, pool_tail=100, policy=(FULL, SSA),
              r_out=None, m_out=None, logits_out=None, stream=None):
     """Router pre-pass on K [B, S, Hkv, d] (bf16, CUDA).  weights/biases: lists of
@@ -125,17 +139,43 @@ def ea_route(K, weights, biases, *, pool_head=100, pool_tail=100, policy=(FULL, 
     m_out = m_out if m_out is not None else torch.empty(B, Hkv, dtype=torch.uint8, device=dev)
     if logits_out is None:
         logits_out = torch.empty(B, Hkv, 2, dtype=torch.float64, device=dev)
-    Ws = [_dev(w, "W", torch.float32).contiguous() for w in weights]
-    bs = [_dev(b, "b", torch.float32).contiguous() for b in biases]
-    dims = [Ws[0].shape[1]] + [w.shape[0] for w in Ws]
-    c_dims = (ctypes.c_int * len(dims))(*dims)
-    c_W = (ctypes.c_void_p * len(Ws))(*[w.data_ptr() for w in Ws])
-    c_b = (ctypes.c_void_p * len(bs))(*[b.data_ptr() for b in bs])
-    mlp = _Mlp(len(Ws), c_dims, c_W, c_b)
+    mlp, _keep = _mlp_struct(weights, biases)
     st = lib().ea_route(_ptr(K), _strides(K), B, S, Hkv, d, pool_head, pool_tail,
                         ctypes.byref(mlp), _Policy(*policy), _ptr(r_out), _ptr(m_out),
                         _ptr(logits_out), _stream(stream))
     _check("ea_route", st)
+    return r_out, m_out, logits_out
+
+
+def ea_route_layers(K_layers, weights, biases, *, pool_head=100, pool_tail=100,
+                    policy=(FULL, SSA), r_out=None, m_out=None, logits_out=None, stream=None):
+    """Router pre-pass of L layers at once.  K_layers: L bf16 CUDA tensors
+    [B, S, Hkv, d] with equal shapes and strides; weights[l] / biases[l]: layer
+    l's MLP as for ea_route.  Returns (r [L, B, Hkv], m [L, B, Hkv],
+    logits [L, B, Hkv, 2])."""
+    L = len(K_layers)
+    if L < 1 or len(weights) != L or len(biases) != L:
+        raise ValueError("K_layers, weights and biases need one entry per layer")
+    K0 = _dev(K_layers[0], "K", torch.bfloat16)
+    for K in K_layers:
+        _dev(K, "K", torch.bfloat16)
+        if K.shape != K0.shape or K.stride() != K0.stride():
+            raise ValueError("every layer's K needs the same shape and strides")
+    B, S, Hkv, d = K0.shape
+    dev = K0.device
+    if r_out is None:
+        r_out = torch.empty(L, B, Hkv, dtype=torch.uint8, device=dev)
+    if m_out is None:
+        m_out = torch.empty(L, B, Hkv, dtype=torch.uint8, device=dev)
+    if logits_out is None:
+        logits_out = torch.empty(L, B, Hkv, 2, dtype=torch.float64, device=dev)
+    built = [_mlp_struct(w, b) for w, b in zip(weights, biases)]
+    mlps = (_Mlp * L)(*[m for m, _ in built])
+    ptrs = (ctypes.c_void_p * L)(*[K.data_ptr() for K in K_layers])
+    st = lib().ea_route_layers(ptrs, L, _strides(K0), B, S, Hkv, d, pool_head, pool_tail, mlps,
+                               _Policy(*policy), _ptr(r_out), _ptr(m_out), _ptr(logits_out),
+                               _stream(stream))
+    _check("ea_route_layers", st)
     return r_out, m_out, logits_out
 
 

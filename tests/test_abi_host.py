@@ -187,3 +187,31 @@ def test_device_entry_points_fail_loudly_without_gpu():
     with pytest.raises(ValueError):
         ea.ea_hybrid_attn_prefill(Q, Q[:, :, :2], Q[:, :, :2], torch.zeros(1, 2, dtype=torch.uint8),
                                   sink=0, window=1)
+
+
+def test_route_layers_rejects_bad_arguments(L):
+    good_dims = (ctypes.c_int * 3)(128, 64, 2)
+    bad_dims = (ctypes.c_int * 3)(128, 64, 3)
+    W = (ctypes.c_void_p * 2)(0x1000, 0x2000)
+    b = (ctypes.c_void_p * 2)(0x3000, 0x4000)
+    strides = _str(65536 * 8 * 128, 8 * 128, 128, 1)
+
+    def call(n, mlps, ptrs, **kw):
+        a = dict(S=65536, ph=100, pt=100, r=_fake(), m=_fake())
+        a.update(kw)
+        return L.ea_route_layers(ptrs, n, strides, 1, a["S"], 8, 128, a["ph"], a["pt"], mlps,
+                                 ea._Policy(0, 1), a["r"], a["m"], None, None)
+
+    # layer 70 of 72 (in the second launch's chunk) has a bad MLP: the call
+    # fails before the first launch (the fake pointers are never dereferenced)
+    mlps = (ea._Mlp * 72)(*[ea._Mlp(2, bad_dims if l == 70 else good_dims, W, b) for l in range(72)])
+    ptrs = (ctypes.c_void_p * 72)(*([0x1000] * 72))
+    assert call(72, mlps, ptrs) == 1
+    good = (ea._Mlp * 2)(ea._Mlp(2, good_dims, W, b), ea._Mlp(2, good_dims, W, b))
+    assert call(0, good, (ctypes.c_void_p * 2)(0x1000, 0x1000)) == 1          # no layers
+    assert call(2, good, (ctypes.c_void_p * 2)(0x1000, None)) == 1            # a null K
+    assert call(2, good, (ctypes.c_void_p * 2)(0x1000, 0x1000), ph=0, pt=0) == 1
+    assert call(2, good, (ctypes.c_void_p * 2)(0x1000, 0x1000), r=None) == 1
+    deep = (ctypes.c_int * 6)(128, 64, 64, 64, 64, 2)                          # 5 dense layers
+    W5 = (ctypes.c_void_p * 5)(*([0x1000] * 5))
+    assert call(1, (ea._Mlp * 1)(ea._Mlp(5, deep, W5, W5)), (ctypes.c_void_p * 1)(0x1000)) == 2

@@ -57,3 +57,44 @@ def test_36_layer_64k_workload_bit_exact(dev):
         np.testing.assert_array_equal(r.cpu().numpy(), ro)
         np.testing.assert_array_equal(m.cpu().numpy(), mo)
         assert np.abs(lo[..., 1] - lo[..., 0]).min() > 1e-9     # decisions are not near ties
+
+
+def test_route_layers_two_launches_mixed_mlps(dev):
+    # 70 layers take two launches (64 + 6); layers alternate between a 1-layer,
+    # a 2-layer and a 3-layer MLP, and pooling windows overlap (S < 200).
+    L, B, S, Hkv, d = 70, 3, 150, 2, 128
+    stack = wl.randn_bf16((L, B, S, Hkv, d), seed=77, device=dev)
+    Ks = [stack[l] for l in range(L)]
+    Ws, bs = [], []
+    g = torch.Generator().manual_seed(78)
+    for l in range(L):
+        dims = [[d, 2], [d, 64, 2], [d, 32, 16, 2]][l % 3]
+        Ws.append([(torch.randn(o, i, generator=g) * 0.05).float().to(dev)
+                   for i, o in zip(dims[:-1], dims[1:])])
+        bs.append([(torch.randn(o, generator=g) * 0.01).float().to(dev) for o in dims[1:]])
+    r, m, logits = ea.ea_route_layers(Ks, Ws, bs, policy=(ea.BLOCK, ea.SSA))
+    torch.cuda.synchronize()
+    r, m, logits = r.cpu().numpy(), m.cpu().numpy(), logits.cpu().numpy()
+    for l in range(L):
+        ro, mo, lo, _ = oracle.route(Ks[l].cpu(), [w.cpu() for w in Ws[l]], [x.cpu() for x in bs[l]],
+                                     pool_head=100, pool_tail=100, fa_impl=ea.BLOCK, sa_impl=ea.SSA)
+        np.testing.assert_array_equal(logits[l], lo, err_msg="layer %d" % l)
+        np.testing.assert_array_equal(r[l], ro, err_msg="layer %d" % l)
+        np.testing.assert_array_equal(m[l], mo, err_msg="layer %d" % l)
+
+
+def test_route_layers_equals_per_layer_route_on_64k_workload(dev):
+    cfg = wl.QWEN_64K_36L
+    Ks = [wl.randn_bf16((cfg.B, cfg.S, cfg.Hkv, cfg.d), seed=3 * (cfg.seed + l) + 1, device=dev)
+          for l in range(cfg.layers)]
+    wb = [wl.router_weights(l, d=cfg.d, hidden=64, seed=cfg.seed, beta=0.0015, device=dev)
+          for l in range(cfg.layers)]
+    r, m, logits = ea.ea_route_layers(Ks, [w for w, _ in wb], [b for _, b in wb])
+    for l in range(cfg.layers):
+        r1, m1, lg1 = ea.ea_route(Ks[l], *wb[l])
+        torch.cuda.synchronize()
+        assert torch.equal(logits[l], lg1) and torch.equal(r[l], r1) and torch.equal(m[l], m1), l
+    # one layer against the oracle as well, on its 200 boundary tokens
+    Kb = torch.cat([Ks[5][:, :100], Ks[5][:, -100:]], dim=1).cpu()
+    _, _, lo, _ = oracle.route(Kb, [w.cpu() for w in wb[5][0]], [x.cpu() for x in wb[5][1]])
+    np.testing.assert_array_equal(logits[5].cpu().numpy(), lo)
