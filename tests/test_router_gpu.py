@@ -98,3 +98,67 @@ def test_route_layers_equals_per_layer_route_on_64k_workload(dev):
     Kb = torch.cat([Ks[5][:, :100], Ks[5][:, -100:]], dim=1).cpu()
     _, _, lo, _ = oracle.route(Kb, [w.cpu() for w in wb[5][0]], [x.cpu() for x in wb[5][1]])
     np.testing.assert_array_equal(logits[5].cpu().numpy(), lo)
+
+
+def _extreme_K(seed, B=2, S=300, Hkv=2, d=128):
+    """K whose channels span the cases of the router's exact pooling: ordinary
+    N(0, 1) values, exponent spreads wide enough that the sequential fp64 sum
+    rounds, a spread just inside 2^53, bf16 subnormals, and signed zeros."""
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((B, S, Hkv, d)).astype(np.float32)
+    # channels 8..39: magnitudes 2^-120 .. 2^120 with random signs
+    K[..., 8:40] = (rng.choice([-1.0, 1.0], size=K[..., 8:40].shape) *
+                    np.exp2(rng.integers(-120, 121, size=K[..., 8:40].shape))).astype(np.float32)
+    # channel 40: 2^40 once among 2^-7 values -> beyond 2^53 quanta, fp64 rounds
+    K[..., 40] = 2.0 ** -7
+    K[:, 150, :, 40] = 2.0 ** 40
+    # channel 41: 2^30 among 2^-10 values -> exact in fp64 (not in fp32)
+    K[..., 41] = 2.0 ** -10
+    K[:, 20, :, 41] = 2.0 ** 30
+    # channel 42: bf16 subnormals and the smallest normal
+    K[..., 42] = rng.choice([2.0 ** -133, -3 * 2.0 ** -133, 2.0 ** -126, 0.0], size=K[..., 42].shape)
+    # channel 43: signed zeros only; channel 44: +x and -x pairs that cancel exactly
+    K[..., 43] = rng.choice([0.0, -0.0], size=K[..., 43].shape)
+    K[:, 0::2, :, 44] = 3.25
+    K[:, 1::2, :, 44] = -3.25
+    return torch.from_numpy(K).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_pooling_extreme_values_bit_exact(dev, seed):
+    K = _extreme_K(seed)
+    W, b = wl.router_weights(seed, d=128, hidden=64, device=dev)
+    r, m, logits = ea.ea_route(K.to(dev), W, b)
+    torch.cuda.synchronize()
+    ro, mo, lo, _ = oracle.route(K, [w.cpu() for w in W], [x.cpu() for x in b])
+    np.testing.assert_array_equal(logits.cpu().numpy(), lo)
+    np.testing.assert_array_equal(r.cpu().numpy(), ro)
+    # the same through a 1-layer MLP that passes two pooled channels straight
+    # to the logits, so each pooled value is compared on its own
+    for c0, c1 in ((40, 41), (42, 43), (44, 8), (9, 10), (0, 1)):
+        W1 = torch.zeros(2, 128)
+        W1[0, c0] = 1.0
+        W1[1, c1] = 1.0
+        _, _, lg = ea.ea_route(K.to(dev), [W1.to(dev)], [torch.zeros(2, device=dev)])
+        torch.cuda.synchronize()
+        _, _, lo1, pooled = oracle.route(K, [W1], [torch.zeros(2)])
+        np.testing.assert_array_equal(lg.cpu().numpy(), lo1, err_msg="channels %d,%d" % (c0, c1))
+        np.testing.assert_array_equal(lg.cpu().numpy()[..., 0], pooled[..., c0])
+
+
+def test_pooling_infinite_and_nan_values(dev):
+    K = _extreme_K(5).float()
+    K[0, 10, 0, 3] = float("inf")
+    K[1, 290, 1, 4] = float("nan")
+    K[1, 20, 0, 5] = float("-inf")
+    K = K.to(torch.bfloat16)
+    for c0, c1 in ((3, 4), (5, 6)):
+        W1 = torch.zeros(2, 128)
+        W1[0, c0] = 1.0
+        W1[1, c1] = 1.0
+        _, _, lg = ea.ea_route(K.to(dev), [W1.to(dev)], [torch.zeros(2, device=dev)])
+        torch.cuda.synchronize()
+        _, _, lo1, _ = oracle.route(K, [W1], [torch.zeros(2)])
+        got, want = lg.cpu().numpy(), lo1
+        assert np.array_equal(np.isnan(got), np.isnan(want))
+        np.testing.assert_array_equal(np.nan_to_num(got), np.nan_to_num(want))
