@@ -13,7 +13,10 @@ GB/s of the kept KV-cache bytes reported beside it.
             flushed (256 MB memset) before every timed step, outside the
             events.
   e2e       the same metric through the C ABI with pinned host buffers: Q/K/V
-            and the mode mask copied in, O and LSE copied out, every step.
+            and the mode mask copied in, O and LSE copied out, every step, by
+            one ea_hybrid_attn_prefill_host call (chunks of query blocks, so
+            the copies overlap the attention); the unpipelined time is given
+            beside it.
   decode    B=32 x 128K-token cache, 2 FA + 6 SSA KV heads: kept K/V bytes per
             step / step time.
   roofline  the attention kernel alone (CUDA events around its launch):
@@ -304,18 +307,29 @@ def run_ours(args, rank, world, dev):
                 "work": "visited-tile flops 4*d*128*128 per tile per query head = %.4e per launch" % tile_flops,
                 "kernel_ms": round(k_ms, 4)}
 
-    # ---- end to end through the C ABI with pinned host buffers
+    # ---- end to end through the C ABI with pinned host buffers: one
+    # ea_hybrid_attn_prefill_host call per step (Q/K/V/m[/mask] copied in,
+    # O and LSE copied back, chunked so that copies overlap the attention)
     e2e = None
     if not args.no_e2e:
         hQ = Q.cpu().pin_memory()
         hK = K.cpu().pin_memory()
         hV = V.cpu().pin_memory()
         hm = m_cpu.pin_memory()
+        hbm = None if bm is None else bm.cpu().pin_memory()
         hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
         hL = torch.empty(LSE.shape, dtype=LSE.dtype, pin_memory=True)
-        dQ, dK, dV, dm = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(m)
+        buf = ea.prefill_host_buffer(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, with_block_mask=hbm is not None,
+                                     device=dev)
 
         def e2e_step():
+            ea.ea_hybrid_attn_prefill_host(hQ, hK, hV, hm, sink=cfg.sink, window=cfg.window,
+                                           block_mask=hbm, O=hO, LSE=hL, device_buffer=buf,
+                                           n_chunks=args.e2e_chunks, stream=stream)
+
+        def serial_step():
+            # the same step without the overlap, for comparison: whole tensors
+            # up, one fused launch, whole outputs back
             dQ.copy_(hQ, non_blocking=True)
             dK.copy_(hK, non_blocking=True)
             dV.copy_(hV, non_blocking=True)
@@ -325,24 +339,35 @@ def run_ours(args, rank, world, dev):
             hO.copy_(O, non_blocking=True)
             hL.copy_(LSE, non_blocking=True)
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        e_ms = 0.0
-        n_e2e = max(3, min(args.steps, 10))
-        for _ in range(n_e2e):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            e2e_step()
-            b.record(stream)
+        def time_steps(fn, n):
+            for _ in range(2):
+                fn()
             torch.cuda.synchronize()
-            e_ms += a.elapsed_time(b)
-        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hm))
+            total = 0.0
+            for _ in range(n):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                total += a.elapsed_time(b)
+            return total
+
+        n_e2e = max(3, min(args.steps, 10))
+        e_ms = time_steps(e2e_step, n_e2e)
+        if ea.ea_check_errors(buf) != 0:
+            raise RuntimeError("device error in the end-to-end prefill")
+        dQ, dK, dV, dm = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(m)
+        s_ms = time_steps(serial_step, n_e2e)
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hm) + ((hbm,) if hbm is not None else ()))
         d2h = sum(t.numel() * t.element_size() for t in (hO, hL))
         e2e = {"value": round(world * useful_flops * n_e2e / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(e_ms / n_e2e, 3)}
-        del hQ, hK, hV, dQ, dK, dV
+               "ms_per_step": round(e_ms / n_e2e, 3),
+               "call": "ea_hybrid_attn_prefill_host (chunked copies overlapped with the attention, "
+                       "%s chunks)" % (args.e2e_chunks or "8"),
+               "serial_ms_per_step": round(s_ms / n_e2e, 3)}
+        del hQ, hK, hV, dQ, dK, dV, buf
 
     # ---- decode
     decode = None
@@ -737,6 +762,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama32k", choices=["llama32k", "tiny", "xa256k"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="chunks of the end-to-end pipelined call (0 = the library's choice)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true",

@@ -232,6 +232,64 @@ ea_status ea_hybrid_attn_prefill_noalloc(const void *Q, const void *K, const voi
                                          const uint8_t *block_mask, int block_size,
                                          uint32_t *visited_bitmap, void *stream);
 
+/*
+ * ea_prefill_host_buffer_size - bytes of device memory ea_hybrid_attn_prefill_host
+ * needs for these sizes (0 on invalid sizes): room for Q, K, V, O, LSE, m, the
+ * block mask when with_block_mask != 0, and the planner workspace.
+ */
+size_t ea_prefill_host_buffer_size(int B, int S, int Hq, int Hkv, int d, int with_block_mask);
+
+/*
+ * ea_hybrid_attn_prefill_host - ea_hybrid_attn_prefill on tensors in HOST
+ * memory, with the host->device copies, the attention and the device->host
+ * copies overlapped (same attention as [EN] §02 eqs. (1)-(3) and §04
+ * Deployment, Algorithm 1(b)).
+ *
+ * Causal masks let query rows [q0, q1) start once the K/V rows below q1 are on
+ * the device, under all three modes.  The call therefore cuts the sequence
+ * into n_chunks runs of whole 128-query blocks.  Chunk c's Q/K/V rows are
+ * copied up on an internal stream; its planner and attention run as soon as
+ * they have arrived (even chunks on `stream`, odd chunks on an internal
+ * compute stream, so that consecutive chunks overlap on the SMs); its O and
+ * LSE rows are copied back on another internal stream while later chunks
+ * compute.  The results equal
+ * ea_hybrid_attn_prefill's bit for bit (each query block is computed by the
+ * same kernel with the same key tiles in the same order).
+ *
+ *   Q_host       host bf16 [B][S][Hq][d] contiguous
+ *   K_host, V_host  host bf16 [B][S][Hkv][d] contiguous
+ *   O_host       host bf16 [B][S][Hq][d] contiguous (written)
+ *   LSE_host     host float [B][Hq][S] contiguous (written), or NULL
+ *   m_host       host uint8 [B][Hkv] (ea_mode values)
+ *   block_mask_host  host uint8 [B][Hkv][nB][nB] as for ea_hybrid_attn_prefill,
+ *                or NULL (then no head may be EA_BLOCK)
+ *   device_buffer  device memory of ea_prefill_host_buffer_size(...) bytes
+ *                (with_block_mask = block_mask_host != NULL), 256-byte
+ *                aligned, owned by the caller; the call uses it as scratch
+ *                and folds every device error word into the workspace at its
+ *                start, so ea_check_errors(device_buffer, stream) reads them
+ *                afterwards.
+ *   n_chunks     0 = automatic (8, at most nB); otherwise 1 <= n_chunks <= 64
+ *                and <= nB.
+ *   stream       the call's work is ordered after earlier work on `stream`,
+ *                and later work on `stream` is ordered after all of it
+ *                (including the last copy back).
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap the attention; pageable memory gives the same results
+ * without the overlap.  The call is asynchronous: O_host and LSE_host hold the
+ * results once `stream` has passed the call's work; the host buffers must stay
+ * valid until then.  Calls that share a device_buffer must be ordered on one
+ * stream.  Constraints and errors otherwise as ea_hybrid_attn_prefill (plus
+ * EA_ERR_WORKSPACE for a missing, misaligned or short device_buffer); every
+ * argument is checked before anything is enqueued.
+ */
+ea_status ea_hybrid_attn_prefill_host(const void *Q_host, const void *K_host, const void *V_host,
+                                      void *O_host, float *LSE_host, int B, int S, int Hq, int Hkv,
+                                      int d, float scale, const uint8_t *m_host, int sink,
+                                      int window, const uint8_t *block_mask_host, int block_size,
+                                      void *device_buffer, size_t buffer_bytes, int n_chunks,
+                                      void *stream);
+
 /* Bytes of device workspace ea_hybrid_attn_decode needs (0 on invalid sizes).
  * num_splits = 0 means the automatic choice; the same value must be passed to
  * ea_hybrid_attn_decode. */

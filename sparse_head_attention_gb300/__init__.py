@@ -9,6 +9,7 @@ present, the device entry points raise instead of computing anything else.
     ea_route                 router pre-pass (pool -> MLP -> argmax -> mode)
     ea_route_layers          the router pre-pass of many model layers in one launch
     ea_hybrid_attn_prefill   fused FA / SSA / block-sparse prefill, one launch
+    ea_hybrid_attn_prefill_host  the prefill on host tensors, copies overlapped
     ea_hybrid_attn_decode    split-KV decode with the prefill-time routing
     ea_sparsity_ratios       Omega_MSR / Omega_ESR (host)
     ea_check_errors          read back the device error word of a workspace
@@ -32,6 +33,7 @@ _lib = None
 # Function names exported by the library (the ones include/ea.h declares).
 EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
            "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
+           "ea_prefill_host_buffer_size", "ea_hybrid_attn_prefill_host",
            "ea_decode_workspace_size",
            "ea_hybrid_attn_decode", "ea_sparsity_ratios", "ea_check_errors")
 
@@ -76,6 +78,11 @@ def lib():
         L.ea_hybrid_attn_prefill_noalloc.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32,
                                                      i32, f32, P, i32, i32, P, i32, P, P]
         L.ea_hybrid_attn_prefill_noalloc.restype = ctypes.c_int
+        L.ea_prefill_host_buffer_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.ea_prefill_host_buffer_size.restype = sz
+        L.ea_hybrid_attn_prefill_host.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P,
+                                                  i32, i32, P, i32, P, sz, i32, P]
+        L.ea_hybrid_attn_prefill_host.restype = ctypes.c_int
         L.ea_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ea_decode_workspace_size.restype = sz
         L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
@@ -264,6 +271,62 @@ def ea_hybrid_attn_prefill_noalloc(Q, K, V, m, *, sink, window, block_mask=None,
         B, S, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window), _ptr(block_mask), TILE,
         _ptr(visited_bitmap), _stream(stream))
     _check("ea_hybrid_attn_prefill_noalloc", st)
+    return O, LSE
+
+
+def ea_prefill_host_buffer_size(B, S, Hq, Hkv, d=128, with_block_mask=False):
+    return int(lib().ea_prefill_host_buffer_size(B, S, Hq, Hkv, d, 1 if with_block_mask else 0))
+
+
+def prefill_host_buffer(B, S, Hq, Hkv, d=128, with_block_mask=False, device="cuda"):
+    """Device scratch for ea_hybrid_attn_prefill_host (256-byte aligned by torch)."""
+    n = ea_prefill_host_buffer_size(B, S, Hq, Hkv, d, with_block_mask)
+    if n == 0:
+        raise ValueError("unsupported prefill sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def _host(t, name, dtype):
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous host %s tensor" % (name, dtype))
+    return t
+
+
+def ea_hybrid_attn_prefill_host(Q, K, V, m, *, sink, window, block_mask=None, scale=None, O=None,
+                                LSE=None, device_buffer=None, n_chunks=0, stream=None,
+                                want_lse=True):
+    """The fused prefill on HOST tensors (contiguous; page-locked for overlap):
+    Q [B, S, Hq, d], K/V [B, S, Hkv, d] bf16, m uint8 [B, Hkv], block_mask uint8
+    [B, Hkv, nB, nB] or None.  Copies in, attention and copies out run as a
+    chunked pipeline on the current CUDA device.  Returns (O, LSE) as host
+    tensors, complete once `stream` (default: the current stream) has passed
+    the call's work."""
+    _host(Q, "Q", torch.bfloat16)
+    _host(K, "K", torch.bfloat16)
+    _host(V, "V", torch.bfloat16)
+    _host(m, "m", torch.uint8)
+    if block_mask is not None:
+        _host(block_mask, "block_mask", torch.uint8)
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pin = Q.is_pinned()
+    if O is None:
+        O = torch.empty(Q.shape, dtype=torch.bfloat16, pin_memory=pin)
+    _host(O, "O", torch.bfloat16)
+    if LSE is None and want_lse:
+        LSE = torch.empty(B, Hq, S, dtype=torch.float32, pin_memory=pin)
+    if LSE is not None:
+        _host(LSE, "LSE", torch.float32)
+    if device_buffer is None:
+        device_buffer = prefill_host_buffer(B, S, Hq, Hkv, d, block_mask is not None)
+    _dev(device_buffer, "device_buffer", torch.uint8)
+    st = lib().ea_hybrid_attn_prefill_host(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, S, Hq, Hkv, d, float(scale), _ptr(m),
+        int(sink), int(window), _ptr(block_mask), TILE, _ptr(device_buffer),
+        device_buffer.numel(), int(n_chunks), _stream(stream))
+    _check("ea_hybrid_attn_prefill_host", st)
     return O, LSE
 
 

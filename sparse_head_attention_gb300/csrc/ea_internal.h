@@ -69,4 +69,19 @@ bool encode_tmap_bf16_4d(void *tmap_out, const void *base, int d, int H, int S, 
 
 int num_sms(int device);
 
+// Planner and attention launch restricted to query blocks [qb_begin, qb_end)
+// (qb_end = -1: up to the last block).  A plan and the launch that consumes it
+// must name the same range.  The exported ea_prefill_plan / ea_prefill_attend
+// are these over every block.
+ea_status prefill_plan_range(int B, int S, int Hq, int Hkv, int d, const uint8_t *m, int sink,
+                             int window, const uint8_t *block_mask, int block_size, void *workspace,
+                             size_t ws_bytes, int qb_begin, int qb_end, void *stream);
+ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                               const int64_t q_str[4], const int64_t kv_str[4],
+                               const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                               float scale, const uint8_t *m, int sink, int window,
+                               const uint8_t *block_mask, int block_size, void *workspace,
+                               size_t ws_bytes, uint32_t *visited_bitmap, int qb_begin, int qb_end,
+                               void *stream);
+
 } // namespace ea

@@ -84,6 +84,7 @@ struct PrefillArgs {
     uint32_t *items;
     ea_ws_header *hdr;
     int B, S, Hq, Hkv, g, npairs, nB, sink, window;
+    int qb_begin, qb_end;        // query blocks this plan covers
     uint32_t n_rows, n_items;
     float scale_log2;
 };
@@ -121,7 +122,8 @@ __device__ __forceinline__ bool tile_is_full(int mode, int qb, int kb, int sink,
 }
 
 // ------------------------------------------------------------ planner
-// One warp per (b, KV head, q block) row: number of visited key tiles.
+// One warp per (b, KV head, q block) row: number of visited key tiles, or -1
+// for a row outside the planned query blocks.
 __global__ void plan_costs_kernel(PrefillArgs a)
 {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
@@ -129,6 +131,11 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         return;
     const int qb = warp % a.nB;
     const int bh = warp / a.nB;  // b * Hkv + h
+    if (qb < a.qb_begin || qb >= a.qb_end) {
+        if (lane == 0)
+            a.costs[warp] = -1;
+        return;
+    }
     const int mode = a.m[bh];
     int n = 0;
     if (mode == EA_FULL) {
@@ -152,9 +159,9 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         a.costs[warp] = n;
 }
 
-// One CTA: stable counting sort of the rows by visited-tile count, longest
-// first; each row contributes its npairs items back to back.  Also resets the
-// work queue head.
+// One CTA: stable counting sort of the planned rows (cost >= 0) by visited-
+// tile count, longest first; each row contributes its npairs items back to
+// back.  Also resets the work queue head.
 __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
 {
     extern __shared__ int hist[];  // [nB + 2]
@@ -165,7 +172,8 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
         hist[c] = 0;
     __syncthreads();
     for (uint32_t r = tid; r < a.n_rows; r += blockDim.x)
-        atomicAdd(&hist[a.costs[r]], 1);
+        if (a.costs[r] >= 0)
+            atomicAdd(&hist[a.costs[r]], 1);
     __syncthreads();
     // Exclusive scan in descending cost order: start[c] = #rows with cost > c.
     // Bin c is visited at position nbins - 1 - c; each thread scans a segment.
@@ -195,8 +203,8 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
         const unsigned lt = (1u << tid) - 1u;
         for (uint32_t base = 0; base < a.n_rows; base += 32) {
             const uint32_t r = base + tid;
-            const bool valid = r < a.n_rows;
-            const int c = valid ? a.costs[r] : -1;
+            const int c = r < a.n_rows ? a.costs[r] : -1;
+            const bool valid = c >= 0;
             const unsigned active = __ballot_sync(0xffffffffu, valid);
             const unsigned peers = __match_any_sync(0xffffffffu, c) & active;
             int pos = 0;
@@ -765,7 +773,8 @@ static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 // arguments that do not depend on the tensors.
 static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint8_t *m, int sink,
                                 int window, const uint8_t *block_mask, int block_size,
-                                void *workspace, size_t ws_bytes, PrefillArgs &a)
+                                void *workspace, size_t ws_bytes, PrefillArgs &a,
+                                int qb_begin = 0, int qb_end = -1)
 {
     if (!m)
         return EA_ERR_INVALID_ARG;
@@ -799,8 +808,14 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
     a.nB = static_cast<int>(nB);
     a.sink = sink < S ? sink : S;        // sink or window beyond S keep the same pairs
     a.window = window < S ? window : S;
+    if (qb_end < 0)
+        qb_end = static_cast<int>(nB);
+    if (qb_begin < 0 || qb_begin >= qb_end || qb_end > nB)
+        return EA_ERR_INVALID_ARG;
+    a.qb_begin = qb_begin;
+    a.qb_end = qb_end;
     a.n_rows = static_cast<uint32_t>(n_rows);
-    a.n_items = static_cast<uint32_t>(n_rows * npairs);
+    a.n_items = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * (qb_end - qb_begin) * npairs);
     return EA_OK;
 }
 
@@ -823,13 +838,15 @@ static ea_status ensure_attributes()
     return EA_OK;
 }
 
-extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
-                                     int sink, int window, const uint8_t *block_mask,
-                                     int block_size, void *workspace, size_t ws_bytes, void *stream)
+namespace ea {
+
+ea_status prefill_plan_range(int B, int S, int Hq, int Hkv, int d, const uint8_t *m, int sink,
+                             int window, const uint8_t *block_mask, int block_size, void *workspace,
+                             size_t ws_bytes, int qb_begin, int qb_end, void *stream)
 {
     PrefillArgs a;
     ea_status s = prefill_common(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size,
-                                 workspace, ws_bytes, a);
+                                 workspace, ws_bytes, a, qb_begin, qb_end);
     if (s != EA_OK)
         return s;
     if ((s = ensure_attributes()) != EA_OK)
@@ -842,18 +859,19 @@ extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
-extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O,
-                                       float *LSE, const int64_t q_str[4], const int64_t kv_str[4],
-                                       const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
-                                       float scale, const uint8_t *m, int sink, int window,
-                                       const uint8_t *block_mask, int block_size, void *workspace,
-                                       size_t ws_bytes, uint32_t *visited_bitmap, void *stream)
+ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                               const int64_t q_str[4], const int64_t kv_str[4],
+                               const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                               float scale, const uint8_t *m, int sink, int window,
+                               const uint8_t *block_mask, int block_size, void *workspace,
+                               size_t ws_bytes, uint32_t *visited_bitmap, int qb_begin, int qb_end,
+                               void *stream)
 {
     if (!Q || !K || !V || !O || !q_str || !kv_str || !o_str || !(scale > 0.f))
         return EA_ERR_INVALID_ARG;
     PrefillArgs a;
     ea_status s = prefill_common(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size,
-                                 workspace, ws_bytes, a);
+                                 workspace, ws_bytes, a, qb_begin, qb_end);
     if (s != EA_OK)
         return s;
     if (q_str[3] != 1 || kv_str[3] != 1 || o_str[3] != 1)
@@ -895,6 +913,28 @@ extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void 
     hybrid_prefill_kernel<<<grid, kThreads, kPrefillSmemBytes, static_cast<cudaStream_t>(stream)>>>(
         tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+} // namespace ea
+
+extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
+                                     int sink, int window, const uint8_t *block_mask,
+                                     int block_size, void *workspace, size_t ws_bytes, void *stream)
+{
+    return prefill_plan_range(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size, workspace,
+                              ws_bytes, 0, -1, stream);
+}
+
+extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O,
+                                       float *LSE, const int64_t q_str[4], const int64_t kv_str[4],
+                                       const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                                       float scale, const uint8_t *m, int sink, int window,
+                                       const uint8_t *block_mask, int block_size, void *workspace,
+                                       size_t ws_bytes, uint32_t *visited_bitmap, void *stream)
+{
+    return prefill_attend_range(Q, K, V, O, LSE, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale, m,
+                                sink, window, block_mask, block_size, workspace, ws_bytes,
+                                visited_bitmap, 0, -1, stream);
 }
 
 extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, void *O,

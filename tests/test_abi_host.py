@@ -215,3 +215,28 @@ def test_route_layers_rejects_bad_arguments(L):
     deep = (ctypes.c_int * 6)(128, 64, 64, 64, 64, 2)                          # 5 dense layers
     W5 = (ctypes.c_void_p * 5)(*([0x1000] * 5))
     assert call(1, (ea._Mlp * 1)(ea._Mlp(5, deep, W5, W5)), (ctypes.c_void_p * 1)(0x1000)) == 2
+
+
+def test_prefill_host_rejects_bad_arguments(L):
+    B, S, Hq, Hkv = 1, 1024, 8, 2
+    need = L.ea_prefill_host_buffer_size(B, S, Hq, Hkv, 128, 0)
+    assert need > L.ea_prefill_host_buffer_size(B, S // 2, Hq, Hkv, 128, 0)
+    assert L.ea_prefill_host_buffer_size(B, S, Hq, Hkv, 128, 1) > need     # room for the mask
+    assert L.ea_prefill_host_buffer_size(B, S, Hq, Hkv, 64, 0) == 0
+
+    def call(**kw):
+        a = dict(Q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None, B=B, S=S, Hq=Hq, Hkv=Hkv,
+                 d=128, scale=0.088, m=_fake(), sink=64, window=256, bm=None, bs=128,
+                 buf=_fake(0x100000), nbytes=need, nch=0)
+        a.update(kw)
+        return L.ea_hybrid_attn_prefill_host(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["S"],
+                                             a["Hq"], a["Hkv"], a["d"], a["scale"], a["m"], a["sink"],
+                                             a["window"], a["bm"], a["bs"], a["buf"], a["nbytes"],
+                                             a["nch"], None)
+
+    for kw, expect in [(dict(Q=None), 1), (dict(m=None), 1), (dict(O=None), 1), (dict(scale=0.0), 1),
+                       (dict(Hkv=3), 1), (dict(window=0), 1), (dict(bs=64), 1), (dict(d=64), 2),
+                       (dict(nch=-1), 1), (dict(nch=9), 1), (dict(nch=65, S=1 << 14), 1),
+                       (dict(buf=None), 3), (dict(buf=_fake(0x100010)), 3), (dict(nbytes=need - 1), 3),
+                       (dict(bm=_fake()), 3)]:      # a mask needs the larger buffer
+        assert call(**kw) == expect, kw
