@@ -444,8 +444,45 @@ def run_decode(args, dev, peaks, flush):
         raise RuntimeError("device error in decode")
     t = statistics.mean(a.elapsed_time(b) for a, b in ms)
     gbs = nbytes / (t * 1e-3) / 1e9
-    del Kc, Vc
+
+    # the same step over a paged cache: 256-row pages of all sequences
+    # scattered through one pool by a random permutation
+    page_size = 256
+    per_seq = cfg.L // page_size
+    perm = torch.randperm(cfg.B * per_seq, generator=torch.Generator().manual_seed(3)).to(dev)
+    table = perm.view(cfg.B, per_seq).to(torch.int32)
+    Kp = torch.empty(cfg.B * per_seq, page_size, cfg.Hkv, cfg.d, dtype=torch.bfloat16, device=dev)
+    Kp[perm] = Kc.view(cfg.B * per_seq, page_size, cfg.Hkv, cfg.d)
+    del Kc
+    Vp = torch.empty_like(Kp)
+    Vp[perm] = Vc.view(cfg.B * per_seq, page_size, cfg.Hkv, cfg.d)
+    del Vc
+
+    def paged_step():
+        ea.ea_hybrid_attn_decode_paged(q, Kp, Vp, table, sl, m, sink=cfg.sink, window=cfg.window, O=O,
+                                       LSE=LSE, workspace=ws)
+
+    for _ in range(args.warmup):
+        paged_step()
+    torch.cuda.synchronize()
+    pms = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        paged_step()
+        b.record(stream)
+        pms.append((a, b))
+    torch.cuda.synchronize()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in paged decode")
+    tp = statistics.mean(a.elapsed_time(b) for a, b in pms)
+    del Kp, Vp
+    paged = {"page_size": page_size, "value": round(nbytes / (tp * 1e-3) / 1e9, 1), "unit": "GB/s",
+             "ms_per_step": round(tp, 4), "frac": round(nbytes / (tp * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+             "layout": "pages of all sequences permuted through one pool; block table [B, L/256]"}
     return {"workload": cfg.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(t, 4),
+            "paged": paged,
             "kept_kv_bytes_per_step": nbytes,
             "roofline": {"bound": "hbm", "kernel": "decode_plan_kernel + decode_split_kernel + decode_merge_kernel",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

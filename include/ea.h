@@ -331,6 +331,38 @@ ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, v
                                 void *stream);
 
 /*
+ * ea_hybrid_attn_decode_paged - ea_hybrid_attn_decode on a paged KV cache: the
+ * cache rows live in fixed-size pages, and each sequence lists its pages in a
+ * block table (the layout serving engines use to grow caches without copies).
+ * Same attention, routing and results as ea_hybrid_attn_decode on the cache
+ * the pages spell out; the pages have no counterpart of this entry point (it
+ * is the decode of the same method over another cache layout).
+ *
+ *   K_pages, V_pages  device bf16 [num_pages][page_size][Hkv][d], element
+ *                strides kv_str[4] (page, row, head, dim)
+ *   block_table  device int32 [B][bt_stride]: key k of sequence b is row
+ *                k % page_size of page block_table[b][k / page_size]; only the
+ *                first ceil(seqlens[b] / page_size) entries of a row are read
+ *   max_pages    pages per sequence at most (seqlens[b] <= max_pages * page_size)
+ *   page_size    rows per page, a multiple of 64
+ *   num_pages    pages in K_pages / V_pages; a table entry outside
+ *                [0, num_pages) is reported by ea_check_errors and reads zeros
+ *   workspace    ea_decode_workspace_size(B, Hq, Hkv, d, max_pages * page_size,
+ *                num_splits) bytes
+ * Other arguments, constraints and errors as ea_hybrid_attn_decode; invalid
+ * table sizes return EA_ERR_INVALID_ARG, a page size that is not a positive
+ * multiple of 64 EA_ERR_UNSUPPORTED.
+ */
+ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pages, const void *V_pages,
+                                      void *O, float *LSE, const int64_t q_str[3],
+                                      const int64_t kv_str[4], const int64_t o_str[3],
+                                      const int32_t *block_table, int64_t bt_stride, int max_pages,
+                                      int page_size, int num_pages, const int32_t *seqlens, int B,
+                                      int Hq, int Hkv, int d, float scale, const uint8_t *m,
+                                      int sink, int window, int num_splits, void *workspace,
+                                      size_t ws_bytes, void *stream);
+
+/*
  * ea_sparsity_ratios - model sparsity ratio and effective sparsity ratio of one
  * input over L layers ([ZH] §02 Background, eqs. (4)-(5); [EN] §02).  HOST
  * function; all pointers are host memory; nothing touches the GPU.

@@ -11,6 +11,7 @@ present, the device entry points raise instead of computing anything else.
     ea_hybrid_attn_prefill   fused FA / SSA / block-sparse prefill, one launch
     ea_hybrid_attn_prefill_host  the prefill on host tensors, copies overlapped
     ea_hybrid_attn_decode    split-KV decode with the prefill-time routing
+    ea_hybrid_attn_decode_paged  the same decode over a paged KV cache
     ea_sparsity_ratios       Omega_MSR / Omega_ESR (host)
     ea_check_errors          read back the device error word of a workspace
 """
@@ -35,7 +36,8 @@ EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_worksp
            "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
            "ea_prefill_host_buffer_size", "ea_hybrid_attn_prefill_host",
            "ea_decode_workspace_size",
-           "ea_hybrid_attn_decode", "ea_sparsity_ratios", "ea_check_errors")
+           "ea_hybrid_attn_decode", "ea_hybrid_attn_decode_paged", "ea_sparsity_ratios",
+           "ea_check_errors")
 
 
 class EAError(RuntimeError):
@@ -87,6 +89,10 @@ def lib():
         L.ea_decode_workspace_size.restype = sz
         L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
                                             P, i32, i32, i32, P, sz, P]
+        L.ea_hybrid_attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int64, i32,
+                                                  i32, i32, P, i32, i32, i32, i32, f32, P, i32,
+                                                  i32, i32, P, sz, P]
+        L.ea_hybrid_attn_decode_paged.restype = ctypes.c_int
         L.ea_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
                                          ctypes.POINTER(f64), ctypes.POINTER(f64)]
         L.ea_check_errors.argtypes = [P, P]
@@ -367,6 +373,43 @@ def ea_hybrid_attn_decode(q, Kc, Vc, seqlens, m, *, sink, window, num_splits=0, 
         _ptr(seqlens), B, Hq, Hkv, d, Lmax, float(scale), _ptr(m), int(sink), int(window),
         int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("ea_hybrid_attn_decode", st)
+    return O, LSE
+
+
+def ea_hybrid_attn_decode_paged(q, K_pages, V_pages, block_table, seqlens, m, *, sink, window,
+                                num_splits=0, scale=None, O=None, LSE=None, workspace=None,
+                                stream=None, want_lse=True):
+    """One decode step over a paged cache.  q [B, Hq, d]; K_pages/V_pages
+    [num_pages, page_size, Hkv, d] bf16; block_table int32 [B, max_pages] (key
+    k of sequence b: row k % page_size of page block_table[b, k // page_size]);
+    seqlens int32 [B]; m uint8 [B, Hkv]; all CUDA.  Returns (O, LSE)."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(K_pages, "K_pages", torch.bfloat16)
+    _dev(V_pages, "V_pages", torch.bfloat16)
+    _dev(block_table, "block_table", torch.int32)
+    _dev(seqlens, "seqlens", torch.int32)
+    _dev(m, "m", torch.uint8)
+    if K_pages.stride() != V_pages.stride() or K_pages.shape != V_pages.shape:
+        raise ValueError("K_pages and V_pages must share shapes and strides")
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [B, max_pages] with unit column stride")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv = K_pages.shape[0], K_pages.shape[1], K_pages.shape[2]
+    max_pages = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(q)
+    if LSE is None and want_lse:
+        LSE = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(B, Hq, Hkv, max_pages * page_size, num_splits, d, q.device)
+    st = lib().ea_hybrid_attn_decode_paged(
+        _ptr(q), _ptr(K_pages), _ptr(V_pages), _ptr(O), _ptr(LSE), _strides(q), _strides(K_pages),
+        _strides(O), _ptr(block_table), block_table.stride(0), max_pages, page_size, num_pages,
+        _ptr(seqlens), B, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window),
+        int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ea_hybrid_attn_decode_paged", st)
     return O, LSE
 
 

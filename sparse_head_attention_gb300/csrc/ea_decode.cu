@@ -18,6 +18,11 @@
 //     per (chunk, q head).
 //   decode_merge_kernel: combines the partials of each (b, q head) by
 //     log-sum-exp weights and writes bf16 O and fp32 LSE.
+// A paged cache (fixed-size pages of rows, a block table per sequence) runs
+// through the same kernels: its tiles are 64-key aligned so that no tile
+// straddles two pages (pages hold a multiple of 64 rows), each key of a tile
+// is tested against the kept ranges, and the producer looks up each tile's
+// page in the block table before issuing its copies.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -50,6 +55,10 @@ struct DecodeArgs {
     float *LSE;
     int B, Hq, Hkv, g, Lmax, sink, window, num_splits, max_splits;
     float scale_log2;
+    // paged cache (page_size == 0: one contiguous [B][Lmax] cache)
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int page_size, num_pages;
 };
 
 struct __align__(1024) DecSmem {
@@ -94,8 +103,21 @@ __device__ __forceinline__ bool unit_keys(const DecodeArgs &a, int b, int h, Key
     return ok;
 }
 
+// Paged cache: the unit's 64-key-aligned tiles are [0, TA) (covering the
+// sink) followed by [TB, TL) (covering the window, from the first tile not
+// already visited), TL = ceil(L / 64).  Returns the tile count.
+__device__ __forceinline__ int paged_tiles(const KeySegs &ks, int &TA, int &TB)
+{
+    const int L = ks.w0 + (ks.n - ks.n0);
+    TA = (ks.n0 + kDecKeys - 1) / kDecKeys;
+    const int TL = (L + kDecKeys - 1) / kDecKeys;
+    TB = max(ks.w0 / kDecKeys, TA);
+    return TA + max(TL - TB, 0);
+}
+
 // One CTA: per-unit chunk counts (automatic: one chunk per
-// EA_DECODE_AUTO_CHUNK kept keys), their prefix sum, and the chunk list.
+// EA_DECODE_AUTO_CHUNK kept keys, or per as many keys of whole tiles for a
+// paged cache), their prefix sum, and the chunk list.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
 {
     __shared__ int scan_tmp[1024];
@@ -108,8 +130,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
         KeySegs ks;
         if (!unit_keys(a, u / a.Hkv, u % a.Hkv, ks))
             raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+        int TA, TB;
+        const int work = a.page_size ? paged_tiles(ks, TA, TB) * kDecKeys : ks.n;
         int ns = a.num_splits > 0 ? a.num_splits
-                                  : (ks.n + EA_DECODE_AUTO_CHUNK - 1) / EA_DECODE_AUTO_CHUNK;
+                                  : (work + EA_DECODE_AUTO_CHUNK - 1) / EA_DECODE_AUTO_CHUNK;
         ns = ns < 1 ? 1 : (ns > a.max_splits ? a.max_splits : ns);
         a.unit_splits[u] = ns;
         local += ns;
@@ -134,11 +158,15 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
         a.hdr->n_items = static_cast<uint32_t>(scan_tmp[1023]);
 }
 
-// Position of chunk c in the key stream.
+// Position of chunk c in the key stream.  Contiguous cache: visited keys
+// [v_begin, v_end) in tiles that start at any key.  Paged cache: the unit's
+// aligned tiles [v_begin, v_end) (tile indices), tile v at key
+// 64 * (v < TA ? v : TB + v - TA).
 struct ChunkInfo {
     int b, h, v_begin, v_end;
     KeySegs ks;
     int a_tiles, b_begin, n_tiles;
+    int TA, TB;
 };
 
 __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
@@ -150,6 +178,17 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
     ci.h = u % a.Hkv;
     unit_keys(a, ci.b, ci.h, ci.ks);
     const int ns = a.unit_splits[u];
+    if (a.page_size) {
+        const int nt = paged_tiles(ci.ks, ci.TA, ci.TB);
+        const int len = (nt + ns - 1) / ns;
+        ci.v_begin = min(sp * len, nt);
+        ci.v_end = min(ci.v_begin + len, nt);
+        ci.n_tiles = ci.v_end - ci.v_begin;
+        ci.a_tiles = 0;
+        ci.b_begin = 0;
+        return ci;
+    }
+    ci.TA = ci.TB = 0;
     const int len = (ci.ks.n + ns - 1) / ns;
     ci.v_begin = min(sp * len, ci.ks.n);
     ci.v_end = min(ci.v_begin + len, ci.ks.n);
@@ -160,10 +199,19 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
     return ci;
 }
 
-// First cache row and number of valid keys of tile t of a chunk (a tile never
-// straddles the sink and window ranges).
-__device__ __forceinline__ void tile_rows(const ChunkInfo &ci, int t, int &key0, int &nvalid)
+// First key and number of leading keys that may be valid of tile t of a chunk
+// (contiguous cache: a tile never straddles the sink and window ranges, and
+// all nvalid keys are kept; paged cache: an aligned tile of 64 keys, each
+// tested against the kept ranges by the caller).
+__device__ __forceinline__ void tile_rows(const DecodeArgs &a, const ChunkInfo &ci, int t,
+                                          int &key0, int &nvalid)
 {
+    if (a.page_size) {
+        const int v = ci.v_begin + t;
+        key0 = kDecKeys * (v < ci.TA ? v : ci.TB + (v - ci.TA));
+        nvalid = kDecKeys;
+        return;
+    }
     if (t < ci.a_tiles) {
         const int v = ci.v_begin + t * kDecKeys;
         key0 = v;
@@ -254,21 +302,42 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // The whole warp walks the tile sequence (converged waits); lane 0
         // issues the copies.  It takes part in no block-wide barrier: the
         // compute warps synchronise among themselves with a named barrier.
+        // Paged cache: lane j holds the page of the chunk's tile 32 * k + j,
+        // looked up a group of 32 tiles ahead of the copies that need it.
         uint32_t issued = 0;
         for (int c = blockIdx.x; c < total; c += gridDim.x) {
             const ChunkInfo ci = chunk_info(a, c);
+            int my_page = 0;
             for (int t = 0; t < ci.n_tiles; ++t) {
+                if (a.page_size && (t & 31) == 0) {
+                    my_page = 0;
+                    if (t + lane < ci.n_tiles) {
+                        int k0, nv;
+                        tile_rows(a, ci, t + lane, k0, nv);
+                        my_page = a.block_table[ci.b * a.bt_stride + k0 / a.page_size];
+                    }
+                }
+                const int page = a.page_size ? __shfl_sync(0xffffffffu, my_page, t & 31) : 0;
                 const int s = issued % kDecStages;
                 if (!mbar_wait(&sm.empty[s], ((issued / kDecStages) & 1) ^ 1, abort, &a.hdr->error))
                     return;
                 if (lane == 0) {
                     int key0, nv;
-                    tile_rows(ci, t, key0, nv);
+                    tile_rows(a, ci, t, key0, nv);
+                    int row = key0, outer = ci.b;
+                    if (a.page_size) {
+                        // a page outside the cache is reported; its copy reads
+                        // the fill value (a box outside the tensor is zero-filled)
+                        if (page < 0 || page >= a.num_pages)
+                            raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+                        row = key0 % a.page_size;
+                        outer = page;
+                    }
                     mbar_arrive_expect_tx(&sm.full[s], 2 * kDecTileBytes);
-                    tma_load_4d(sm.k[s], &tm_k, 0, ci.h, key0, ci.b, &sm.full[s]);
-                    tma_load_4d(sm.k[s] + kDecHalfBytes, &tm_k, 64, ci.h, key0, ci.b, &sm.full[s]);
-                    tma_load_4d(sm.v[s], &tm_v, 0, ci.h, key0, ci.b, &sm.full[s]);
-                    tma_load_4d(sm.v[s] + kDecHalfBytes, &tm_v, 64, ci.h, key0, ci.b, &sm.full[s]);
+                    tma_load_4d(sm.k[s], &tm_k, 0, ci.h, row, outer, &sm.full[s]);
+                    tma_load_4d(sm.k[s] + kDecHalfBytes, &tm_k, 64, ci.h, row, outer, &sm.full[s]);
+                    tma_load_4d(sm.v[s], &tm_v, 0, ci.h, row, outer, &sm.full[s]);
+                    tma_load_4d(sm.v[s] + kDecHalfBytes, &tm_v, 64, ci.h, row, outer, &sm.full[s]);
                 }
                 __syncwarp();
                 ++issued;
@@ -308,7 +377,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 return;  // timed out (error word set) or another warp did
             ++consumed;
             int key0, nv;
-            tile_rows(ci, t, key0, nv);
+            tile_rows(a, ci, t, key0, nv);
             const uint32_t kb = smem_u32(sm.k[s]), vb = smem_u32(sm.v[s]);
             const int kw = warp * 16;   // this warp's first key in the tile
 
@@ -329,10 +398,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             float x[4] = {sc[0][0] * a.scale_log2, sc[0][1] * a.scale_log2,
                           sc[1][0] * a.scale_log2, sc[1][1] * a.scale_log2};
             const int kcol[4] = {kw + 2 * qd, kw + 2 * qd + 1, kw + 8 + 2 * qd, kw + 9 + 2 * qd};
+            if (a.page_size) {
+                // aligned tile: keep key k iff (k < sink end or k >= window
+                // start) and k < L
+                const int L = ci.ks.w0 + (ci.ks.n - ci.ks.n0);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (kcol[e] >= nv)
-                    x[e] = NEG_INF;
+                for (int e = 0; e < 4; ++e) {
+                    const int k = key0 + kcol[e];
+                    if (!((k < ci.ks.n0 || k >= ci.ks.w0) && k < L))
+                        x[e] = NEG_INF;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (kcol[e] >= nv)
+                        x[e] = NEG_INF;
+            }
             float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -499,13 +580,16 @@ using namespace ea;
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, void *O,
-                                           float *LSE, const int64_t q_str[3],
-                                           const int64_t kv_str[4], const int64_t o_str[3],
-                                           const int32_t *seqlens, int B, int Hq, int Hkv, int d,
-                                           int Lmax, float scale, const uint8_t *m, int sink,
-                                           int window, int num_splits, void *workspace,
-                                           size_t ws_bytes, void *stream)
+// Shared by the contiguous and the paged entry points.  Contiguous: Kc/Vc
+// [B][Lmax][Hkv][d] with strides kv_str; paged (page_size > 0): Kc/Vc
+// [num_pages][page_size][Hkv][d], Lmax = max_pages * page_size.
+static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, void *O, float *LSE,
+                               const int64_t q_str[3], const int64_t kv_str[4],
+                               const int64_t o_str[3], const int32_t *seqlens, int B, int Hq,
+                               int Hkv, int d, int Lmax, float scale, const uint8_t *m, int sink,
+                               int window, int num_splits, void *workspace, size_t ws_bytes,
+                               const int32_t *block_table, int64_t bt_stride, int page_size,
+                               int num_pages, void *stream)
 {
     if (!q || !Kc || !Vc || !O || !q_str || !kv_str || !o_str || !seqlens || !m)
         return EA_ERR_INVALID_ARG;
@@ -533,8 +617,10 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
         return EA_ERR_WORKSPACE;
 
     alignas(64) CUtensorMap tk, tv;
-    if (!encode_tmap_bf16_4d(&tk, Kc, d, Hkv, Lmax, B, kv_str, 64, kDecKeys, true) ||
-        !encode_tmap_bf16_4d(&tv, Vc, d, Hkv, Lmax, B, kv_str, 64, kDecKeys, true))
+    const int rows = page_size ? page_size : Lmax;
+    const int outer = page_size ? num_pages : B;
+    if (!encode_tmap_bf16_4d(&tk, Kc, d, Hkv, rows, outer, kv_str, 64, kDecKeys, true) ||
+        !encode_tmap_bf16_4d(&tv, Vc, d, Hkv, rows, outer, kv_str, 64, kDecKeys, true))
         return EA_ERR_INVALID_ARG;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -564,6 +650,10 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
     a.num_splits = num_splits;
     a.max_splits = max_splits;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int dev = 0;
@@ -580,4 +670,40 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
         return EA_ERR_CUDA;
     decode_merge_kernel<<<dim3(Hq, B), EA_HEAD_DIM, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
+}
+
+extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, void *O,
+                                           float *LSE, const int64_t q_str[3],
+                                           const int64_t kv_str[4], const int64_t o_str[3],
+                                           const int32_t *seqlens, int B, int Hq, int Hkv, int d,
+                                           int Lmax, float scale, const uint8_t *m, int sink,
+                                           int window, int num_splits, void *workspace,
+                                           size_t ws_bytes, void *stream)
+{
+    return decode_launch(q, Kc, Vc, O, LSE, q_str, kv_str, o_str, seqlens, B, Hq, Hkv, d, Lmax,
+                         scale, m, sink, window, num_splits, workspace, ws_bytes, nullptr, 0, 0, 0,
+                         stream);
+}
+
+extern "C" ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pages,
+                                                 const void *V_pages, void *O, float *LSE,
+                                                 const int64_t q_str[3], const int64_t kv_str[4],
+                                                 const int64_t o_str[3], const int32_t *block_table,
+                                                 int64_t bt_stride, int max_pages, int page_size,
+                                                 int num_pages, const int32_t *seqlens, int B,
+                                                 int Hq, int Hkv, int d, float scale,
+                                                 const uint8_t *m, int sink, int window,
+                                                 int num_splits, void *workspace, size_t ws_bytes,
+                                                 void *stream)
+{
+    if (!block_table || max_pages < 1 || num_pages < 1 || bt_stride < max_pages)
+        return EA_ERR_INVALID_ARG;
+    if (page_size < kDecKeys || page_size % kDecKeys != 0)
+        return EA_ERR_UNSUPPORTED;
+    const int64_t Lmax = static_cast<int64_t>(max_pages) * page_size;
+    if (Lmax >= (int64_t(1) << 31))
+        return EA_ERR_UNSUPPORTED;
+    return decode_launch(q, K_pages, V_pages, O, LSE, q_str, kv_str, o_str, seqlens, B, Hq, Hkv,
+                         d, static_cast<int>(Lmax), scale, m, sink, window, num_splits, workspace,
+                         ws_bytes, block_table, bt_stride, page_size, num_pages, stream);
 }
