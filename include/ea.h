@@ -13,9 +13,12 @@
  *
  * Conventions shared by every entry point
  *   - Tensors are caller-owned device memory unless marked "host".  The library
- *     never allocates or frees device memory; scratch space is the caller's
- *     workspace buffer.  No state is kept between calls except what lives in
- *     that workspace.
+ *     never allocates or frees device memory at run time; scratch space is the
+ *     caller's workspace buffer.  State kept between calls, besides what lives
+ *     in that workspace: per device, the fixed scratch array of
+ *     ea_hybrid_attn_prefill_noalloc, the copy streams and events that
+ *     ea_hybrid_attn_prefill_host creates on first use, and which kernels have
+ *     had their shared-memory limits raised.
  *   - Element strides are given in ELEMENTS (not bytes), outermost first.  The
  *     innermost (head-dim) stride must be 1.
  *   - bf16 tensors are passed as void* to raw 16-bit bf16 storage.
