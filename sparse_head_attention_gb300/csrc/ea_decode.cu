@@ -121,6 +121,7 @@ __device__ __forceinline__ int paged_tiles(const KeySegs &ks, int &TA, int &TB)
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
 {
     __shared__ int scan_tmp[1024];
+    griddep_launch_dependents();   // the split kernel may start its prologue
     const int units = a.B * a.Hkv;
     const int tid = threadIdx.x;
     const int per = (units + blockDim.x - 1) / blockDim.x;
@@ -283,7 +284,6 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int r = lane >> 2, qd = lane & 3;   // fragment row / quad position
     const float NEG_INF = -__int_as_float(0x7f800000);
-    const int total = static_cast<int>(a.hdr->n_items);
     volatile int *abort = &sm.abort;
 
     if (tid == 0) {
@@ -296,6 +296,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
+    // The chunk list comes from the planner launched just before; every CTA is
+    // resident (one per SM) before the merge kernel may be scheduled.
+    griddep_wait();
+    griddep_launch_dependents();
+    const int total = static_cast<int>(a.hdr->n_items);
 
     if (warp == kDecWarps) {
         // ------------------------------------------------------------ producer
@@ -507,6 +512,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a)
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float LOG2E = 1.4426950408889634f;
     const int qh = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+    griddep_wait();   // the partials of the split kernel launched just before
     const int u = b * a.Hkv + qh / a.g, hh = qh % a.g;
     const int first = a.unit_first[u], ns = a.unit_splits[u];
     const int64_t base = static_cast<int64_t>(first) * a.g + hh;
@@ -570,8 +576,34 @@ static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, c
         if (dev < 64)
             attr_done[dev] = true;
     }
-    decode_split_kernel<<<grid, kDecThreads, smem, st>>>(tk, tv, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel, tk, tv, a);
+}
+
+// The merge kernel, launched so that its CTAs may be scheduled while the split
+// kernel finishes (it waits for the split kernel before reading anything).
+static cudaError_t launch_merge(const DecodeArgs &a, int Hq, int B, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(Hq, B);
+    cfg.blockDim = dim3(EA_HEAD_DIM);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, a);
 }
 
 } // namespace ea
@@ -668,7 +700,8 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     const cudaError_t e = launch_decode(tk, tv, a, grid, st);
     if (e != cudaSuccess)
         return EA_ERR_CUDA;
-    decode_merge_kernel<<<dim3(Hq, B), EA_HEAD_DIM, 0, st>>>(a);
+    if (launch_merge(a, Hq, B, st) != cudaSuccess)
+        return EA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 

@@ -320,4 +320,19 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Programmatic dependent launch.  griddep_wait blocks until the grids this
+// one depends on (launched before it on the stream) have completed and their
+// memory is visible; griddep_launch_dependents lets the next grid of the
+// stream, if launched with programmatic stream serialisation, start its
+// prologue now.  Without that launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 } // namespace ea
