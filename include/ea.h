@@ -202,6 +202,46 @@ ea_status ea_prefill_attend(const void *Q, const void *K, const void *V, void *O
                             const uint8_t *block_mask, int block_size, void *workspace,
                             size_t ws_bytes, uint32_t *visited_bitmap, void *stream);
 
+/* Bytes of device workspace ea_hybrid_attn_prefill_varlen needs (0 on
+ * invalid sizes); 256-byte aligned like every workspace. */
+size_t ea_prefill_varlen_workspace_size(int B, int total_tokens, int max_seqlen, int Hq, int Hkv,
+                                        int d);
+
+/*
+ * ea_hybrid_attn_prefill_varlen - ea_hybrid_attn_prefill over a batch of
+ * sequences of different lengths packed back to back (the layout of a serving
+ * engine's prefill batch), in one launch.  Same attention and masks per
+ * sequence as ea_hybrid_attn_prefill ([EN] §02 eqs. (1)-(3); §04 Deployment,
+ * Algorithm 1(b)); no sequence attends to another.
+ *
+ *   Q, O         device bf16 [total_tokens][Hq][d], element strides q_str[3] /
+ *                o_str[3] (token, head, dim)
+ *   K, V         device bf16 [total_tokens][Hkv][d], strides kv_str[3]
+ *   LSE          device float [Hq][total_tokens] contiguous, or NULL
+ *   cu_seqlens   device int32 [B + 1]: sequence b is tokens
+ *                [cu_seqlens[b], cu_seqlens[b + 1]) (cu_seqlens[0] >= 0,
+ *                non-decreasing, cu_seqlens[B] <= total_tokens); a sequence of
+ *                length 0 has no output
+ *   max_seqlen   an upper bound on every sequence's length (<= 2^21)
+ *   m            device uint8 [B][Hkv]
+ *   block_mask   device uint8, per sequence b an [Hkv][nB_b][nB_b] block
+ *                (nB_b = ceil(len_b / 128)), blocks of consecutive sequences
+ *                back to back; NULL if no head is EA_BLOCK
+ *   workspace    ea_prefill_varlen_workspace_size(...) bytes, 256-aligned
+ * A sequence whose length is negative, above max_seqlen or runs past
+ * total_tokens is skipped (no output) and reported by ea_check_errors, as are
+ * the conditions ea_hybrid_attn_prefill reports there.  Other constraints and
+ * host-side errors as ea_hybrid_attn_prefill.
+ */
+ea_status ea_hybrid_attn_prefill_varlen(const void *Q, const void *K, const void *V, void *O,
+                                        float *LSE, const int64_t q_str[3],
+                                        const int64_t kv_str[3], const int64_t o_str[3],
+                                        const int32_t *cu_seqlens, int B, int total_tokens,
+                                        int max_seqlen, int Hq, int Hkv, int d, float scale,
+                                        const uint8_t *m, int sink, int window,
+                                        const uint8_t *block_mask, int block_size,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
 /*
  * ea_hybrid_attn_prefill_noalloc - ea_hybrid_attn_prefill for callers that
  * cannot provide a workspace, e.g. an engine whose device memory is owned by

@@ -10,6 +10,7 @@ present, the device entry points raise instead of computing anything else.
     ea_route_layers          the router pre-pass of many model layers in one launch
     ea_hybrid_attn_prefill   fused FA / SSA / block-sparse prefill, one launch
     ea_hybrid_attn_prefill_host  the prefill on host tensors, copies overlapped
+    ea_hybrid_attn_prefill_varlen  sequences of different lengths in one launch
     ea_hybrid_attn_decode    split-KV decode with the prefill-time routing
     ea_hybrid_attn_decode_paged  the same decode over a paged KV cache
     ea_sparsity_ratios       Omega_MSR / Omega_ESR (host)
@@ -35,6 +36,7 @@ _lib = None
 EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_workspace_size", "ea_hybrid_attn_prefill",
            "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
            "ea_prefill_host_buffer_size", "ea_hybrid_attn_prefill_host",
+           "ea_prefill_varlen_workspace_size", "ea_hybrid_attn_prefill_varlen",
            "ea_decode_workspace_size",
            "ea_hybrid_attn_decode", "ea_hybrid_attn_decode_paged", "ea_sparsity_ratios",
            "ea_check_errors")
@@ -85,6 +87,11 @@ def lib():
         L.ea_hybrid_attn_prefill_host.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P,
                                                   i32, i32, P, i32, P, sz, i32, P]
         L.ea_hybrid_attn_prefill_host.restype = ctypes.c_int
+        L.ea_prefill_varlen_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.ea_prefill_varlen_workspace_size.restype = sz
+        L.ea_hybrid_attn_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
+                                                    i32, i32, f32, P, i32, i32, P, i32, P, sz, P]
+        L.ea_hybrid_attn_prefill_varlen.restype = ctypes.c_int
         L.ea_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ea_decode_workspace_size.restype = sz
         L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
@@ -333,6 +340,50 @@ def ea_hybrid_attn_prefill_host(Q, K, V, m, *, sink, window, block_mask=None, sc
         int(sink), int(window), _ptr(block_mask), TILE, _ptr(device_buffer),
         device_buffer.numel(), int(n_chunks), _stream(stream))
     _check("ea_hybrid_attn_prefill_host", st)
+    return O, LSE
+
+
+def ea_prefill_varlen_workspace_size(B, total_tokens, max_seqlen, Hq, Hkv, d=128):
+    return int(lib().ea_prefill_varlen_workspace_size(B, total_tokens, max_seqlen, Hq, Hkv, d))
+
+
+def prefill_varlen_workspace(B, total_tokens, max_seqlen, Hq, Hkv, d=128, device="cuda"):
+    n = ea_prefill_varlen_workspace_size(B, total_tokens, max_seqlen, Hq, Hkv, d)
+    if n == 0:
+        raise ValueError("unsupported variable-length prefill sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ea_hybrid_attn_prefill_varlen(Q, K, V, cu_seqlens, m, *, max_seqlen, sink, window,
+                                  block_mask=None, scale=None, O=None, LSE=None, workspace=None,
+                                  stream=None, want_lse=True):
+    """Sequences of different lengths packed back to back, one launch.
+    Q [total, Hq, d], K/V [total, Hkv, d] bf16; cu_seqlens int32 [B + 1];
+    m uint8 [B, Hkv]; block_mask uint8, per sequence [Hkv, nB_b, nB_b] back
+    to back (or None); all CUDA.  Returns (O [total, Hq, d], LSE [Hq, total])."""
+    _dev(Q, "Q", torch.bfloat16)
+    _dev(K, "K", torch.bfloat16)
+    _dev(V, "V", torch.bfloat16)
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(m, "m", torch.uint8)
+    if K.stride() != V.stride():
+        raise ValueError("K and V must share strides")
+    total, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if O is None:
+        O = torch.empty_like(Q)
+    if LSE is None and want_lse:
+        LSE = torch.empty(Hq, total, dtype=torch.float32, device=Q.device)
+    if workspace is None:
+        workspace = prefill_varlen_workspace(B, total, max_seqlen, Hq, Hkv, d, Q.device)
+    st = lib().ea_hybrid_attn_prefill_varlen(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _strides(Q), _strides(K), _strides(O),
+        _ptr(cu_seqlens), B, total, int(max_seqlen), Hq, Hkv, d, float(scale), _ptr(m), int(sink),
+        int(window), _ptr(block_mask), TILE, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ea_hybrid_attn_prefill_varlen", st)
     return O, LSE
 
 

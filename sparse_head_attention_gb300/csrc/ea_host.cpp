@@ -27,6 +27,26 @@ PrefillWs prefill_ws_layout(int B, int S, int Hq, int Hkv)
     return w;
 }
 
+PrefillVarlenWs prefill_varlen_ws_layout(int B, int total_tokens, int Hq, int Hkv)
+{
+    PrefillVarlenWs w{};
+    w.rows = static_cast<int64_t>(Hkv) * (ceil_div(total_tokens, EA_TILE) + B);
+    const int64_t pairs = ceil_div(Hq / Hkv, 2);
+    size_t off = sizeof(ea_ws_header);
+    w.costs = off;
+    off = align_up(off + sizeof(int32_t) * w.rows, 256);
+    w.items = off;
+    off = align_up(off + sizeof(uint32_t) * w.rows * pairs, 256);
+    w.row_off = off;
+    off = align_up(off + sizeof(int32_t) * (static_cast<size_t>(B) + 1), 256);
+    w.mask_off = off;
+    off = align_up(off + sizeof(int64_t) * (static_cast<size_t>(B) + 1), 256);
+    w.row_desc = off;
+    off = align_up(off + 8 * static_cast<size_t>(w.rows), 256);
+    w.total = off;
+    return w;
+}
+
 DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits)
 {
     DecodeWs w{};
@@ -128,6 +148,15 @@ extern "C" size_t ea_prefill_workspace_size(int B, int S, int Hq, int Hkv, int d
     if (B < 1 || S < 1 || S > EA_MAX_SEQ || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d != EA_HEAD_DIM)
         return 0;
     return prefill_ws_layout(B, S, Hq, Hkv).total;
+}
+
+extern "C" size_t ea_prefill_varlen_workspace_size(int B, int total_tokens, int max_seqlen, int Hq,
+                                                   int Hkv, int d)
+{
+    if (B < 1 || total_tokens < 1 || max_seqlen < 1 || max_seqlen > EA_MAX_SEQ || Hq < 1 ||
+        Hkv < 1 || Hq % Hkv != 0 || d != EA_HEAD_DIM)
+        return 0;
+    return prefill_varlen_ws_layout(B, total_tokens, Hq, Hkv).total;
 }
 
 extern "C" size_t ea_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int num_splits)

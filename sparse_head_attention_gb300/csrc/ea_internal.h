@@ -45,6 +45,19 @@ struct PrefillWs {
 };
 PrefillWs prefill_ws_layout(int B, int S, int Hq, int Hkv);
 
+// Workspace of a variable-length prefill: rows are bounded by
+// Hkv * (ceil(total_tokens / 128) + B) (each sequence rounds up once).
+struct PrefillVarlenWs {
+    int64_t rows;   // upper bound on planned rows
+    size_t costs;   // int32 [rows]
+    size_t items;   // uint32 [rows * pairs]
+    size_t row_off; // int32 [B + 1]: first row of each sequence
+    size_t mask_off;// int64 [B + 1]: first block-mask byte of each sequence
+    size_t row_desc;// int2 [rows]: {b, h << 16 | qb} of each planned row
+    size_t total;
+};
+PrefillVarlenWs prefill_varlen_ws_layout(int B, int total_tokens, int Hq, int Hkv);
+
 // Byte offsets of the decode workspace regions.  A chunk is one split of one
 // (b, KV head) unit; every unit has at most max_splits chunks.
 struct DecodeWs {

@@ -77,6 +77,7 @@ struct PrefillArgs {
     __nv_bfloat16 *O;
     int64_t o_sb, o_ss, o_sh;
     float *LSE;
+    int64_t lse_sb, lse_sh;      // LSE[b * lse_sb + qh * lse_sh + token]
     const uint8_t *m;
     const uint8_t *block_mask;
     uint32_t *visited;
@@ -85,9 +86,96 @@ struct PrefillArgs {
     ea_ws_header *hdr;
     int B, S, Hq, Hkv, g, npairs, nB, sink, window;
     int qb_begin, qb_end;        // query blocks this plan covers
-    uint32_t n_rows, n_items;
+    uint32_t n_rows, n_items;    // rows to scan, items at most (the plan counts the real ones)
     float scale_log2;
+    // variable-length batch (cu_seqlens != NULL): sequence b is tokens
+    // [cu_seqlens[b], cu_seqlens[b + 1]) of one packed [tokens][heads][d]
+    // tensor; its rows start at row_off[b] and its block mask at mask_off[b]
+    const int32_t *cu_seqlens;
+    int32_t *row_off;
+    int64_t *mask_off;
+    int2 *row_desc;              // per planned row: {b, h << 16 | qb}, written by the planner
+    int max_seqlen, total_tokens;
 };
+
+// One (b, KV head, query block) row of the plan.  tok0 is the sequence's first
+// token in the tensors' token dimension, tma_b its batch coordinate, mask_row
+// the offset of the row's block-mask entries.
+struct RowInfo {
+    int b, h, qb, tok0, S, nB, tma_b;
+    int64_t mask_row;
+};
+
+// Fields of a variable-length row once b, h and qb are known.
+__device__ __forceinline__ void varlen_row_fields(const PrefillArgs &a, RowInfo &x)
+{
+    x.tok0 = a.cu_seqlens[x.b];
+    x.S = a.cu_seqlens[x.b + 1] - x.tok0;
+    x.nB = (x.S + T - 1) / T;
+    x.tma_b = 0;
+    x.mask_row = a.mask_off[x.b] + (static_cast<int64_t>(x.h) * x.nB + x.qb) * x.nB;
+}
+
+// A row of a fixed-length batch: rows are [b][h][qb].
+__device__ __forceinline__ void decode_row_dense(int row, const PrefillArgs &a, RowInfo &x)
+{
+    x.qb = row % a.nB;
+    const int bh = row / a.nB;
+    x.h = bh % a.Hkv;
+    x.b = bh / a.Hkv;
+    x.tok0 = 0;
+    x.S = a.S;
+    x.nB = a.nB;
+    x.tma_b = x.b;
+    x.mask_row = (static_cast<int64_t>(bh) * a.nB + x.qb) * a.nB;
+}
+
+// Planner side: find the row's sequence (variable-length batches search the
+// per-sequence row offsets) and record it for the attention kernel.
+__device__ __forceinline__ bool decode_row_search(int row, const PrefillArgs &a, RowInfo &x)
+{
+    if (!a.cu_seqlens) {
+        decode_row_dense(row, a, x);
+        return true;
+    }
+    if (row >= a.row_off[a.B])
+        return false;
+    // the last sequence whose first row is <= row (it is never empty)
+    int lo = 0, hi = a.B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.row_off[mid] <= row)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    x.b = lo;
+    const int S = a.cu_seqlens[lo + 1] - a.cu_seqlens[lo];
+    const int nB = (S + T - 1) / T;
+    const int local = row - a.row_off[lo];
+    x.h = local / nB;
+    x.qb = local - x.h * nB;
+    varlen_row_fields(a, x);
+    return true;
+}
+
+// Kernel side: a planned row (variable-length rows through the planner's
+// record, which keeps the search out of the warps' register budgets).  The
+// attention kernel is compiled separately for fixed- and variable-length
+// batches, so that the fixed-length one carries none of this.
+template <bool kVarlen>
+__device__ __forceinline__ void decode_row(int row, const PrefillArgs &a, RowInfo &x)
+{
+    if (!kVarlen) {
+        decode_row_dense(row, a, x);
+        return;
+    }
+    const int2 d = a.row_desc[row];
+    x.b = d.x;
+    x.h = static_cast<int>(static_cast<uint32_t>(d.y) >> 16);
+    x.qb = d.y & 0xFFFF;
+    varlen_row_fields(a, x);
+}
 
 // ------------------------------------------------------------ tile sequences
 // SSA key tiles of query block qb: the sink tiles [0, n_sink) below the window,
@@ -129,14 +217,16 @@ __global__ void plan_costs_kernel(PrefillArgs a)
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
     if (warp >= static_cast<int>(a.n_rows))
         return;
-    const int qb = warp % a.nB;
-    const int bh = warp / a.nB;  // b * Hkv + h
-    if (qb < a.qb_begin || qb >= a.qb_end) {
+    RowInfo x;
+    if (!decode_row_search(warp, a, x) || x.qb < a.qb_begin || x.qb >= a.qb_end) {
         if (lane == 0)
             a.costs[warp] = -1;
         return;
     }
-    const int mode = a.m[bh];
+    if (a.cu_seqlens && lane == 0)
+        a.row_desc[warp] = make_int2(x.b, (x.h << 16) | x.qb);
+    const int qb = x.qb;
+    const int mode = a.m[x.b * a.Hkv + x.h];
     int n = 0;
     if (mode == EA_FULL) {
         n = qb + 1;
@@ -145,7 +235,7 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         ssa_tiles(qb, a.sink, a.window, n_sink, kb_lo);
         n = n_sink + (qb - kb_lo + 1);
     } else if (mode == EA_BLOCK && a.block_mask) {
-        const uint8_t *row = a.block_mask + (static_cast<int64_t>(bh) * a.nB + qb) * a.nB;
+        const uint8_t *row = a.block_mask + x.mask_row;
         for (int kb = lane; kb <= qb; kb += 32)
             n += row[kb] != 0;
         for (int o = 16; o > 0; o >>= 1)
@@ -171,9 +261,17 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
     for (int c = tid; c < nbins; c += blockDim.x)
         hist[c] = 0;
     __syncthreads();
+    __shared__ int n_planned;
+    if (tid == 0)
+        n_planned = 0;
+    __syncthreads();
+    int mine = 0;
     for (uint32_t r = tid; r < a.n_rows; r += blockDim.x)
-        if (a.costs[r] >= 0)
+        if (a.costs[r] >= 0) {
             atomicAdd(&hist[a.costs[r]], 1);
+            ++mine;
+        }
+    atomicAdd(&n_planned, mine);
     __syncthreads();
     // Exclusive scan in descending cost order: start[c] = #rows with cost > c.
     // Bin c is visited at position nbins - 1 - c; each thread scans a segment.
@@ -222,24 +320,72 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
     if (tid == 0) {
         a.hdr->work_counter = 0;
         a.hdr->drained = 0;
-        a.hdr->n_items = a.n_items;
+        a.hdr->n_items = static_cast<uint32_t>(n_planned) * static_cast<uint32_t>(a.npairs);
+    }
+}
+
+// One CTA: per-sequence row and block-mask offsets of a variable-length batch.
+// A sequence with a bad length (negative, beyond max_seqlen, or ending past
+// total_tokens) is reported and planned with no rows.
+__global__ void __launch_bounds__(1024) varlen_setup_kernel(PrefillArgs a)
+{
+    __shared__ long long scan_r[1024], scan_m[1024];
+    const int tid = threadIdx.x;
+    const int per = (a.B + blockDim.x - 1) / blockDim.x;
+    const int lo = tid * per, hi = min(lo + per, a.B);
+    long long rows = 0, bytes = 0;
+    for (int b = lo; b < hi; ++b) {
+        const int c0 = a.cu_seqlens[b], c1 = a.cu_seqlens[b + 1];
+        int S = c1 - c0;
+        if (c0 < 0 || S < 0 || S > a.max_seqlen || c1 > a.total_tokens) {
+            raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+            S = 0;
+        }
+        const long long nB = (S + T - 1) / T;
+        rows += a.Hkv * nB;
+        bytes += a.Hkv * nB * nB;
+    }
+    scan_r[tid] = rows;
+    scan_m[tid] = bytes;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const long long vr = tid >= off ? scan_r[tid - off] : 0;
+        const long long vm = tid >= off ? scan_m[tid - off] : 0;
+        __syncthreads();
+        scan_r[tid] += vr;
+        scan_m[tid] += vm;
+        __syncthreads();
+    }
+    long long run_r = scan_r[tid] - rows, run_m = scan_m[tid] - bytes;
+    for (int b = lo; b < hi; ++b) {
+        a.row_off[b] = static_cast<int32_t>(run_r);
+        a.mask_off[b] = run_m;
+        const int c0 = a.cu_seqlens[b], c1 = a.cu_seqlens[b + 1];
+        int S = c1 - c0;
+        if (c0 < 0 || S < 0 || S > a.max_seqlen || c1 > a.total_tokens)
+            S = 0;
+        const long long nB = (S + T - 1) / T;
+        run_r += a.Hkv * nB;
+        run_m += a.Hkv * nB * nB;
+    }
+    if (tid == 1023) {
+        a.row_off[a.B] = static_cast<int32_t>(scan_r[1023]);
+        a.mask_off[a.B] = scan_m[1023];
     }
 }
 
 // ------------------------------------------------------------ attention
-struct ItemInfo {
-    int b, h, qb, pair, row;
+struct ItemInfo : RowInfo {
+    int pair, row;
 };
 
+template <bool kVarlen>
 __device__ __forceinline__ ItemInfo decode_item(int item, const PrefillArgs &a)
 {
     ItemInfo x;
     x.pair = item % a.npairs;
     x.row = item / a.npairs;
-    x.qb = x.row % a.nB;
-    const int bh = x.row / a.nB;
-    x.h = bh % a.Hkv;
-    x.b = bh / a.Hkv;
+    decode_row<kVarlen>(x.row, a, x);
     return x;
 }
 
@@ -301,12 +447,14 @@ struct BlockScan {
     }
 };
 
+template <bool kVarlen>
 __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
                                               const CUtensorMap *tm_v, const PrefillArgs &a,
                                               PrefillSmem &sm, int lane)
 {
     uint32_t *err = &a.hdr->error;
     uint32_t kv_it = 0, q_it = 0;
+    const uint32_t n_items = a.hdr->n_items;   // written by the planner
     bool ok = true;
     for (int it = 0; ok; ++it) {
         const int slot = it & 1;
@@ -315,7 +463,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
         int item = -1;
         if (lane == 0) {
             const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
-            item = x < a.n_items ? static_cast<int>(a.items[x]) : -1;
+            item = x < n_items ? static_cast<int>(a.items[x]) : -1;
             // Every CTA sees the empty queue exactly once; the last one resets
             // the head so the same plan can feed another launch.
             if (item < 0 && atomicAdd(&a.hdr->drained, 1u) == gridDim.x - 1) {
@@ -328,7 +476,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
         item = __shfl_sync(0xffffffffu, item, 0);
         if (item < 0)
             break;
-        const ItemInfo x = decode_item(item, a);
+        const ItemInfo x = decode_item<kVarlen>(item, a);
         const int N = a.costs[x.row];
         if (N == 0)
             continue;
@@ -342,8 +490,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
             for (int t = 0; t < 2; ++t) {
                 bool st;
                 const int qh = item_head(x, t, a, st);
-                tma_load_4d(sm.q[t], tm_q, 0, qh, x.qb * T, x.b, &sm.q_full);
-                tma_load_4d(sm.q[t] + kHalfBytes, tm_q, 64, qh, x.qb * T, x.b, &sm.q_full);
+                tma_load_4d(sm.q[t], tm_q, 0, qh, x.tok0 + x.qb * T, x.tma_b, &sm.q_full);
+                tma_load_4d(sm.q[t] + kHalfBytes, tm_q, 64, qh, x.tok0 + x.qb * T, x.tma_b,
+                            &sm.q_full);
             }
         }
         __syncwarp();
@@ -353,8 +502,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         BlockScan scan;
         if (mode == EA_BLOCK)
-            scan.init(a.block_mask + (static_cast<int64_t>(x.b * a.Hkv + x.h) * a.nB + x.qb) * a.nB,
-                      x.qb + 1, lane);
+            scan.init(a.block_mask + x.mask_row, x.qb + 1, lane);
         for (int n = 0; n < N && ok; ++n) {
             const int kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
 #pragma unroll 1
@@ -368,8 +516,9 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
                 if (lane == 0) {
                     const CUtensorMap *tm = which == 0 ? tm_k : tm_v;
                     mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
-                    tma_load_4d(sm.kv[s], tm, 0, x.h, kb * T, x.b, &sm.kv_full[s]);
-                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, kb * T, x.b, &sm.kv_full[s]);
+                    tma_load_4d(sm.kv[s], tm, 0, x.h, x.tok0 + kb * T, x.tma_b, &sm.kv_full[s]);
+                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, x.tok0 + kb * T, x.tma_b,
+                                &sm.kv_full[s]);
                     if (which == 0 && a.visited) {
                         const uint64_t bit =
                             (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(kb);
@@ -460,8 +609,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
             mbar_arrive(&sm.item_empty[slot]);
         if (item < 0)
             break;
-        const ItemInfo x = decode_item(item, a);
-        const int N = a.costs[x.row];
+        const int N = a.costs[item / a.npairs];
         if (N == 0)
             continue;
         if (!mbar_wait(&sm.q_full, q_it & 1, &sm.abort, err))
@@ -524,6 +672,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
 // online softmax in the exp2 domain, P (bf16) written back over the first 64
 // columns of S for the PV MMA.  S_n(t) being ready implies PV_{n-1}(t) has
 // completed, so O_t can be rescaled in place without another wait.
+template <bool kVarlen>
 __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem,
                                              int warp)
 {
@@ -544,7 +693,7 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         mbar_arrive(&sm.item_empty[slot]);
         if (item < 0)
             break;
-        const ItemInfo x = decode_item(item, a);
+        const ItemInfo x = decode_item<kVarlen>(item, a);
         bool store;
         const int qh = item_head(x, t, a, store);
         const int N = a.costs[x.row];
@@ -554,8 +703,7 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         bool diag_kept = false;
         if (mode == EA_BLOCK && N > 0)
-            diag_kept = a.block_mask[(static_cast<int64_t>(x.b * a.Hkv + x.h) * a.nB + x.qb) * a.nB +
-                                     x.qb] != 0;
+            diag_kept = a.block_mask[x.mask_row + x.qb] != 0;
         const int i = x.qb * T + r;
         float m_run = NEG_INF, l_run = 0.f;
         bool ok = true;
@@ -668,9 +816,14 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             ++o_cnt;
             tc_fence_after();
         }
-        const bool row_ok = store && i < a.S;
+        // the row's sequence, length and offsets, decoded again here so that
+        // none of them stays live across the tile loop
+        RowInfo e;
+        decode_row<kVarlen>(x.row, a, e);
+        const bool row_ok = store && i < e.S;
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
-        __nv_bfloat16 *orow = a.O + x.b * a.o_sb + static_cast<int64_t>(i) * a.o_ss + qh * a.o_sh;
+        __nv_bfloat16 *orow =
+            a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
             uint32_t o[32];
@@ -695,12 +848,13 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             }
         }
         if (row_ok && a.LSE)
-            a.LSE[(static_cast<int64_t>(x.b) * a.Hq + qh) * a.S + i] =
+            a.LSE[e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
                 l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
         tc_fence_before();
     }
 }
 
+template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     hybrid_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -747,12 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 8) {
         regs_dec<kCtrlRegs>();
         if (warp == kProducerWarp)
-            producer_role(&tm_q, &tm_k, &tm_v, a, sm, lane);
+            producer_role<kVarlen>(&tm_q, &tm_k, &tm_v, a, sm, lane);
         else if (warp == kMmaWarp)
             mma_role(a, sm, tmem, lane);
     } else {
         regs_inc<kSoftmaxRegs>();
-        softmax_role(a, sm, tmem, warp);
+        softmax_role<kVarlen>(a, sm, tmem, warp);
     }
 
     tc_fence_before();
@@ -814,6 +968,8 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
         return EA_ERR_INVALID_ARG;
     a.qb_begin = qb_begin;
     a.qb_end = qb_end;
+    a.lse_sb = static_cast<int64_t>(Hq) * S;
+    a.lse_sh = S;
     a.n_rows = static_cast<uint32_t>(n_rows);
     a.n_items = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * (qb_end - qb_begin) * npairs);
     return EA_OK;
@@ -828,7 +984,11 @@ static ea_status ensure_attributes()
         return EA_ERR_CUDA;
     if (dev < 64 && g_attr_done[dev])
         return EA_OK;
-    if (cudaFuncSetAttribute(hybrid_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(hybrid_prefill_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPrefillSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(hybrid_prefill_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPrefillSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(int) * (EA_MAX_SEQ / T + 2))) != cudaSuccess)
@@ -858,6 +1018,9 @@ ea_status prefill_plan_range(int B, int S, int Hq, int Hkv, int d, const uint8_t
     plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
+
+static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const PrefillArgs &a, void *stream);
 
 ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                const int64_t q_str[4], const int64_t kv_str[4],
@@ -894,11 +1057,22 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
     a.LSE = LSE;
     a.visited = visited_bitmap;
     a.scale_log2 = scale * 1.4426950408889634f;
+    return launch_attend(tq, tk, tv, a, stream);
+}
+
+// The persistent attention launch over a plan made with the same arguments.
+static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const PrefillArgs &a, void *stream)
+{
+    ea_status s;
     if ((s = ensure_attributes()) != EA_OK)
         return s;
     // The register split inside the kernel assumes this launch size.
+    const bool varlen = a.cu_seqlens != nullptr;
     cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, hybrid_prefill_kernel) != cudaSuccess)
+    if (cudaFuncGetAttributes(&fa, varlen ? reinterpret_cast<const void *>(hybrid_prefill_kernel<true>)
+                                          : reinterpret_cast<const void *>(hybrid_prefill_kernel<false>)) !=
+        cudaSuccess)
         return EA_ERR_CUDA;
     if (fa.numRegs != kLaunchRegs)
         return EA_ERR_UNSUPPORTED;
@@ -910,12 +1084,104 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
         return EA_ERR_CUDA;
     const unsigned grid =
         static_cast<unsigned>(a.n_items < static_cast<uint32_t>(sms) ? a.n_items : sms);
-    hybrid_prefill_kernel<<<grid, kThreads, kPrefillSmemBytes, static_cast<cudaStream_t>(stream)>>>(
-        tq, tk, tv, a);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (varlen)
+        hybrid_prefill_kernel<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+    else
+        hybrid_prefill_kernel<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
 } // namespace ea
+
+extern "C" ea_status ea_hybrid_attn_prefill_varlen(
+    const void *Q, const void *K, const void *V, void *O, float *LSE, const int64_t q_str[3],
+    const int64_t kv_str[3], const int64_t o_str[3], const int32_t *cu_seqlens, int B,
+    int total_tokens, int max_seqlen, int Hq, int Hkv, int d, float scale, const uint8_t *m,
+    int sink, int window, const uint8_t *block_mask, int block_size, void *workspace,
+    size_t ws_bytes, void *stream)
+{
+    if (!Q || !K || !V || !O || !q_str || !kv_str || !o_str || !cu_seqlens || !m ||
+        !(scale > 0.f))
+        return EA_ERR_INVALID_ARG;
+    if (B < 1 || total_tokens < 1 || max_seqlen < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
+        sink < 0 || window < 1 || block_size != EA_TILE)
+        return EA_ERR_INVALID_ARG;
+    if (d != EA_HEAD_DIM || max_seqlen > EA_MAX_SEQ || Hkv > 65535)
+        return EA_ERR_UNSUPPORTED;
+    if (q_str[2] != 1 || kv_str[2] != 1 || o_str[2] != 1)
+        return EA_ERR_INVALID_ARG;
+    for (int k = 0; k < 2; ++k)
+        if (q_str[k] <= 0 || kv_str[k] <= 0 || o_str[k] <= 0 || q_str[k] % 8 || kv_str[k] % 8 ||
+            o_str[k] % 8)
+            return EA_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return EA_ERR_INVALID_ARG;
+    const PrefillVarlenWs L = prefill_varlen_ws_layout(B, total_tokens, Hq, Hkv);
+    const int g = Hq / Hkv;
+    const int npairs = (g + 1) / 2;
+    if (L.rows * npairs >= (int64_t(1) << 31))
+        return EA_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < L.total)
+        return EA_ERR_WORKSPACE;
+    // one packed sequence of total_tokens rows, batch extent 1
+    const int64_t q4[4] = {static_cast<int64_t>(total_tokens) * q_str[0], q_str[0], q_str[1], 1};
+    const int64_t kv4[4] = {static_cast<int64_t>(total_tokens) * kv_str[0], kv_str[0], kv_str[1], 1};
+    alignas(64) CUtensorMap tq, tk, tv;
+    if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, total_tokens, 1, q4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tk, K, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tv, V, d, Hkv, total_tokens, 1, kv4, 64, T, true))
+        return EA_ERR_INVALID_ARG;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    PrefillArgs a{};
+    a.m = m;
+    a.block_mask = block_mask;
+    a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
+    a.items = reinterpret_cast<uint32_t *>(ws + L.items);
+    a.hdr = reinterpret_cast<ea_ws_header *>(ws);
+    a.B = B;
+    a.S = max_seqlen;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.npairs = npairs;
+    a.nB = static_cast<int>(ceil_div(max_seqlen, T));
+    a.sink = sink < max_seqlen ? sink : max_seqlen;
+    a.window = window < max_seqlen ? window : max_seqlen;
+    a.qb_begin = 0;
+    a.qb_end = a.nB;
+    a.n_rows = static_cast<uint32_t>(L.rows);
+    a.n_items = static_cast<uint32_t>(L.rows * npairs);
+    a.O = static_cast<__nv_bfloat16 *>(O);
+    a.o_sb = 0;
+    a.o_ss = o_str[0];
+    a.o_sh = o_str[1];
+    a.LSE = LSE;
+    a.lse_sb = 0;
+    a.lse_sh = total_tokens;
+    a.visited = nullptr;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.cu_seqlens = cu_seqlens;
+    a.row_off = reinterpret_cast<int32_t *>(ws + L.row_off);
+    a.mask_off = reinterpret_cast<int64_t *>(ws + L.mask_off);
+    a.row_desc = reinterpret_cast<int2 *>(ws + L.row_desc);
+    a.max_seqlen = max_seqlen;
+    a.total_tokens = total_tokens;
+
+    ea_status s;
+    if ((s = ensure_attributes()) != EA_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int warps_per_cta = 8;
+    varlen_setup_kernel<<<1, 1024, 0, st>>>(a);
+    plan_costs_kernel<<<static_cast<unsigned>(ceil_div(a.n_rows, warps_per_cta)),
+                        warps_per_cta * 32, 0, st>>>(a);
+    plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return EA_ERR_CUDA;
+    return launch_attend(tq, tk, tv, a, stream);
+}
 
 extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
                                      int sink, int window, const uint8_t *block_mask,

@@ -261,3 +261,28 @@ def test_paged_decode_rejects_bad_arguments(L):
                        (dict(q=None), 1), (dict(Hq=30), 1), (dict(d=64), 2), (dict(ws=None), 3),
                        (dict(wsb=1024), 3)]:
         assert call(**kw) == expect, kw
+
+
+def test_varlen_prefill_rejects_bad_arguments(L):
+    B, total, maxS, Hq, Hkv = 3, 5000, 3000, 8, 2
+    need = L.ea_prefill_varlen_workspace_size(B, total, maxS, Hq, Hkv, 128)
+    assert need > 256 and L.ea_prefill_varlen_workspace_size(B, total, maxS, Hq, Hkv, 64) == 0
+    assert L.ea_prefill_varlen_workspace_size(B, total, (1 << 21) + 1, Hq, Hkv, 128) == 0
+
+    def call(**kw):
+        a = dict(Q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None, qs=_str(Hq * 128, 128, 1),
+                 kvs=_str(Hkv * 128, 128, 1), os_=_str(Hq * 128, 128, 1), cu=_fake(), B=B, total=total,
+                 maxS=maxS, Hq=Hq, Hkv=Hkv, d=128, scale=0.088, m=_fake(), sink=64, window=256, bm=None,
+                 bs=128, ws=_fake(0x100000), wsb=need)
+        a.update(kw)
+        return L.ea_hybrid_attn_prefill_varlen(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["qs"], a["kvs"],
+                                               a["os_"], a["cu"], a["B"], a["total"], a["maxS"], a["Hq"],
+                                               a["Hkv"], a["d"], a["scale"], a["m"], a["sink"], a["window"],
+                                               a["bm"], a["bs"], a["ws"], a["wsb"], None)
+
+    for kw, expect in [(dict(cu=None), 1), (dict(Q=None), 1), (dict(B=0), 1), (dict(total=0), 1),
+                       (dict(maxS=0), 1), (dict(Hkv=3), 1), (dict(window=0), 1), (dict(bs=64), 1),
+                       (dict(scale=0.0), 1), (dict(d=64), 2), (dict(maxS=(1 << 21) + 1), 2),
+                       (dict(qs=_str(Hq * 128, 128, 2)), 1), (dict(kvs=_str(Hkv * 128, 100, 1)), 1),
+                       (dict(Q=_fake(0x1008)), 1), (dict(ws=None), 3), (dict(wsb=need - 1), 3)]:
+        assert call(**kw) == expect, kw
