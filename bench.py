@@ -374,6 +374,9 @@ def run_ours(args, rank, world, dev):
     if not args.no_decode:
         decode = run_decode(args, dev, peaks, flush)
 
+    # ---- a variable-length serving batch in one launch
+    varlen = run_varlen(args, dev, peaks, flush)
+
     # ---- router latency (36-layer 64K shape: 8 KV heads, 128 -> 64 -> 2)
     router = run_router(dev)
 
@@ -399,6 +402,7 @@ def run_ours(args, rank, world, dev):
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "decode": decode,
+        "varlen": varlen,
         "router": router,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -496,6 +500,66 @@ def run_decode(args, dev, peaks, flush):
                          if cfg.B == 32 else None,
                          "peak_source": peaks["source"]},
             "gpu_launches_per_step": 3, "clocks": clk}
+
+
+def run_varlen(args, dev, peaks, flush):
+    """A serving-like prefill batch in one ea_hybrid_attn_prefill_varlen launch:
+    128 sequences of 256..8192 tokens (seeded uniform), packed back to back,
+    heads and routing of the 32K layer (32/8 heads, 2 FA + 6 SSA, 128/2048).
+    Work is counted per sequence with the same closed forms as the 32K line."""
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    cfg = wl.LLAMA_32K
+    rng = np.random.default_rng(11)
+    lens = [int(x) for x in rng.integers(256, 8193, size=128)]
+    total = sum(lens)
+    Q = wl.randn_bf16((total, cfg.Hq, cfg.d), seed=21, device=dev)
+    K = wl.randn_bf16((total, cfg.Hkv, cfg.d), seed=22, device=dev)
+    V = wl.randn_bf16((total, cfg.Hkv, cfg.d), seed=23, device=dev)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device=dev)
+    _, m1 = wl.routing_from_sa_heads(1, cfg.Hkv, cfg.sa_heads, cfg.fa_impl, cfg.sa_impl)
+    m_cpu = m1.repeat(len(lens), 1)
+    m = m_cpu.to(dev)
+    g = cfg.Hq // cfg.Hkv
+    useful = tile = 0
+    for L in lens:
+        for h in range(cfg.Hkv):
+            mode = int(m_cpu[0, h])
+            useful += kept_pairs_per_kv_head(mode, L, cfg.sink, cfg.window) * g
+            tile += visited_tiles_per_kv_head(mode, L, cfg.sink, cfg.window) * g
+    useful *= 4 * cfg.d
+    tile *= 4 * cfg.d * 128 * 128
+    ws = ea.prefill_varlen_workspace(len(lens), total, max(lens), cfg.Hq, cfg.Hkv, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(cfg.Hq, total, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ea.ea_hybrid_attn_prefill_varlen(Q, K, V, cu, m, max_seqlen=max(lens), sink=cfg.sink,
+                                         window=cfg.window, O=O, LSE=LSE, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(5, min(args.steps, 20))):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in the variable-length prefill")
+    ms = statistics.median(x.elapsed_time(y) for x, y in ts)
+    return {"workload": "128 sequences of 256..8192 tokens (%d in all), 32/8 heads, 2 FA + 6 SSA" % total,
+            "ms_per_step": round(ms, 4),
+            "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 1),
+            "visited_tile_tflops": round(tile / (ms * 1e-3) / 1e12, 1),
+            "frac": round(tile / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "step": "setup + planner + fused kernel, one launch for all sequences",
+            "l2": "flushed before every timed step (256 MB memset, outside the events)"}
 
 
 def run_router(dev):
