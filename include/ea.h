@@ -182,9 +182,9 @@ ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, vo
  * followed by ea_prefill_attend with the same arguments and workspace.
  *
  * ea_prefill_plan enqueues the planner: per (b, KV head, 128-query block) the
- * number of key tiles that hold at least one kept pair, then a stable
- * longest-first work queue of (block, query-head pair) items, written to the
- * workspace.  ea_prefill_attend enqueues the persistent attention kernel that
+ * number of key tiles that hold at least one kept pair, then a longest-first
+ * work queue of (block, query-head pair) items (rows of equal cost in no set
+ * order; results do not depend on it), written to the workspace.  ea_prefill_attend enqueues the persistent attention kernel that
  * consumes that queue; it must follow a plan made with the same m,
  * block_mask, sink, window and sizes, on the same stream; one plan may feed
  * any number of ea_prefill_attend launches (the kernel re-arms the queue when

@@ -10,8 +10,8 @@
 // How (GB300 design, not the A100/H100 Block-Sparse-Attention kernel the pages
 // name as their implementation):
 //   1. plan_costs: visited key tiles per (b, KV head, 128-query block).
-//   2. plan_sort : one CTA, stable counting sort of those rows, longest first,
-//                  into a work queue of (row, head pair) items.
+//   2. plan_sort : one CTA, counting sort of those rows, longest first, into
+//                  a work queue of (row, head pair) items.
 //   3. hybrid_prefill_kernel: persistent, one CTA per SM, items taken from an
 //      atomic queue head.  An item is two query heads of one GQA group over one
 //      128-query block, so each K/V tile in shared memory feeds two MMAs.
@@ -249,9 +249,11 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         a.costs[warp] = n;
 }
 
-// One CTA: stable counting sort of the planned rows (cost >= 0) by visited-
-// tile count, longest first; each row contributes its npairs items back to
-// back.  Also resets the work queue head.
+// One CTA: counting sort of the planned rows (cost >= 0) by visited-tile
+// count, longest first; each row contributes its npairs items back to back.
+// The order among rows of equal cost is unspecified (every item is computed
+// the same way whatever the order, so results do not depend on it).  Also
+// resets the work queue head.
 __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
 {
     extern __shared__ int hist[];  // [nB + 2]
@@ -296,25 +298,28 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
         run += cnt;
     }
     __syncthreads();
-    // Stable scatter by one warp, 32 rows at a time in row order.
-    if (tid < 32) {
-        const unsigned lt = (1u << tid) - 1u;
-        for (uint32_t base = 0; base < a.n_rows; base += 32) {
-            const uint32_t r = base + tid;
+    // Scatter by every warp, 32 rows at a time: the lanes of a warp with the
+    // same cost take consecutive slots, their first lane claims them for the
+    // group with one shared-memory atomic.
+    {
+        const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+        const unsigned lt = (1u << lane) - 1u;
+        for (uint32_t base = warp * 32u; base < a.n_rows; base += 32u * nwarps) {
+            const uint32_t r = base + lane;
             const int c = r < a.n_rows ? a.costs[r] : -1;
             const bool valid = c >= 0;
             const unsigned active = __ballot_sync(0xffffffffu, valid);
             const unsigned peers = __match_any_sync(0xffffffffu, c) & active;
-            int pos = 0;
-            if (valid)
-                pos = hist[c] + __popc(peers & lt);
-            __syncwarp();
-            if (valid && (peers & lt) == 0)
-                hist[c] += __popc(peers);
-            __syncwarp();
-            if (valid)
+            const int leader = peers ? __ffs(peers) - 1 : 0;
+            int start = 0;
+            if (valid && lane == leader)
+                start = atomicAdd(&hist[c], __popc(peers));
+            start = __shfl_sync(0xffffffffu, start, leader);
+            if (valid) {
+                const int pos = start + __popc(peers & lt);
                 for (int p = 0; p < a.npairs; ++p)
                     a.items[static_cast<uint64_t>(pos) * a.npairs + p] = r * a.npairs + p;
+            }
         }
     }
     if (tid == 0) {
