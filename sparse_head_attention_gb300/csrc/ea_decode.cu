@@ -12,7 +12,7 @@
 //     and the list of chunks.  Short SSA units get few chunks, long FA units
 //     many, so no CTA is spent on a handful of keys.
 //   decode_split_kernel: persistent, one CTA per SM walking the chunk list.
-//     Each chunk's keys stream through a 4-stage shared-memory ring filled by
+//     Each chunk's keys stream through a 6-stage shared-memory ring filled by
 //     TMA (64 keys x 256 B per K or V box); the group's query heads share each
 //     K/V row; fp32 online softmax per head.  Output: a partial (O / l, LSE)
 //     per (chunk, q head).

@@ -335,4 +335,13 @@ __device__ __forceinline__ void griddep_launch_dependents()
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// One 32-byte (256-bit) global store of eight 32-bit words; the address must
+// be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 } // namespace ea

@@ -25,7 +25,11 @@
 //                   finally normalise O and store O / LSE.
 //      TMEM: 512 columns = per head t: S_t / P_t (128 fp32 columns) + O_t (128);
 //      the PV MMA reads P straight from TMEM, so P never touches shared memory.
-//      Shared memory: Q (2 x 32 KB) and a 5-stage K/V ring (5 x 32 KB).
+//      Shared memory: Q (2 x 32 KB) and a 4-stage K/V ring (4 x 32 KB).
+//   Batches are either B sequences of one length S ([B][S][heads][d] tensors)
+//   or sequences of different lengths packed back to back (cu_seqlens); the
+//   attention kernel is compiled once for each, so that the fixed-length one
+//   carries none of the other's row decoding.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +42,7 @@ namespace ea {
 
 constexpr int T = EA_TILE;
 constexpr int D = EA_HEAD_DIM;
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
 constexpr int kProducerWarp = 8;
@@ -78,6 +82,7 @@ struct PrefillArgs {
     int64_t o_sb, o_ss, o_sh;
     float *LSE;
     int64_t lse_sb, lse_sh;      // LSE[b * lse_sb + qh * lse_sh + token]
+    int o_v8;                    // every O row starts 32-byte aligned: 256-bit stores
     const uint8_t *m;
     const uint8_t *block_mask;
     uint32_t *visited;
@@ -841,14 +846,21 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                     o[c] = 0u;
             }
             if (row_ok) {
+                uint32_t w[16];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(o[q4 * 8 + 0]) * inv_l, __uint_as_float(o[q4 * 8 + 1]) * inv_l);
-                    v.y = pack_bf16x2(__uint_as_float(o[q4 * 8 + 2]) * inv_l, __uint_as_float(o[q4 * 8 + 3]) * inv_l);
-                    v.z = pack_bf16x2(__uint_as_float(o[q4 * 8 + 4]) * inv_l, __uint_as_float(o[q4 * 8 + 5]) * inv_l);
-                    v.w = pack_bf16x2(__uint_as_float(o[q4 * 8 + 6]) * inv_l, __uint_as_float(o[q4 * 8 + 7]) * inv_l);
-                    *reinterpret_cast<uint4 *>(orow + ch * 32 + q4 * 8) = v;
+                for (int c = 0; c < 16; ++c)
+                    w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                       __uint_as_float(o[2 * c + 1]) * inv_l);
+                if (a.o_v8) {
+                    // whole 32-byte sectors: half the store instructions
+#pragma unroll
+                    for (int q8 = 0; q8 < 2; ++q8)
+                        st_global_v8(orow + ch * 32 + q8 * 16, &w[q8 * 8]);
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        *reinterpret_cast<uint4 *>(orow + ch * 32 + q4 * 8) =
+                            make_uint4(w[q4 * 4], w[q4 * 4 + 1], w[q4 * 4 + 2], w[q4 * 4 + 3]);
                 }
             }
         }
@@ -1059,6 +1071,8 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
     a.o_sb = o_str[0];
     a.o_ss = o_str[1];
     a.o_sh = o_str[2];
+    a.o_v8 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 && o_str[0] % 16 == 0 && o_str[1] % 16 == 0 &&
+             o_str[2] % 16 == 0;
     a.LSE = LSE;
     a.visited = visited_bitmap;
     a.scale_log2 = scale * 1.4426950408889634f;
@@ -1162,6 +1176,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.o_sb = 0;
     a.o_ss = o_str[0];
     a.o_sh = o_str[1];
+    a.o_v8 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 && o_str[0] % 16 == 0 && o_str[1] % 16 == 0;
     a.LSE = LSE;
     a.lse_sb = 0;
     a.lse_sh = total_tokens;
