@@ -25,7 +25,8 @@
 //                   finally normalise O and store O / LSE.
 //      TMEM: 512 columns = per head t: S_t / P_t (128 fp32 columns) + O_t (128);
 //      the PV MMA reads P straight from TMEM, so P never touches shared memory.
-//      Shared memory: Q (2 x 32 KB) and a 4-stage K/V ring (4 x 32 KB).
+//      Shared memory: Q (2 x 32 KB), a 3-stage K/V ring (3 x 32 KB) and the O
+//      tiles of both heads on their way out (2 x 32 KB, stored by TMA).
 //   Batches are either B sequences of one length S ([B][S][heads][d] tensors)
 //   or sequences of different lengths packed back to back (cu_seqlens); the
 //   attention kernel is compiled once for each, so that the fixed-length one
@@ -42,7 +43,7 @@ namespace ea {
 
 constexpr int T = EA_TILE;
 constexpr int D = EA_HEAD_DIM;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
 constexpr int kProducerWarp = 8;
@@ -65,6 +66,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // V is M
 struct __align__(1024) PrefillSmem {
     uint8_t q[2][kTileBytes];
     uint8_t kv[kStages][kTileBytes];
+    uint8_t ostage[2][kTileBytes];   // per head: 4 warps x (32 rows x two 64-column boxes)
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t q_full, q_empty;
@@ -684,7 +686,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
 // completed, so O_t can be rescaled in place without another wait.
 template <bool kVarlen>
 __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem,
-                                             int warp)
+                                             int warp, const CUtensorMap *tm_o)
 {
     uint32_t *err = &a.hdr->error;
     const int t = warp >> 2;                    // head of the pair handled by this warpgroup
@@ -834,6 +836,18 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
         __nv_bfloat16 *orow =
             a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh;
+        // Fixed-length batches: each warp stages its 32 rows in shared memory
+        // (128-byte swizzle, as the tensor map expects) and its lane 0 stores
+        // them with TMA, which skips rows past S.  Variable-length batches
+        // store directly: the rows past a sequence belong to the next one.
+        const bool staged = !kVarlen && store;
+        const int wrow = r & 31;
+        uint8_t *wstage = sm.ostage[t] + (warp & 3) * (kTileBytes / 4);
+        if (staged) {
+            if ((r & 31) == 0)
+                bulk_wait_read_all();     // the previous item's store has read the stage
+            __syncwarp();
+        }
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {
             uint32_t o[32];
@@ -845,12 +859,21 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                 for (int c = 0; c < 32; ++c)
                     o[c] = 0u;
             }
-            if (row_ok) {
-                uint32_t w[16];
+            uint32_t w[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                       __uint_as_float(o[2 * c + 1]) * inv_l);
+            for (int c = 0; c < 16; ++c)
+                w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                   __uint_as_float(o[2 * c + 1]) * inv_l);
+            if (staged) {
+                // columns ch*32 .. +31: box ch/2, 16-byte chunks (ch%2)*4 .. +3
+                uint8_t *box = wstage + (ch >> 1) * (kTileBytes / 8);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int c16 = (ch & 1) * 4 + j;
+                    *reinterpret_cast<uint4 *>(box + wrow * 128 + ((c16 ^ (wrow & 7)) << 4)) =
+                        make_uint4(w[j * 4], w[j * 4 + 1], w[j * 4 + 2], w[j * 4 + 3]);
+                }
+            } else if (row_ok) {
                 if (a.o_v8) {
                     // whole 32-byte sectors: half the store instructions
 #pragma unroll
@@ -864,18 +887,32 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                 }
             }
         }
+        if (staged) {
+            fence_proxy_async_smem();     // the stage's writes -> the TMA unit
+            __syncwarp();
+            if ((r & 31) == 0) {
+                const int row0 = x.qb * T + (warp & 3) * 32;
+                tma_store_4d(tm_o, wstage, 0, qh, row0, e.b);
+                tma_store_4d(tm_o, wstage + kTileBytes / 8, 64, qh, row0, e.b);
+                bulk_commit_group();
+            }
+        }
         if (row_ok && a.LSE)
             a.LSE[e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
                 l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
         tc_fence_before();
     }
+    // the last stores must be complete before the CTA (and its shared memory) goes
+    if ((threadIdx.x & 31) == 0)
+        bulk_wait_all();
 }
 
 template <bool kVarlen>
 __global__ void __launch_bounds__(kThreads, 1)
     hybrid_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a)
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
@@ -923,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_role(a, sm, tmem, lane);
     } else {
         regs_inc<kSoftmaxRegs>();
-        softmax_role<kVarlen>(a, sm, tmem, warp);
+        softmax_role<kVarlen>(a, sm, tmem, warp, &tm_o);
     }
 
     tc_fence_before();
@@ -1037,7 +1074,7 @@ ea_status prefill_plan_range(int B, int S, int Hq, int Hkv, int d, const uint8_t
 }
 
 static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const PrefillArgs &a, void *stream);
+                               const CUtensorMap &to, const PrefillArgs &a, void *stream);
 
 ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                const int64_t q_str[4], const int64_t kv_str[4],
@@ -1062,10 +1099,11 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
             return EA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
         return EA_ERR_INVALID_ARG;
-    alignas(64) CUtensorMap tq, tk, tv;
+    alignas(64) CUtensorMap tq, tk, tv, to;
     if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, S, B, q_str, 64, T, true) ||
         !encode_tmap_bf16_4d(&tk, K, d, Hkv, S, B, kv_str, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tv, V, d, Hkv, S, B, kv_str, 64, T, true))
+        !encode_tmap_bf16_4d(&tv, V, d, Hkv, S, B, kv_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&to, O, d, Hq, S, B, o_str, 64, 32, true))
         return EA_ERR_INVALID_ARG;
     a.O = static_cast<__nv_bfloat16 *>(O);
     a.o_sb = o_str[0];
@@ -1076,12 +1114,12 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
     a.LSE = LSE;
     a.visited = visited_bitmap;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return launch_attend(tq, tk, tv, a, stream);
+    return launch_attend(tq, tk, tv, to, a, stream);
 }
 
 // The persistent attention launch over a plan made with the same arguments.
 static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const PrefillArgs &a, void *stream)
+                               const CUtensorMap &to, const PrefillArgs &a, void *stream)
 {
     ea_status s;
     if ((s = ensure_attributes()) != EA_OK)
@@ -1105,9 +1143,9 @@ static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, con
         static_cast<unsigned>(a.n_items < static_cast<uint32_t>(sms) ? a.n_items : sms);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (varlen)
-        hybrid_prefill_kernel<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+        hybrid_prefill_kernel<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, to, a);
     else
-        hybrid_prefill_kernel<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, a);
+        hybrid_prefill_kernel<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, to, a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
@@ -1146,10 +1184,12 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     // one packed sequence of total_tokens rows, batch extent 1
     const int64_t q4[4] = {static_cast<int64_t>(total_tokens) * q_str[0], q_str[0], q_str[1], 1};
     const int64_t kv4[4] = {static_cast<int64_t>(total_tokens) * kv_str[0], kv_str[0], kv_str[1], 1};
-    alignas(64) CUtensorMap tq, tk, tv;
+    const int64_t o4[4] = {static_cast<int64_t>(total_tokens) * o_str[0], o_str[0], o_str[1], 1};
+    alignas(64) CUtensorMap tq, tk, tv, to;
     if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, total_tokens, 1, q4, 64, T, true) ||
         !encode_tmap_bf16_4d(&tk, K, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tv, V, d, Hkv, total_tokens, 1, kv4, 64, T, true))
+        !encode_tmap_bf16_4d(&tv, V, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&to, O, d, Hq, total_tokens, 1, o4, 64, 32, true))
         return EA_ERR_INVALID_ARG;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -1200,7 +1240,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return EA_ERR_CUDA;
-    return launch_attend(tq, tk, tv, a, stream);
+    return launch_attend(tq, tk, tv, to, a, stream);
 }
 
 extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
