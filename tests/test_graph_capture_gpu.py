@@ -1,0 +1,117 @@
+"""The entry points inside CUDA graphs: a call captured once and replayed with
+new input values (written into the same buffers) must give exactly what an
+eager call on those values gives.  Serving engines run decode steps this way."""
+import numpy as np
+import pytest
+import torch
+
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import workloads as wl
+from gpu_helpers import check_no_device_error, gpu_device
+
+pytestmark = pytest.mark.gpu
+FULL, SSA = ea.FULL, ea.SSA
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return gpu_device()
+
+
+def capture(fn):
+    """Warm up on a side stream (first-call attribute setup happens outside
+    the capture), then capture one call."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def test_decode_step_replayed(dev):
+    cfg = wl.DecodeConfig("t", B=4, Hq=16, Hkv=4, d=128, L=3000, sink=64, window=700)
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev, seqlens=[3000, 17, 1500, 2049])
+    m = torch.tensor([[FULL, SSA, SSA, FULL]] * 4, dtype=torch.uint8, device=dev)
+    ws = ea.decode_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.L, device=dev)
+    O = torch.empty_like(q)
+    LSE = torch.empty(cfg.B, cfg.Hq, dtype=torch.float32, device=dev)
+
+    def step():
+        ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m, sink=cfg.sink, window=cfg.window, O=O, LSE=LSE,
+                                 workspace=ws)
+
+    g = capture(step)
+    for seed in (5, 6, 7):
+        q.copy_(wl.randn_bf16(q.shape, seed=seed, device=dev))
+        sl.copy_(torch.tensor([3000 - seed, 1 + seed, 1500, 2049 + seed], dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        Og, Lg = O.clone(), LSE.clone()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(Og, O) and torch.equal(Lg, LSE), seed
+    check_no_device_error(ws)
+
+
+def test_prefill_replayed(dev):
+    B, S, Hq, Hkv = 1, 1500, 8, 2
+    Q, K, V = (t.to(dev) for t in wl.qkv(B, S, Hq, Hkv, 128, seed=40))
+    m = torch.tensor([[FULL, SSA]], dtype=torch.uint8, device=dev)
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+
+    def step():
+        ea.ea_hybrid_attn_prefill(Q, K, V, m, sink=32, window=400, O=O, LSE=LSE, workspace=ws)
+
+    g = capture(step)
+    for seed in (41, 42):
+        Q.copy_(wl.randn_bf16(Q.shape, seed=seed, device=dev))
+        m.copy_(torch.tensor([[SSA, FULL]] if seed == 42 else [[FULL, SSA]], dtype=torch.uint8))
+        g.replay()
+        torch.cuda.synchronize()
+        Og, Lg = O.clone(), LSE.clone()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(Og, O) and torch.equal(Lg, LSE), seed
+    check_no_device_error(ws)
+
+
+def test_varlen_prefill_and_router_replayed(dev):
+    lens = [700, 1, 300]
+    total, Hq, Hkv = sum(lens), 8, 2
+    Q = wl.randn_bf16((total, Hq, 128), seed=50, device=dev)
+    K = wl.randn_bf16((total, Hkv, 128), seed=51, device=dev)
+    V = wl.randn_bf16((total, Hkv, 128), seed=52, device=dev)
+    cu = torch.tensor([0, 700, 701, 1001], dtype=torch.int32, device=dev)
+    m = torch.tensor([[FULL, SSA]] * 3, dtype=torch.uint8, device=dev)
+    ws = ea.prefill_varlen_workspace(3, total, 700, Hq, Hkv, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(Hq, total, dtype=torch.float32, device=dev)
+    Kr = wl.randn_bf16((1, 4096, 8, 128), seed=53, device=dev)
+    W, b = wl.router_weights(0, d=128, hidden=64, device=dev)
+    r = torch.empty(1, 8, dtype=torch.uint8, device=dev)
+    mr = torch.empty_like(r)
+    lg = torch.empty(1, 8, 2, dtype=torch.float64, device=dev)
+
+    def step():
+        ea.ea_hybrid_attn_prefill_varlen(Q, K, V, cu, m, max_seqlen=700, sink=16, window=128, O=O,
+                                         LSE=LSE, workspace=ws)
+        ea.ea_route(Kr, W, b, r_out=r, m_out=mr, logits_out=lg)
+
+    g = capture(step)
+    for seed in (54, 55):
+        Q.copy_(wl.randn_bf16(Q.shape, seed=seed, device=dev))
+        Kr.copy_(wl.randn_bf16(Kr.shape, seed=seed + 10, device=dev))
+        g.replay()
+        torch.cuda.synchronize()
+        Og, Lg, lgg = O.clone(), LSE.clone(), lg.clone()
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(Og, O) and torch.equal(Lg, LSE) and torch.equal(lgg, lg), seed
+    check_no_device_error(ws)
