@@ -53,7 +53,7 @@ struct DecodeArgs {
     __nv_bfloat16 *O;
     int64_t o_sb, o_sh;
     float *LSE;
-    int B, Hq, Hkv, g, Lmax, sink, window, num_splits, max_splits;
+    int B, Hq, Hkv, g, Lmax, sink, window, num_splits, max_splits, num_sms;
     float scale_log2;
     // paged cache (page_size == 0: one contiguous [B][Lmax] cache)
     const int32_t *block_table;
@@ -115,26 +115,51 @@ __device__ __forceinline__ int paged_tiles(const KeySegs &ks, int &TA, int &TB)
     return TA + max(TL - TB, 0);
 }
 
-// One CTA: per-unit chunk counts (automatic: one chunk per
-// EA_DECODE_AUTO_CHUNK kept keys, or per as many keys of whole tiles for a
-// paged cache), their prefix sum, and the chunk list.
+// Kept keys of a unit as the split kernel walks them (whole tiles for a paged
+// cache).
+__device__ __forceinline__ int unit_work(const DecodeArgs &a, int u, bool &ok)
+{
+    KeySegs ks;
+    ok = unit_keys(a, u / a.Hkv, u % a.Hkv, ks);
+    int TA, TB;
+    return a.page_size ? paged_tiles(ks, TA, TB) * kDecKeys : ks.n;
+}
+
+// One CTA: per-unit chunk counts, their prefix sum, and the chunk list.  The
+// automatic chunk size aims at about four chunks per SM over the whole step
+// (fewer, longer chunks mean fewer partial results to write and merge), between
+// EA_DECODE_AUTO_CHUNK and EA_DECODE_MAX_CHUNK kept keys, so that a small
+// batch still spreads over every SM.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
 {
     __shared__ int scan_tmp[1024];
+    __shared__ unsigned long long total_work;
     griddep_launch_dependents();   // the split kernel may start its prologue
     const int units = a.B * a.Hkv;
     const int tid = threadIdx.x;
     const int per = (units + blockDim.x - 1) / blockDim.x;
     const int lo = tid * per, hi = min(lo + per, units);
+    if (tid == 0)
+        total_work = 0;
+    __syncthreads();
+    unsigned long long mine = 0;
+    for (int u = lo; u < hi; ++u) {
+        bool ok;
+        mine += static_cast<unsigned long long>(unit_work(a, u, ok));
+    }
+    atomicAdd(&total_work, mine);
+    __syncthreads();
+    const long long target = 4ll * (a.num_sms > 0 ? a.num_sms : 1);
+    long long chunk = (static_cast<long long>(total_work) + target - 1) / target;
+    chunk = chunk < EA_DECODE_AUTO_CHUNK ? EA_DECODE_AUTO_CHUNK
+                                         : (chunk > EA_DECODE_MAX_CHUNK ? EA_DECODE_MAX_CHUNK : chunk);
     int local = 0;
     for (int u = lo; u < hi; ++u) {
-        KeySegs ks;
-        if (!unit_keys(a, u / a.Hkv, u % a.Hkv, ks))
+        bool ok;
+        const int work = unit_work(a, u, ok);
+        if (!ok)
             raise_error(&a.hdr->error, EA_DEVERR_CHECK);
-        int TA, TB;
-        const int work = a.page_size ? paged_tiles(ks, TA, TB) * kDecKeys : ks.n;
-        int ns = a.num_splits > 0 ? a.num_splits
-                                  : (work + EA_DECODE_AUTO_CHUNK - 1) / EA_DECODE_AUTO_CHUNK;
+        int ns = a.num_splits > 0 ? a.num_splits : static_cast<int>((work + chunk - 1) / chunk);
         ns = ns < 1 ? 1 : (ns > a.max_splits ? a.max_splits : ns);
         a.unit_splits[u] = ns;
         local += ns;
@@ -682,6 +707,7 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     a.num_splits = num_splits;
     a.max_splits = max_splits;
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.num_sms = 0;   // set below
     a.block_table = block_table;
     a.bt_stride = bt_stride;
     a.page_size = page_size;
@@ -694,6 +720,7 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     const int sms = num_sms(dev);
     if (sms <= 0)
         return EA_ERR_CUDA;
+    a.num_sms = sms;
     const int64_t max_chunks = static_cast<int64_t>(B) * Hkv * max_splits;
     const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
     decode_plan_kernel<<<1, 1024, 0, st>>>(a);

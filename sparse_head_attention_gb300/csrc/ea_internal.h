@@ -71,6 +71,9 @@ struct DecodeWs {
 DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits);
 // Keys per chunk when the split count is automatic.
 #define EA_DECODE_AUTO_CHUNK 2048
+// Largest automatic decode chunk (kept keys); the planner picks a size between
+// the two from the step's total kept keys.
+#define EA_DECODE_MAX_CHUNK 8192
 int decode_max_splits(int Lmax, int num_splits);
 
 // Encodes a 4-D bf16 TMA tensor map (dims innermost first: head dim, heads,
