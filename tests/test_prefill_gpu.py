@@ -280,3 +280,28 @@ def test_longest_supported_sequence(dev):
                  LSE[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy(), Oref, Lref, "S=2^21")
     with pytest.raises(ValueError):
         ea.prefill_workspace(B, S + 1, Hq, Hkv, device=dev)
+
+
+def test_random_configurations_wider(dev):
+    # A second seeded sweep, longer sequences and group sizes up to 5; it holds
+    # rows whose outputs reach |O| > 2 (few kept keys), where bf16 output
+    # rounding matters for the tolerance.
+    rng = np.random.default_rng(777)
+    for case in range(30):
+        B = int(rng.integers(1, 4))
+        S = int(rng.integers(1, 1200))
+        Hkv = int(rng.integers(1, 4))
+        g = int(rng.integers(1, 6))
+        Hq = Hkv * g
+        sink = int(rng.integers(0, 300))
+        window = int(rng.integers(1, 700))
+        modes = rng.integers(0, 3, size=(B, Hkv)).astype(np.uint8)
+        density = float(rng.uniform(0.1, 0.9))
+        drop = rng.random((B, Hkv, (S + 127) // 128, (S + 127) // 128)) < 0.1
+        Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=5000 + case)
+        bm = wl.block_mask(B, Hkv, S, density=density, seed=case).numpy()
+        bm[drop] = 0
+        O, LSE, _ = run(dev, Q, K, V, modes, sink, window, bm=bm, visited=True)
+        Oref, Lref = oracle.prefill_full(Q, K, V, modes, sink=sink, window=window, block_mask=bm)
+        assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
+                     "case %d (B=%d S=%d Hq=%d Hkv=%d sink=%d window=%d)" % (case, B, S, Hq, Hkv, sink, window))
