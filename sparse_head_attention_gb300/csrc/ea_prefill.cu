@@ -205,6 +205,12 @@ __device__ __forceinline__ int seq_kb(int mode, int n, int n_sink, int kb_lo)
     return n < n_sink ? n : kb_lo + (n - n_sink);
 }
 
+// Word with the low n bits set (n clamped to 0..32).
+__device__ __forceinline__ uint32_t low_bits(int n)
+{
+    return n <= 0 ? 0u : n >= 32 ? 0xffffffffu : (1u << n) - 1u;
+}
+
 // Does every (query, key) pair of tile (qb, kb) pass the head's mask?  Only
 // tiles that fail this need per-element masking.
 __device__ __forceinline__ bool tile_is_full(int mode, int qb, int kb, int sink, int window)
@@ -739,17 +745,28 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
             tmem_wait_ld();
 
-            // mask edge tiles only
+            // mask edge tiles only: key j = j0 + c is kept when c <= hi (causal)
+            // and, for SSA, when c < sk (sink) or c > lo (inside the window).
+            // Each 32-column chunk gets one keep word built from three prefix
+            // masks; testing a bit against a constant column costs far less
+            // than re-deriving the three comparisons per column.
             const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
             if (edge) {
                 const int j0 = kb * T;
+                const int hi = i - j0;
+                int sk = -1, lo = -1;
+                if (mode == EA_SSA) {
+                    sk = a.sink - j0;
+                    lo = i - a.window - j0;
+                }
 #pragma unroll
-                for (int c = 0; c < 128; ++c) {
-                    const int j = j0 + c;
-                    const bool keep =
-                        j <= i && (mode != EA_SSA || j < a.sink || i - j < a.window);
-                    if (!keep)
-                        s[c] = __float_as_uint(NEG_INF);
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t w = low_bits(hi + 1 - 32 * q) &
+                                       (low_bits(sk - 32 * q) | ~low_bits(lo + 1 - 32 * q));
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        if (!((w >> c) & 1u))
+                            s[32 * q + c] = __float_as_uint(NEG_INF);
                 }
             }
             // row max: eight independent 3-input chains
