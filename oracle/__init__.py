@@ -20,6 +20,14 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   visited        - pinned: closed-form tile sets for FA/SSA, block mask for BLOCK.
   route          - pinned: hand-computed integer examples (tests/golden).
   sparsity_ratios- pinned: hand-counted masks (tests/golden), closed form for SSA.
+  xa_block_scores- pinned: stride 1 equals block sums of library softmax attention
+                   probabilities; a single nonzero query/key pair lights exactly the
+                   antidiagonal cell; Q = 0 gives the closed-form uniform scores; row
+                   totals equal the number of softmax rows.  The scoring itself is a
+                   reading (the pages name antidiagonal scoring without defining it).
+  xa_select      - pinned: tau = 0 keeps only the diagonal, tau = 1 keeps every block
+                   with mass, a planted dominant block is chosen, brute force over all
+                   subsets on small rows.
 """
 import ctypes
 import math
@@ -51,8 +59,12 @@ def lib():
                                       i32, i32, P, P, P, P]
         L.ea_oracle_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
                                                 P, P, P]
+        L.ea_oracle_xa_block_scores.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, i32, i32,
+                                                i32, i32, P]
+        L.ea_oracle_xa_select.argtypes = [P, i64, f64, P]
         for f in (L.ea_oracle_prefill_rows, L.ea_oracle_decode, L.ea_oracle_visited,
-                  L.ea_oracle_route, L.ea_oracle_sparsity_ratios):
+                  L.ea_oracle_route, L.ea_oracle_sparsity_ratios, L.ea_oracle_xa_block_scores,
+                  L.ea_oracle_xa_select):
             f.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -206,3 +218,51 @@ def sparsity_ratios(r, m, S, *, sink=0, window=1, block_masks=None, T=128):
     if rc != 0:
         raise ValueError("oracle sparsity_ratios rejected its arguments (rc=%d)" % rc)
     return msr.value, esr.value, kept
+
+
+def xa_block_scores(Q, K, b, h, *, stride=16, T=128, scale=None):
+    """XA antidiagonal block scores (float64 [nB, nB], zero above the diagonal) of
+    KV head h of batch row b, summed over the query heads that read it.
+    Q: bf16 [B, S, Hq, d]; K: bf16 [B, S, Hkv, d]."""
+    q, qs = _bf16_bits(Q)
+    k, ks = _bf16_bits(K)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    nB = (S + T - 1) // T
+    W = np.zeros((nB, nB), dtype=np.float64)
+    rc = lib().ea_oracle_xa_block_scores(_ptr(q), _ptr(qs), _ptr(k), _ptr(ks), S, Hq, Hkv, d,
+                                         scale, stride, T, b, h, _ptr(W))
+    if rc != 0:
+        raise ValueError("oracle xa_block_scores rejected its arguments (rc=%d)" % rc)
+    return W
+
+
+def xa_select(W, tau):
+    """XA threshold selection: uint8 [nB, nB] block mask from float64 scores [nB, nB]."""
+    W = np.ascontiguousarray(W, dtype=np.float64)
+    nB = W.shape[0]
+    assert W.shape == (nB, nB)
+    mask = np.zeros((nB, nB), dtype=np.uint8)
+    rc = lib().ea_oracle_xa_select(_ptr(W), nB, float(tau), _ptr(mask))
+    if rc != 0:
+        raise ValueError("oracle xa_select rejected its arguments (rc=%d)" % rc)
+    return mask
+
+
+def xa_estimate(Q, K, modes, *, stride=16, tau=0.9, T=128, scale=None):
+    """Scores float64 [B, Hkv, nB, nB] and block masks uint8 [B, Hkv, nB, nB] for the
+    heads whose mode is BLOCK (other heads' entries stay zero)."""
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    m = _u8(modes, B * Hkv).reshape(B, Hkv)
+    nB = (S + T - 1) // T
+    W = np.zeros((B, Hkv, nB, nB), dtype=np.float64)
+    M = np.zeros((B, Hkv, nB, nB), dtype=np.uint8)
+    for b in range(B):
+        for h in range(Hkv):
+            if m[b, h] == BLOCK:
+                W[b, h] = xa_block_scores(Q, K, b, h, stride=stride, T=T, scale=scale)
+                M[b, h] = xa_select(W[b, h], tau)
+    return W, M

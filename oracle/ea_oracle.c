@@ -439,3 +439,148 @@ int ea_oracle_sparsity_ratios(const uint8_t *r, const uint8_t *m, int L, int Hkv
     *esr = (double)pruned_total / ((double)L * (double)Hkv * (double)causal);
     return 0;
 }
+
+/*
+ * XA block scores of one (b, KV head): antidiagonal scoring.
+ * The pages name XA as XAttention, a training-free block-sparse attention that
+ * picks key blocks by antidiagonal scoring ([EN] Glossary "XA"; [ZH] glossary
+ * "XA"), with stride 16 and threshold 0.9 ([EN] §07 Table 8, "stride/threshold
+ * 16/0.9"; [EN] §01 "XA, tau=0.9"), but do not write the scoring out.  This
+ * follows the plainest reading of those words (listed with the other readings
+ * in the design doc):
+ *   - the score matrix is cut into s x s cells (s = stride): cell (a, c) holds
+ *     queries a*s .. a*s+s-1 and keys c*s .. c*s+s-1;
+ *   - a cell's score is the mean of the scaled logits on its antidiagonal
+ *     (query offset u pairs with key offset s-1-u):
+ *       A[a][c] = (scale / s) * sum_{u<s} <q[a*s+u], k[c*s+s-1-u]>;
+ *   - every downsampled query row a is normalised by a softmax over its causal
+ *     cells c <= a:  P[a][c] = exp(A[a][c]) / sum_{c'<=a} exp(A[a][c']);
+ *   - block (qb, kb) of the T x T block grid scores the sum of P over the cells
+ *     inside it and over the query heads that read this KV head (the block mask
+ *     is per KV head).
+ * Tokens at or beyond S contribute nothing to a cell's sum; cell rows and
+ * columns are the ceil(S/s) cells that hold at least one token.  T must be a
+ * multiple of s.
+ * W receives [nB][nB] (nB = ceil(S/T)), zero above the diagonal.
+ * Q strides qs[4] and K strides ks[4] are in elements over (b, s, h, dim).
+ */
+int ea_oracle_xa_block_scores(const uint16_t *Q, const int64_t *qs, const uint16_t *K,
+                              const int64_t *ks, int S, int Hq, int Hkv, int d, double scale,
+                              int stride, int T, int b, int h, double *W)
+{
+    if (S <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || stride <= 0 || T <= 0 ||
+        T % stride || h < 0 || h >= Hkv)
+        return -1;
+    const int g = Hq / Hkv;
+    const int64_t s = stride;
+    const int64_t nA = ((int64_t)S + s - 1) / s;
+    const int64_t nB = ((int64_t)S + T - 1) / T;
+    memset(W, 0, sizeof(double) * nB * nB);
+    double *A = (double *)malloc(sizeof(double) * nA);
+    if (!A)
+        return -2;
+    for (int qi = 0; qi < g; ++qi) {
+        const int qh = h * g + qi;
+        for (int64_t a = 0; a < nA; ++a) {
+            /* antidiagonal means of row a, for every causal cell c <= a */
+#pragma omp parallel for schedule(static)
+            for (int64_t c = 0; c <= a; ++c) {
+                double sum = 0.0;
+                for (int64_t u = 0; u < s; ++u) {
+                    const int64_t i = a * s + u, j = c * s + (s - 1 - u);
+                    if (i >= S || j >= S)
+                        continue;
+                    const uint16_t *q = Q + b * qs[0] + i * qs[1] + qh * qs[2];
+                    const uint16_t *k = K + b * ks[0] + j * ks[1] + h * ks[2];
+                    double dot = 0.0;
+                    for (int x = 0; x < d; ++x)
+                        dot += bf16_to_double(q[x * qs[3]]) * bf16_to_double(k[x * ks[3]]);
+                    sum += dot;
+                }
+                A[c] = scale * sum / (double)s;
+            }
+            /* softmax over c <= a */
+            double mx = -INFINITY;
+            for (int64_t c = 0; c <= a; ++c)
+                if (A[c] > mx)
+                    mx = A[c];
+            double den = 0.0;
+            for (int64_t c = 0; c <= a; ++c)
+                den += exp(A[c] - mx);
+            const int64_t qb = a * s / T;
+            for (int64_t c = 0; c <= a; ++c)
+                W[qb * nB + c * s / T] += exp(A[c] - mx) / den;
+        }
+    }
+    free(A);
+    return 0;
+}
+
+typedef struct {
+    double w;
+    int64_t kb;
+} oracle_xa_entry;
+
+/* Highest score first; equal scores by lower key block first. */
+static int oracle_xa_cmp(const void *x, const void *y)
+{
+    const oracle_xa_entry *p = (const oracle_xa_entry *)x, *q = (const oracle_xa_entry *)y;
+    if (p->w > q->w)
+        return -1;
+    if (p->w < q->w)
+        return 1;
+    return (p->kb > q->kb) - (p->kb < q->kb);
+}
+
+/*
+ * XA threshold selection over the block scores of one head (same reading as
+ * above; the threshold is [EN] §07 Table 8's 0.9): in every query-block row qb,
+ * order the causal key blocks kb <= qb by score, highest first (ties: lower kb
+ * first), and keep the shortest leading run whose scores add up to at least
+ * tau times the row's total.  If rounding leaves every run short of that, every
+ * block with a positive score is kept.  The diagonal block is always kept (every
+ * query attends to its own key).
+ * W: [nB][nB]; mask receives [nB][nB] bytes (1 = keep), zero above the diagonal.
+ */
+int ea_oracle_xa_select(const double *W, int64_t nB, double tau, uint8_t *mask)
+{
+    if (nB <= 0 || !(tau >= 0.0))
+        return -1;
+    oracle_xa_entry *e = (oracle_xa_entry *)malloc(sizeof(oracle_xa_entry) * nB);
+    if (!e)
+        return -2;
+    memset(mask, 0, (size_t)(nB * nB));
+    for (int64_t qb = 0; qb < nB; ++qb) {
+        const double *row = W + qb * nB;
+        uint8_t *out = mask + qb * nB;
+        double total = 0.0;
+        for (int64_t kb = 0; kb <= qb; ++kb) {
+            e[kb].w = row[kb];
+            e[kb].kb = kb;
+            total += row[kb];
+        }
+        qsort(e, (size_t)(qb + 1), sizeof(oracle_xa_entry), oracle_xa_cmp);
+        const double target = tau * total;
+        double run = 0.0;
+        int64_t n = -1;
+        for (int64_t k = 0; k <= qb; ++k) {
+            if (run >= target) {
+                n = k;
+                break;
+            }
+            run += e[k].w;
+        }
+        if (n < 0 && run >= target)
+            n = qb + 1;
+        if (n < 0) {
+            for (int64_t kb = 0; kb <= qb; ++kb)
+                out[kb] = row[kb] > 0.0;
+        } else {
+            for (int64_t k = 0; k < n; ++k)
+                out[e[k].kb] = 1;
+        }
+        out[qb] = 1;
+    }
+    free(e);
+    return 0;
+}
