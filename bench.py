@@ -26,6 +26,7 @@ GB/s of the kept KV-cache bytes reported beside it.
 of this method here) on a bounded row sample of the same workload.
 """
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -46,6 +47,7 @@ METRIC = "hybrid-attn prefill useful TFLOP/s (% bf16 peak); decode GB/s (% HBM)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+BLOCK_MODE = 2
 
 
 # ------------------------------------------------------------------ counting
@@ -385,6 +387,11 @@ def run_ours(args, rank, world, dev):
     # ---- router latency (36-layer 64K shape: 8 KV heads, 128 -> 64 -> 2)
     router = run_router(dev)
 
+    # ---- XA block-mask estimation and the XA-SSA layer that uses it (256K)
+    xa = None
+    if not args.no_xa:
+        xa = run_xa(args, dev, peaks, flush)
+
     # ---- sparsity ratios of the timed layer (host)
     msr, esr = ea.ea_sparsity_ratios(
         (m_cpu.numpy() == cfg.sa_impl).astype(np.uint8), m_cpu.numpy(), cfg.S, sink=cfg.sink,
@@ -409,6 +416,7 @@ def run_ours(args, rank, world, dev):
         "decode": decode,
         "varlen": varlen,
         "router": router,
+        "xa": xa,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V, m_cpu, bm_cpu, args)
@@ -564,6 +572,88 @@ def run_varlen(args, dev, peaks, flush):
             "visited_tile_tflops": round(tile / (ms * 1e-3) / 1e12, 1),
             "frac": round(tile / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "step": "setup + planner + fused kernel, one launch for all sequences",
+            "l2": "flushed before every timed step (256 MB memset, outside the events)"}
+
+
+def run_xa(args, dev, peaks, flush):
+    """XA block-mask estimation on the 256K XA-SSA layer (2 BLOCK + 6 SSA KV heads,
+    32 query heads), inputs with planted hot key blocks; then the whole XA-SSA
+    layer step: estimation of the BLOCK heads' masks followed by the fused prefill
+    (planner + kernel) that consumes them.  Estimation work: 2 * 16 * 128 flops per
+    causal 16 x 16 cell per query head (the antidiagonal's 16 dot products), or per
+    computed cell of the 128 x 256 cell tiles."""
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    cfg = wl.XA_SSA_256K
+    if args.xa_seq != cfg.S:
+        cfg = dataclasses.replace(cfg, name="xa_ssa_prefill_s%d" % args.xa_seq, S=args.xa_seq)
+    Q, K = wl.xa_planted_qk(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, cfg.d, seed=0, device=dev)
+    V = wl.randn_bf16((cfg.B, cfg.S, cfg.Hkv, cfg.d), seed=2, device=dev)
+    _, m_cpu = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads, cfg.fa_impl, cfg.sa_impl)
+    m = m_cpu.to(dev)
+    units = int((m_cpu == BLOCK_MODE).sum())
+    g = cfg.Hq // cfg.Hkv
+    nB = cfg.S // 128
+    nA = cfg.S // 16
+    useful = nA * (nA + 1) // 2 * 4096 * g * units
+    n_rt = (nA + 127) // 128
+    tile = sum(rt // 2 + 1 for rt in range(n_rt)) * 128 * 256 * 4096 * g * units
+    xws = ea.xa_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, units, device=dev)
+    bm = torch.zeros(cfg.B, cfg.Hkv, nB, nB, dtype=torch.uint8, device=dev)
+    pws = ea.prefill_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(cfg.B, cfg.Hq, cfg.S, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def estimate():
+        ea.ea_xa_estimate(Q, K, m, max_units=units, block_mask=bm, workspace=xws)
+
+    def layer():
+        estimate()
+        ea.ea_hybrid_attn_prefill(Q, K, V, m, sink=cfg.sink, window=cfg.window, block_mask=bm,
+                                  O=O, LSE=LSE, workspace=pws)
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(5, min(args.steps, 10))):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(x.elapsed_time(y) for x, y in ts)
+
+    est_ms = timed(estimate)
+    layer_ms = timed(layer)
+    if ea.ea_check_errors(xws) != 0 or ea.ea_check_errors(pws) != 0:
+        raise RuntimeError("device error in the XA estimation step")
+    bm_cpu = bm.cpu()
+    dens = []
+    pf_tile = 0
+    for h in range(cfg.Hkv):
+        mode = int(m_cpu[0, h])
+        head = bm_cpu[0, h].numpy() if mode == BLOCK_MODE else None
+        if head is not None:
+            dens.append(round(float(head.sum()) / (nB * (nB + 1) / 2), 4))
+        pf_tile += visited_tiles_per_kv_head(mode, cfg.S, cfg.sink, cfg.window, head) * g
+    pf_tile *= 4 * cfg.d * 128 * 128
+    del Q, K, V, O, LSE, xws, pws
+    return {"workload": "%s: 2 BLOCK + 6 SSA KV heads, 32 query heads, planted hot key blocks (5 %%); "
+                        "stride 16, threshold 0.9" % cfg.name,
+            "estimate_ms": round(est_ms, 4),
+            "estimate_useful_tflops": round(useful / (est_ms * 1e-3) / 1e12, 1),
+            "estimate_tile_tflops": round(tile / (est_ms * 1e-3) / 1e12, 1),
+            "estimate_frac": round(tile / (est_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "estimate_step": "unit list + antidiagonal score pass + threshold selection (3 launches)",
+            "block_density": dens,
+            "layer_ms": round(layer_ms, 4),
+            "layer_step": "estimation + planner + fused prefill on the estimated masks (5 launches)",
+            "layer_prefill_tile_tflops": round(pf_tile / ((layer_ms - est_ms) * 1e-3) / 1e12, 1),
             "l2": "flushed before every timed step (256 MB memset, outside the events)"}
 
 
@@ -876,6 +966,11 @@ def main():
                     help="chunks of the end-to-end pipelined call (0 = the library's choice)")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-xa", action="store_true", help="skip the XA estimation line")
+    ap.add_argument("--xa-only", action="store_true",
+                    help="time only the XA estimation (profiling helper; prints its object)")
+    ap.add_argument("--xa-seq", type=int, default=262144,
+                    help="sequence length of the XA line (262144 is the benchmark workload)")
     ap.add_argument("--decode-only", action="store_true",
                     help="time only the decode workload (profiling helper; prints its object)")
     ap.add_argument("--routed-layers", action="store_true",
@@ -914,6 +1009,11 @@ def main():
     if args.serial_sweep:
         if rank == 0:
             run_serial_sweep(args, dev)
+        return 0
+    if args.xa_only:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        if rank == 0:
+            print(json.dumps(run_xa(args, dev, measured_peaks(), flush)), flush=True)
         return 0
     if args.decode_only:
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)

@@ -411,6 +411,57 @@ ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pages, const 
                                       size_t ws_bytes, void *stream);
 
 /*
+ * ea_xa_estimate - XA block-mask estimation for the EA_BLOCK heads: scores each
+ * 128 x 128 block of every BLOCK head by antidiagonal scoring and keeps the
+ * smallest set of blocks per query-block row that holds `threshold` of the
+ * row's score.  The pages name XAttention's antidiagonal scoring as XA's way of
+ * choosing key blocks ([EN] Glossary "XA"; [ZH] glossary "XA") with stride 16
+ * and threshold 0.9 ([EN] §07 Table 8, "stride/threshold 16/0.9"), without
+ * writing the scoring out; this computes the following reading of it.
+ *
+ * With s = stride, cell (a, c) holds queries a*s .. a*s+s-1 and keys
+ * c*s .. c*s+s-1, and for every query head qh of the KV head h:
+ *   A[a][c]   = (scale / s) * sum_{u<s} q[a*s+u] . k[c*s+s-1-u]    (antidiagonal mean)
+ *   P[a][c]   = softmax over cells c <= a of A[a][c]
+ *   W[qb][kb] = sum over the group's query heads and the cells of block
+ *               (qb, kb) (cell rows a*s in qb, cell columns c*s in kb) of P
+ * Row qb of the mask keeps the fewest key blocks kb <= qb, highest W first
+ * (equal W: lower kb first), whose W add up to at least threshold times the
+ * row's total (all blocks with W > 0 if rounding leaves every run short), plus
+ * the diagonal block; every other entry is 0.  Rows of heads whose mode is not
+ * EA_BLOCK are not written.
+ *
+ *   Q            device bf16 [B][S][Hq][d],  element strides q_str[4]
+ *   K            device bf16 [B][S][Hkv][d], element strides k_str[4]
+ *   m            device uint8 [B][Hkv] (ea_mode values)
+ *   stride       must be 16;  S must be a multiple of it
+ *   threshold    in [0, 1] (the pages' value is 0.9)
+ *   block_size   must be 128 (the fused prefill's mask granularity)
+ *   max_units    upper bound on the number of (b, h) with m == EA_BLOCK; more
+ *                raise EA_DEVERR_CHECK (ea_check_errors) and the extra heads'
+ *                rows are not written
+ *   block_mask   device uint8 [B][Hkv][nB][nB] (output), nB = S / 128 rounded up
+ *   block_scores device float [B][Hkv][nB][nB] (output, W; 0 above the
+ *                diagonal), or NULL
+ *   workspace    device, >= ea_xa_workspace_size(...) bytes, 256-aligned
+ *
+ * Three stream-ordered launches (unit list, antidiagonal score pass on the
+ * tensor cores, selection); no host synchronisation.  Results do not depend on
+ * which CTA ran which work item.
+ * Constraints: d == 128; Hq % Hkv == 0 and Hq / Hkv <= 64; 16 <= S <= 2^21;
+ * base pointers 16-byte aligned; strides of the b, s and h dimensions multiples
+ * of 8 elements, head-dim stride 1.
+ * Errors: EA_ERR_INVALID_ARG, EA_ERR_UNSUPPORTED, EA_ERR_WORKSPACE on the host;
+ * EA_ERR_CUDA on a failed launch; device-side problems via ea_check_errors.
+ */
+size_t ea_xa_workspace_size(int B, int S, int Hq, int Hkv, int d, int stride, int max_units);
+ea_status ea_xa_estimate(const void *Q, const void *K, const int64_t q_str[4],
+                         const int64_t k_str[4], int B, int S, int Hq, int Hkv, int d, float scale,
+                         const uint8_t *m, int stride, float threshold, int block_size,
+                         int max_units, uint8_t *block_mask, float *block_scores, void *workspace,
+                         size_t ws_bytes, void *stream);
+
+/*
  * ea_sparsity_ratios - model sparsity ratio and effective sparsity ratio of one
  * input over L layers ([ZH] §02 Background, eqs. (4)-(5); [EN] §02).  HOST
  * function; all pointers are host memory; nothing touches the GPU.

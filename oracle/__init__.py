@@ -60,7 +60,7 @@ def lib():
         L.ea_oracle_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
                                                 P, P, P]
         L.ea_oracle_xa_block_scores.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, i32, i32,
-                                                i32, i32, P]
+                                                i32, i32, P, P]
         L.ea_oracle_xa_select.argtypes = [P, i64, f64, P]
         for f in (L.ea_oracle_prefill_rows, L.ea_oracle_decode, L.ea_oracle_visited,
                   L.ea_oracle_route, L.ea_oracle_sparsity_ratios, L.ea_oracle_xa_block_scores,
@@ -220,10 +220,11 @@ def sparsity_ratios(r, m, S, *, sink=0, window=1, block_masks=None, T=128):
     return msr.value, esr.value, kept
 
 
-def xa_block_scores(Q, K, b, h, *, stride=16, T=128, scale=None):
+def xa_block_scores(Q, K, b, h, *, stride=16, T=128, scale=None, qb_rows=None):
     """XA antidiagonal block scores (float64 [nB, nB], zero above the diagonal) of
     KV head h of batch row b, summed over the query heads that read it.
-    Q: bf16 [B, S, Hq, d]; K: bf16 [B, S, Hkv, d]."""
+    Q: bf16 [B, S, Hq, d]; K: bf16 [B, S, Hkv, d].  qb_rows: compute only these
+    query-block rows (the rest stay zero)."""
     q, qs = _bf16_bits(Q)
     k, ks = _bf16_bits(K)
     B, S, Hq, d = q.shape
@@ -232,8 +233,12 @@ def xa_block_scores(Q, K, b, h, *, stride=16, T=128, scale=None):
         scale = 1.0 / math.sqrt(d)
     nB = (S + T - 1) // T
     W = np.zeros((nB, nB), dtype=np.float64)
+    sel = None
+    if qb_rows is not None:
+        sel = np.zeros(nB, dtype=np.uint8)
+        sel[np.asarray(qb_rows, dtype=np.int64)] = 1
     rc = lib().ea_oracle_xa_block_scores(_ptr(q), _ptr(qs), _ptr(k), _ptr(ks), S, Hq, Hkv, d,
-                                         scale, stride, T, b, h, _ptr(W))
+                                         scale, stride, T, b, h, _ptr(sel), _ptr(W))
     if rc != 0:
         raise ValueError("oracle xa_block_scores rejected its arguments (rc=%d)" % rc)
     return W

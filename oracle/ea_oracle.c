@@ -461,12 +461,14 @@ int ea_oracle_sparsity_ratios(const uint8_t *r, const uint8_t *m, int L, int Hkv
  * Tokens at or beyond S contribute nothing to a cell's sum; cell rows and
  * columns are the ceil(S/s) cells that hold at least one token.  T must be a
  * multiple of s.
- * W receives [nB][nB] (nB = ceil(S/T)), zero above the diagonal.
+ * W receives [nB][nB] (nB = ceil(S/T)), zero above the diagonal; when qb_sel
+ * (bytes [nB]) is given, only the rows qb with qb_sel[qb] != 0 are computed and
+ * the others stay zero.
  * Q strides qs[4] and K strides ks[4] are in elements over (b, s, h, dim).
  */
 int ea_oracle_xa_block_scores(const uint16_t *Q, const int64_t *qs, const uint16_t *K,
                               const int64_t *ks, int S, int Hq, int Hkv, int d, double scale,
-                              int stride, int T, int b, int h, double *W)
+                              int stride, int T, int b, int h, const uint8_t *qb_sel, double *W)
 {
     if (S <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || d <= 0 || stride <= 0 || T <= 0 ||
         T % stride || h < 0 || h >= Hkv)
@@ -482,6 +484,8 @@ int ea_oracle_xa_block_scores(const uint16_t *Q, const int64_t *qs, const uint16
     for (int qi = 0; qi < g; ++qi) {
         const int qh = h * g + qi;
         for (int64_t a = 0; a < nA; ++a) {
+            if (qb_sel && !qb_sel[a * s / T])
+                continue;
             /* antidiagonal means of row a, for every causal cell c <= a */
 #pragma omp parallel for schedule(static)
             for (int64_t c = 0; c <= a; ++c) {

@@ -38,8 +38,8 @@ EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_worksp
            "ea_prefill_host_buffer_size", "ea_hybrid_attn_prefill_host",
            "ea_prefill_varlen_workspace_size", "ea_hybrid_attn_prefill_varlen",
            "ea_decode_workspace_size",
-           "ea_hybrid_attn_decode", "ea_hybrid_attn_decode_paged", "ea_sparsity_ratios",
-           "ea_check_errors")
+           "ea_hybrid_attn_decode", "ea_hybrid_attn_decode_paged", "ea_xa_workspace_size",
+           "ea_xa_estimate", "ea_sparsity_ratios", "ea_check_errors")
 
 
 class EAError(RuntimeError):
@@ -100,6 +100,11 @@ def lib():
                                                   i32, i32, P, i32, i32, i32, i32, f32, P, i32,
                                                   i32, i32, P, sz, P]
         L.ea_hybrid_attn_decode_paged.restype = ctypes.c_int
+        L.ea_xa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+        L.ea_xa_workspace_size.restype = sz
+        L.ea_xa_estimate.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, f32, P, i32, f32, i32,
+                                     i32, P, P, P, sz, P]
+        L.ea_xa_estimate.restype = ctypes.c_int
         L.ea_sparsity_ratios.argtypes = [P, P, i32, i32, i32, i32, i32, P, i32,
                                          ctypes.POINTER(f64), ctypes.POINTER(f64)]
         L.ea_check_errors.argtypes = [P, P]
@@ -462,6 +467,60 @@ def ea_hybrid_attn_decode_paged(q, K_pages, V_pages, block_table, seqlens, m, *,
         int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("ea_hybrid_attn_decode_paged", st)
     return O, LSE
+
+
+XA_STRIDE = 16
+
+
+def ea_xa_workspace_size(B, S, Hq, Hkv, max_units, d=128, stride=XA_STRIDE):
+    return int(lib().ea_xa_workspace_size(B, S, Hq, Hkv, d, stride, max_units))
+
+
+def xa_workspace(B, S, Hq, Hkv, max_units, d=128, device="cuda"):
+    """A zeroed XA estimation workspace for at most max_units BLOCK (b, KV head) units."""
+    n = ea_xa_workspace_size(B, S, Hq, Hkv, max_units, d)
+    if n == 0:
+        raise ValueError("unsupported XA estimation sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ea_xa_estimate(Q, K, m, *, threshold=0.9, max_units=None, block_mask=None,
+                   block_scores=None, want_scores=False, scale=None, workspace=None,
+                   stride=XA_STRIDE, stream=None):
+    """XA block-mask estimation (antidiagonal scoring) for the heads whose mode is
+    BLOCK.  Q [B, S, Hq, d], K [B, S, Hkv, d] bf16 (CUDA), m uint8 [B, Hkv] (CUDA).
+    Returns (block_mask uint8 [B, Hkv, nB, nB], block_scores float32 or None); rows
+    of other heads are left as they are in a caller-given block_mask (zeros in a
+    new one)."""
+    _dev(Q, "Q", torch.bfloat16)
+    _dev(K, "K", torch.bfloat16)
+    _dev(m, "m", torch.uint8)
+    B, S, Hq, d = Q.shape
+    Hkv = K.shape[2]
+    nB = (S + TILE - 1) // TILE
+    if max_units is None:
+        max_units = B * Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if block_mask is None:
+        block_mask = torch.zeros(B, Hkv, nB, nB, dtype=torch.uint8, device=Q.device)
+    _dev(block_mask, "block_mask", torch.uint8)
+    if not block_mask.is_contiguous():
+        raise ValueError("block_mask must be contiguous")
+    if block_scores is None and want_scores:
+        block_scores = torch.zeros(B, Hkv, nB, nB, dtype=torch.float32, device=Q.device)
+    if block_scores is not None:
+        _dev(block_scores, "block_scores", torch.float32)
+        if not block_scores.is_contiguous():
+            raise ValueError("block_scores must be contiguous")
+    if workspace is None:
+        workspace = xa_workspace(B, S, Hq, Hkv, max_units, d, Q.device)
+    st = lib().ea_xa_estimate(_ptr(Q), _ptr(K), _strides(Q), _strides(K), B, S, Hq, Hkv, d,
+                              float(scale), _ptr(m), int(stride), float(threshold), TILE,
+                              int(max_units), _ptr(block_mask), _ptr(block_scores),
+                              _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ea_xa_estimate", st)
+    return block_mask, block_scores
 
 
 def ea_sparsity_ratios(r, m, S, *, sink, window, block_masks=None):

@@ -122,6 +122,16 @@ __device__ __forceinline__ void tma_load_4d(void *smem_dst, const void *tmap, in
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void *smem_dst, const void *tmap, int c0, int c1, int c2,
+                                            int c3, int c4, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+                 "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Tiled TMA store of one box from shared memory (bulk-group completion).
 // Rows outside the tensor are not written.
 __device__ __forceinline__ void tma_store_4d(const void *tmap, const void *smem_src, int c0, int c1,

@@ -68,6 +68,30 @@ DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits)
     return w;
 }
 
+XaWs xa_ws_layout(int B, int S, int Hq, int Hkv, int max_units)
+{
+    (void)B;
+    XaWs w{};
+    const size_t g = Hq / Hkv;
+    const size_t u = static_cast<size_t>(max_units);
+    w.nA = S / EA_XA_STRIDE;
+    w.nct = ceil_div(w.nA, 256);
+    // rows a < nA hold 32 * (a / 256 + 1) sums each
+    const int64_t G = w.nA / 256, r = w.nA % 256;
+    w.tri = 32 * (256 * G * (G + 1) / 2 + r * (G + 1));
+    size_t off = sizeof(ea_ws_header);
+    w.units = off;
+    off = align_up(off + sizeof(int32_t) * u, 256);
+    w.tsum = off;
+    off = align_up(off + sizeof(float) * u * g * w.nA * w.nct, 256);
+    w.rmax = off;
+    off = align_up(off + sizeof(float) * u * g * w.nA * w.nct, 256);
+    w.esum = off;
+    off = align_up(off + sizeof(float) * u * g * w.tri, 256);
+    w.total = off;
+    return w;
+}
+
 // Chunks per unit: the caller's count, or one per EA_DECODE_AUTO_CHUNK keys of
 // the longest possible sequence.
 int decode_max_splits(int Lmax, int num_splits)
@@ -117,6 +141,29 @@ bool encode_tmap_bf16_4d(void *tmap_out, const void *base, int d, int H, int S, 
     return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_bf16_cells(void *tmap_out, const void *base, int d, int H, int stride, int nA,
+                            int B, const int64_t strides_elems[4], int box_rows)
+{
+    auto fn = get_encode_fn();
+    if (!fn)
+        return false;
+    // token t = a * stride + u: dims (dim, head, u, a, b) innermost first
+    cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(stride), static_cast<cuuint64_t>(nA),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[4] = {static_cast<cuuint64_t>(strides_elems[2]) * 2,
+                             static_cast<cuuint64_t>(strides_elems[1]) * 2,
+                             static_cast<cuuint64_t>(strides_elems[1]) * 2 * stride,
+                             static_cast<cuuint64_t>(strides_elems[0]) * 2};
+    cuuint32_t box[5] = {64u, 1u, 1u, static_cast<cuuint32_t>(box_rows), 1u};
+    cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+    CUresult r = fn(reinterpret_cast<CUtensorMap *>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                    const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int num_sms(int device)
 {
     int n = 0;
@@ -148,6 +195,16 @@ extern "C" size_t ea_prefill_workspace_size(int B, int S, int Hq, int Hkv, int d
     if (B < 1 || S < 1 || S > EA_MAX_SEQ || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d != EA_HEAD_DIM)
         return 0;
     return prefill_ws_layout(B, S, Hq, Hkv).total;
+}
+
+extern "C" size_t ea_xa_workspace_size(int B, int S, int Hq, int Hkv, int d, int stride,
+                                       int max_units)
+{
+    if (B < 1 || S < 1 || S > EA_MAX_SEQ || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 ||
+        d != EA_HEAD_DIM || stride != EA_XA_STRIDE || S % stride != 0 || max_units < 1 ||
+        static_cast<int64_t>(max_units) > static_cast<int64_t>(B) * Hkv)
+        return 0;
+    return xa_ws_layout(B, S, Hq, Hkv, max_units).total;
 }
 
 extern "C" size_t ea_prefill_varlen_workspace_size(int B, int total_tokens, int max_seqlen, int Hq,

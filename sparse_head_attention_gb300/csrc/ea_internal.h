@@ -83,6 +83,33 @@ bool encode_tmap_bf16_4d(void *tmap_out, const void *base, int d, int H, int S, 
                          const int64_t strides_elems[4], int box_inner, int box_rows,
                          bool swizzle128);
 
+// Encodes a 5-D bf16 TMA tensor map that reads tokens as cells of `stride`
+// consecutive tokens: dims (head dim, heads, offset u in the cell, cell a,
+// batch), token a * stride + u; the sequence length must be nA * stride.  Box:
+// 64 x 1 x 1 x box_rows x 1 with 128-byte swizzle (box_rows cells at one
+// offset u).
+bool encode_tmap_bf16_cells(void *tmap_out, const void *base, int d, int H, int stride, int nA,
+                            int B, const int64_t strides_elems[4], int box_rows);
+
+// XA estimation workspace (one slot per BLOCK (b, KV head) unit, at most
+// max_units): per slot and query head of the group, and per cell row and
+// 256-cell key tile, the row's max over the tile (log2 units) and the total of
+// exp2(score - max) over the tile; and the per-row sums of exp2(score - tile
+// max) over each key block (row a holds 32 * (a / 256 + 1) of them, rows packed
+// back to back).
+#define EA_XA_STRIDE 16
+struct XaWs {
+    int64_t nA;      // cell rows (S / stride)
+    int64_t nct;     // 256-cell key tiles (ceil(nA / 256))
+    int64_t tri;     // floats of one (unit, query head) row-sum block
+    size_t units;    // int32 [max_units]: b << 16 | h of each BLOCK unit
+    size_t tsum;     // float [max_units][g][nA][nct]
+    size_t rmax;     // float [max_units][g][nA][nct]
+    size_t esum;     // float [max_units][g][tri]
+    size_t total;
+};
+XaWs xa_ws_layout(int B, int S, int Hq, int Hkv, int max_units);
+
 int num_sms(int device);
 
 // Planner and attention launch restricted to query blocks [qb_begin, qb_end)

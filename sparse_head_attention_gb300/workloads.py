@@ -119,6 +119,31 @@ def block_mask(B: int, Hkv: int, S: int, density: float = 0.2, seed: int = 0,
     return keep.to(torch.uint8)
 
 
+def xa_planted_qk(B: int, S: int, Hq: int, Hkv: int, d: int, hot_frac: float = 0.05,
+                  gain: float = 0.67, seed: int = 0, device="cpu"):
+    """Q [B, S, Hq, d] and K [B, S, Hkv, d] bf16 with planted block structure, for
+    block-mask estimation: N(0, 1) entries (seeds 3*seed + {0, 1}); then, per
+    (b, KV head), a vector v of entries +-gain (random signs) is added to every
+    query of the heads that read it and to every key of a random set of 128-token
+    "hot" key blocks (each block hot with probability hot_frac; key block 0 always
+    hot).  Values are drawn in float32 and rounded to bf16 once, at the end."""
+    g = Hq // Hkv
+    Q = torch.randn((B, S, Hq, d), generator=_gen(3 * seed + 0, device), device=device)
+    K = torch.randn((B, S, Hkv, d), generator=_gen(3 * seed + 1, device), device=device)
+    nB = (S + TILE - 1) // TILE
+    gc = _gen(7919 * seed + 17, "cpu")
+    for b in range(B):
+        for h in range(Hkv):
+            v = (torch.randint(0, 2, (d,), generator=gc).float() * 2 - 1) * gain
+            hot = torch.rand(nB, generator=gc) < hot_frac
+            hot[0] = True
+            v = v.to(device)
+            Q[b, :, h * g:(h + 1) * g, :] += v
+            tok_hot = hot.repeat_interleave(TILE)[:S].to(device)
+            K[b, tok_hot, h, :] += v
+    return Q.to(torch.bfloat16), K.to(torch.bfloat16)
+
+
 def router_weights(layer: int, d: int = 128, hidden: int = 64, seed: int = 0,
                    beta: float = 0.0, device="cpu"):
     """Weights of the 2-layer router MLP d -> hidden -> 2 for one layer:

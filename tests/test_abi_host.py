@@ -286,3 +286,34 @@ def test_varlen_prefill_rejects_bad_arguments(L):
                        (dict(qs=_str(Hq * 128, 128, 2)), 1), (dict(kvs=_str(Hkv * 128, 100, 1)), 1),
                        (dict(Q=_fake(0x1008)), 1), (dict(ws=None), 3), (dict(wsb=need - 1), 3)]:
         assert call(**kw) == expect, kw
+
+
+def test_xa_estimate_rejects_bad_arguments(L):
+    B, S, Hq, Hkv = 1, 4096, 8, 2
+    need = L.ea_xa_workspace_size(B, S, Hq, Hkv, 128, 16, 2)
+    assert need > 256
+    assert L.ea_xa_workspace_size(B, S, Hq, Hkv, 128, 16, 3) == 0      # more units than heads
+    assert L.ea_xa_workspace_size(B, S + 8, Hq, Hkv, 128, 16, 2) == 0  # S not a multiple of 16
+    assert L.ea_xa_workspace_size(B, S, Hq, Hkv, 128, 8, 2) == 0       # stride 16 only
+    assert L.ea_xa_workspace_size(B, S, Hq, Hkv, 64, 16, 2) == 0
+    assert L.ea_xa_workspace_size(B, S, Hq, Hkv, 128, 16, 1) < need    # one unit needs less
+    assert L.ea_xa_workspace_size(B, 4 * S, Hq, Hkv, 128, 16, 2) > need
+
+    def call(**kw):
+        a = dict(Q=_fake(), K=_fake(), qs=_str(S * Hq * 128, Hq * 128, 128, 1),
+                 ks=_str(S * Hkv * 128, Hkv * 128, 128, 1), B=B,
+                 S=S, Hq=Hq, Hkv=Hkv, d=128, scale=0.088, m=_fake(), stride=16, tau=0.9, bs=128,
+                 units=2, bm=_fake(), sc=None, ws=_fake(0x100000), wsb=need)
+        a.update(kw)
+        return L.ea_xa_estimate(a["Q"], a["K"], a["qs"], a["ks"], a["B"], a["S"], a["Hq"], a["Hkv"],
+                                a["d"], a["scale"], a["m"], a["stride"], a["tau"], a["bs"],
+                                a["units"], a["bm"], a["sc"], a["ws"], a["wsb"], None)
+
+    for kw, expect in [(dict(Q=None), 1), (dict(K=None), 1), (dict(m=None), 1), (dict(bm=None), 1),
+                       (dict(B=0), 1), (dict(Hkv=3), 1), (dict(bs=64), 1), (dict(scale=0.0), 1),
+                       (dict(tau=-0.1), 1), (dict(tau=float("nan")), 1), (dict(units=0), 1),
+                       (dict(units=3), 1), (dict(d=64), 2), (dict(stride=8), 2), (dict(S=S + 8), 2),
+                       (dict(S=(1 << 21) + 16), 2), (dict(qs=_str(S * Hq * 128, Hq * 128, 128, 2)), 1),
+                       (dict(ks=_str(S * Hkv * 128, Hkv * 128, 100, 1)), 1), (dict(K=_fake(0x1008)), 1),
+                       (dict(ws=None), 3), (dict(ws=_fake(0x100010)), 3), (dict(wsb=need - 1), 3)]:
+        assert call(**kw) == expect, kw
