@@ -94,15 +94,21 @@ def prefill_work(cfg, m, bm):
     return 4 * cfg.d * useful, 4 * cfg.d * 128 * 128 * visited
 
 
-def decode_kept_bytes(cfg, m):
-    """K+V bytes of the kept cache entries (read once, shared by the group)."""
+def decode_kept_bytes(cfg, m, rows=None):
+    """K+V bytes of the kept cache entries (read once, shared by the group).
+    rows: the decode rows [B, Hkv, nB] of the block mask, for BLOCK heads."""
     keys = 0
     for b in range(cfg.B):
         for h in range(cfg.Hkv):
             L = cfg.L
-            if int(m[b, h]) == 1:
+            mode = int(m[b, h])
+            if mode == 1:
                 ns = min(cfg.sink, L)
                 keys += ns + (L - max(L - cfg.window, ns))
+            elif mode == BLOCK_MODE:
+                qb = (L - 1) // 128
+                kept = np.nonzero(np.asarray(rows[b, h, :qb + 1]))[0]
+                keys += int(sum(min(128, L - 128 * int(kb)) for kb in kept))
             else:
                 keys += L
     return keys * 2 * cfg.d * 2
@@ -465,6 +471,46 @@ def run_decode(args, dev, peaks, flush):
     t = statistics.mean(a.elapsed_time(b) for a, b in ms)
     gbs = nbytes / (t * 1e-3) / 1e9
 
+    # XA-SSA routing of the same cache: the two FA heads become BLOCK heads
+    # reading the kept blocks of their decode row (L - 1) / 128 of a block mask
+    # (each block kept with probability 0.2, the first and the query's own block
+    # always; only the decode rows are drawn, the other rows stay empty)
+    nBd = (cfg.L + 127) // 128
+    _, m_xa_cpu = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads, BLOCK_MODE, 1)
+    rows = torch.rand((cfg.B, cfg.Hkv, nBd), generator=torch.Generator().manual_seed(7)) < 0.2
+    rows[..., 0] = True
+    rows[..., (cfg.L - 1) // 128] = True
+    rows[..., (cfg.L - 1) // 128 + 1:] = False
+    bm_xa = torch.zeros((cfg.B, cfg.Hkv, nBd, nBd), dtype=torch.uint8, device=dev)
+    bm_xa[:, :, (cfg.L - 1) // 128, :] = rows.to(torch.uint8).to(dev)
+    m_xa = m_xa_cpu.to(dev)
+    xbytes = decode_kept_bytes(cfg, m_xa_cpu.numpy(), rows.numpy())
+
+    def xa_step():
+        ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m_xa, sink=cfg.sink, window=cfg.window, O=O,
+                                 LSE=LSE, workspace=ws, block_mask=bm_xa)
+
+    for _ in range(args.warmup):
+        xa_step()
+    torch.cuda.synchronize()
+    xms = []
+    for _ in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        xa_step()
+        b.record(stream)
+        xms.append((a, b))
+    torch.cuda.synchronize()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in the XA-SSA decode")
+    tx = statistics.mean(a.elapsed_time(b) for a, b in xms)
+    del bm_xa
+    xa_ssa = {"routing": "2 BLOCK (decode rows of a 0.2-density block mask) + 6 SSA KV heads",
+              "value": round(xbytes / (tx * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(tx, 4),
+              "frac": round(xbytes / (tx * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+              "kept_kv_bytes_per_step": xbytes,
+              "gpu_launches_per_step": 4}
+
     # the same step over a paged cache: 256-row pages of all sequences
     # scattered through one pool by a random permutation
     page_size = 256
@@ -504,6 +550,7 @@ def run_decode(args, dev, peaks, flush):
             "l2": "inputs larger than L2 (%.1f GB of K/V cache), no flush between steps"
                   % (2 * cfg.B * cfg.L * cfg.Hkv * cfg.d * 2 / 1e9),
             "paged": paged,
+            "xa_ssa": xa_ssa,
             "kept_kv_bytes_per_step": nbytes,
             "roofline": {"bound": "hbm", "kernel": "decode_plan_kernel + decode_split_kernel + decode_merge_kernel",
                          "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

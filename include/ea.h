@@ -352,17 +352,24 @@ size_t ea_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lmax, int num
  * the current token) and query head qh (KV head h = qh / (Hq/Hkv)):
  *   EA_FULL : keys j in [0, L)
  *   EA_SSA  : keys j in [0, L) with j < sink or (L - 1) - j < window
+ *   EA_BLOCK: keys j in [0, L) with block_mask[b][h][(L - 1) / 128][j / 128] != 0
+ * i.e. exactly the keys the prefill's row L - 1 keeps under the same mode and
+ * mask (the block mask chosen at prefill is reused across decode steps; the
+ * pages give no other decode reading of it).
  * O[b][qh][:] = softmax(scale * q . k_j) V over those keys; LSE[b][qh] its
- * natural log-sum-exp.  L = 0 gives O = 0, LSE = -inf.  Work is split along
- * the key axis and merged by log-sum-exp.
+ * natural log-sum-exp.  L = 0, or no kept key, gives O = 0, LSE = -inf.  Work
+ * is split along the key axis and merged by log-sum-exp.
  *
  *   q        device bf16 [B][Hq][d], element strides q_str[3]
  *   Kc, Vc   device bf16 [B][Lmax][Hkv][d], element strides kv_str[4] (shared)
  *   O        device bf16 [B][Hq][d], element strides o_str[3]
  *   LSE      device float [B][Hq] contiguous, or NULL
  *   seqlens  device int32 [B], each in [0, Lmax] (checked on the device)
- *   m        device uint8 [B][Hkv]; EA_BLOCK is rejected (device error word):
- *            the pages define no decode reading of a block mask
+ *   m        device uint8 [B][Hkv] (ea_mode values)
+ *   block_mask  device uint8 [B][Hkv][nB][nB], nB = ceil(Lmax / 128), or NULL
+ *            if no head is EA_BLOCK (a BLOCK head without a mask is reported
+ *            by ea_check_errors); nB must not exceed 65535
+ *   block_size  must be 128
  *   num_splits  0 = automatic, else 1..1024 key-axis splits per (b, KV head)
  *   workspace   device, >= ea_decode_workspace_size(...) bytes, 256-aligned
  *
@@ -375,8 +382,8 @@ ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, v
                                 const int64_t q_str[3], const int64_t kv_str[4],
                                 const int64_t o_str[3], const int32_t *seqlens, int B, int Hq,
                                 int Hkv, int d, int Lmax, float scale, const uint8_t *m, int sink,
-                                int window, int num_splits, void *workspace, size_t ws_bytes,
-                                void *stream);
+                                int window, const uint8_t *block_mask, int block_size,
+                                int num_splits, void *workspace, size_t ws_bytes, void *stream);
 
 /*
  * ea_hybrid_attn_decode_paged - ea_hybrid_attn_decode on a paged KV cache: the
@@ -395,6 +402,7 @@ ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const void *Vc, v
  *   page_size    rows per page, a multiple of 64
  *   num_pages    pages in K_pages / V_pages; a table entry outside
  *                [0, num_pages) is reported by ea_check_errors and reads zeros
+ *   block_mask   as for ea_hybrid_attn_decode with Lmax = max_pages * page_size
  *   workspace    ea_decode_workspace_size(B, Hq, Hkv, d, max_pages * page_size,
  *                num_splits) bytes
  * Other arguments, constraints and errors as ea_hybrid_attn_decode; invalid
@@ -407,7 +415,8 @@ ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pages, const 
                                       const int32_t *block_table, int64_t bt_stride, int max_pages,
                                       int page_size, int num_pages, const int32_t *seqlens, int B,
                                       int Hq, int Hkv, int d, float scale, const uint8_t *m,
-                                      int sink, int window, int num_splits, void *workspace,
+                                      int sink, int window, const uint8_t *block_mask,
+                                      int block_size, int num_splits, void *workspace,
                                       size_t ws_bytes, void *stream);
 
 /*

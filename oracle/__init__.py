@@ -16,7 +16,8 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   prefill_rows   - pinned: library SDPA in fp64 with a dense mask, closed forms
                    (Q = 0, constant V, single kept key), SSA/BLOCK reductions to FA
                    and to block-local causal attention.
-  decode         - pinned: equals the prefill oracle's last row; library SDPA.
+  decode         - pinned: equals the prefill oracle's last row (FA, SSA and BLOCK
+                   with the same block mask); library SDPA.
   visited        - pinned: closed-form tile sets for FA/SSA, block mask for BLOCK.
   route          - pinned: hand-computed integer examples (tests/golden).
   sparsity_ratios- pinned: hand-counted masks (tests/golden), closed form for SSA.
@@ -53,7 +54,7 @@ def lib():
         L.ea_oracle_prefill_rows.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f64,
                                              P, i32, i32, P, i32, i64, P, P, P]
         L.ea_oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, f64,
-                                       P, i32, i32, P, P]
+                                       P, i32, i32, P, i32, P, P]
         L.ea_oracle_visited.argtypes = [i32, i32, i32, P, i32, i32, P, i32, i32, i32, P]
         L.ea_oracle_route.argtypes = [P, P, i32, i32, i32, i32, i32, i32, i32, P, P, P,
                                       i32, i32, P, P, P, P]
@@ -137,9 +138,10 @@ def prefill_full(Q, K, V, modes, **kw):
     return O.reshape(B, S, Hq, d), LSE.reshape(B, S, Hq).transpose(0, 2, 1).copy()
 
 
-def decode(q, Kc, Vc, seqlens, modes, *, sink=0, window=1, scale=None):
+def decode(q, Kc, Vc, seqlens, modes, *, sink=0, window=1, block_mask=None, T=128, scale=None):
     """O float64 [B, Hq, d], LSE float64 [B, Hq] of one decode step.
-    q: bf16 [B, Hq, d]; Kc, Vc: bf16 [B, Lmax, Hkv, d]; seqlens int [B]."""
+    q: bf16 [B, Hq, d]; Kc, Vc: bf16 [B, Lmax, Hkv, d]; seqlens int [B];
+    block_mask uint8 [B, Hkv, nB, nB] (nB = ceil(Lmax / T)) when any mode is BLOCK."""
     qq, qs = _bf16_bits(q)
     k, ks = _bf16_bits(Kc)
     v, vs = _bf16_bits(Vc)
@@ -152,9 +154,10 @@ def decode(q, Kc, Vc, seqlens, modes, *, sink=0, window=1, scale=None):
     m = _u8(modes, B * Hkv)
     O = np.zeros((B, Hq, d), dtype=np.float64)
     LSE = np.zeros((B, Hq), dtype=np.float64)
+    bm = _u8(block_mask)
     rc = lib().ea_oracle_decode(_ptr(qq), _ptr(qs), _ptr(k), _ptr(v), _ptr(ks), _ptr(sl),
                                 B, Hq, Hkv, d, Lmax, scale, _ptr(m), sink, window,
-                                _ptr(O), _ptr(LSE))
+                                _ptr(bm), T, _ptr(O), _ptr(LSE))
     if rc != 0:
         raise ValueError("oracle decode rejected its arguments (rc=%d)" % rc)
     return O, LSE

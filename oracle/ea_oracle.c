@@ -174,28 +174,34 @@ int ea_oracle_prefill_rows(const uint16_t *Q, const int64_t *qs,
  * Decode: one new query per sequence attends to its cached keys [0, L), with
  * L = seqlens[b] (the cache already holds the current token).  The routing
  * decision made at prefill is reused ([EN] §08 Commentary, stated limit ③:
- * routing is decided once per request, at prefill).  FA keeps every key;
- * SSA keeps j < sink or (L-1) - j < window.  BLOCK has no decode reading on
- * the pages: rejected with -2.
+ * routing is decided once per request, at prefill).  The query is the
+ * sequence's position L - 1 and keeps exactly the keys the prefill's row L - 1
+ * keeps under the same mask (oracle_allowed above): FA every key; SSA
+ * j < sink or (L-1) - j < window; BLOCK the keys of the blocks kept in row
+ * (L-1) / T of the head's block mask, which covers nB = ceil(Lmax / T) blocks
+ * and is reused across decode steps (the pages give no other decode reading).
+ * A query with no kept key gets O = 0 and LSE = -inf.
  * q strides qs[3] over (b, h, dim); cache strides kvs[4] over (b, pos, h, dim).
+ * block_mask: [B][Hkv][nB][nB] bytes, required if any mode is BLOCK.
  * O is [B][Hq][d] doubles, LSE is [B][Hq].
  */
 int ea_oracle_decode(const uint16_t *q, const int64_t *qs,
                      const uint16_t *Kc, const uint16_t *Vc, const int64_t *kvs,
                      const int32_t *seqlens, int B, int Hq, int Hkv, int d, int Lmax,
                      double scale, const uint8_t *modes, int sink, int window,
-                     double *O, double *LSE)
+                     const uint8_t *block_mask, int T, double *O, double *LSE)
 {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || Lmax <= 0)
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0 || Lmax <= 0 || T <= 0)
         return -1;
+    const int64_t nB = ((int64_t)Lmax + T - 1) / T;
     for (int b = 0; b < B; ++b) {
         if (seqlens[b] < 0 || seqlens[b] > Lmax)
             return -1;
         for (int h = 0; h < Hkv; ++h) {
             const int mode = modes[b * Hkv + h];
-            if (mode == ORACLE_BLOCK)
+            if (mode == ORACLE_BLOCK && !block_mask)
                 return -2;
-            if (mode != ORACLE_FULL && mode != ORACLE_SSA)
+            if (mode != ORACLE_FULL && mode != ORACLE_SSA && mode != ORACLE_BLOCK)
                 return -1;
         }
     }
@@ -212,8 +218,10 @@ int ea_oracle_decode(const uint16_t *q, const int64_t *qs,
                 o[c] = 0.0;
             double *s = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
             double mx = -INFINITY;
+            const uint8_t *bm = mode == ORACLE_BLOCK ? block_mask + ((int64_t)b * Hkv + h) * nB * nB
+                                                     : NULL;
             for (int64_t j = 0; j < L; ++j) {
-                const int keep = (mode == ORACLE_FULL) || (j < sink) || ((L - 1) - j < window);
+                const int keep = oracle_allowed(mode, L - 1, j, sink, window, bm, nB, T);
                 if (!keep) {
                     s[j] = NAN;
                     continue;
@@ -226,7 +234,7 @@ int ea_oracle_decode(const uint16_t *q, const int64_t *qs,
                 if (s[j] > mx)
                     mx = s[j];
             }
-            if (L == 0) {
+            if (L == 0 || mx == -INFINITY) {
                 LSE[(int64_t)b * Hq + qh] = -INFINITY;
                 free(s);
                 continue;

@@ -95,10 +95,10 @@ def lib():
         L.ea_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ea_decode_workspace_size.restype = sz
         L.ea_hybrid_attn_decode.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, f32,
-                                            P, i32, i32, i32, P, sz, P]
+                                            P, i32, i32, P, i32, i32, P, sz, P]
         L.ea_hybrid_attn_decode_paged.argtypes = [P, P, P, P, P, P, P, P, P, ctypes.c_int64, i32,
                                                   i32, i32, P, i32, i32, i32, i32, f32, P, i32,
-                                                  i32, i32, P, sz, P]
+                                                  i32, P, i32, i32, P, sz, P]
         L.ea_hybrid_attn_decode_paged.restype = ctypes.c_int
         L.ea_xa_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         L.ea_xa_workspace_size.restype = sz
@@ -403,10 +403,22 @@ def decode_workspace(B, Hq, Hkv, Lmax, num_splits=0, d=128, device="cuda"):
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def ea_hybrid_attn_decode(q, Kc, Vc, seqlens, m, *, sink, window, num_splits=0, scale=None,
-                          O=None, LSE=None, workspace=None, stream=None, want_lse=True):
+def _block_mask_arg(block_mask, B, Hkv, Lmax):
+    if block_mask is None:
+        return None
+    _dev(block_mask, "block_mask", torch.uint8)
+    nB = (Lmax + TILE - 1) // TILE
+    if tuple(block_mask.shape) != (B, Hkv, nB, nB) or not block_mask.is_contiguous():
+        raise ValueError("block_mask must be a contiguous [B, Hkv, %d, %d] tensor" % (nB, nB))
+    return block_mask
+
+
+def ea_hybrid_attn_decode(q, Kc, Vc, seqlens, m, *, sink, window, block_mask=None, num_splits=0,
+                          scale=None, O=None, LSE=None, workspace=None, stream=None, want_lse=True):
     """One decode step.  q [B, Hq, d], Kc/Vc [B, Lmax, Hkv, d] bf16 (CUDA),
-    seqlens int32 [B] (CUDA), m uint8 [B, Hkv] (CUDA).  Returns (O, LSE)."""
+    seqlens int32 [B] (CUDA), m uint8 [B, Hkv] (CUDA), block_mask uint8
+    [B, Hkv, nB, nB] (nB = ceil(Lmax / 128), CUDA) when a head is BLOCK.
+    Returns (O, LSE)."""
     _dev(q, "q", torch.bfloat16)
     _dev(Kc, "Kc", torch.bfloat16)
     _dev(Vc, "Vc", torch.bfloat16)
@@ -424,17 +436,18 @@ def ea_hybrid_attn_decode(q, Kc, Vc, seqlens, m, *, sink, window, num_splits=0, 
         LSE = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = decode_workspace(B, Hq, Hkv, Lmax, num_splits, d, q.device)
+    bm = _block_mask_arg(block_mask, B, Hkv, Lmax)
     st = lib().ea_hybrid_attn_decode(
         _ptr(q), _ptr(Kc), _ptr(Vc), _ptr(O), _ptr(LSE), _strides(q), _strides(Kc), _strides(O),
         _ptr(seqlens), B, Hq, Hkv, d, Lmax, float(scale), _ptr(m), int(sink), int(window),
-        int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
+        _ptr(bm), TILE, int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("ea_hybrid_attn_decode", st)
     return O, LSE
 
 
 def ea_hybrid_attn_decode_paged(q, K_pages, V_pages, block_table, seqlens, m, *, sink, window,
-                                num_splits=0, scale=None, O=None, LSE=None, workspace=None,
-                                stream=None, want_lse=True):
+                                block_mask=None, num_splits=0, scale=None, O=None, LSE=None,
+                                workspace=None, stream=None, want_lse=True):
     """One decode step over a paged cache.  q [B, Hq, d]; K_pages/V_pages
     [num_pages, page_size, Hkv, d] bf16; block_table int32 [B, max_pages] (key
     k of sequence b: row k % page_size of page block_table[b, k // page_size]);
@@ -460,11 +473,12 @@ def ea_hybrid_attn_decode_paged(q, K_pages, V_pages, block_table, seqlens, m, *,
         LSE = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = decode_workspace(B, Hq, Hkv, max_pages * page_size, num_splits, d, q.device)
+    bm = _block_mask_arg(block_mask, B, Hkv, max_pages * page_size)
     st = lib().ea_hybrid_attn_decode_paged(
         _ptr(q), _ptr(K_pages), _ptr(V_pages), _ptr(O), _ptr(LSE), _strides(q), _strides(K_pages),
         _strides(O), _ptr(block_table), block_table.stride(0), max_pages, page_size, num_pages,
         _ptr(seqlens), B, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window),
-        int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
+        _ptr(bm), TILE, int(num_splits), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("ea_hybrid_attn_decode_paged", st)
     return O, LSE
 

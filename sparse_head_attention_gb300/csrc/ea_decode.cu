@@ -6,8 +6,12 @@
 // A decode step reads every kept cache entry once, so it is bound by HBM
 // bandwidth.  The design reads each (b, KV head)'s kept keys exactly once and
 // shares every K/V row among the query heads of the GQA group:
+//   decode_blocks_kernel (only when a block mask is given): one warp per
+//     unit; for EA_BLOCK units the list of key blocks kept in the mask row of
+//     the query's block ((L - 1) / 128), ascending.
 //   decode_plan_kernel: per (b, KV head) unit the number of kept keys (FULL:
-//     [0, L); SSA: the sink [0, sink) and the window [L - window, L)), its
+//     [0, L); SSA: the sink [0, sink) and the window [L - window, L); BLOCK:
+//     the kept blocks' keys below L, walked as 64-key tiles), its
 //     chunk count (about 2048 keys each unless the caller fixes the count),
 //     and the list of chunks.  Short SSA units get few chunks, long FA units
 //     many, so no CTA is spent on a handful of keys.
@@ -55,6 +59,12 @@ struct DecodeArgs {
     float *LSE;
     int B, Hq, Hkv, g, Lmax, sink, window, num_splits, max_splits, num_sms;
     float scale_log2;
+    // block-sparse heads: mask [B][Hkv][nBm][nBm] (NULL when no head may be
+    // EA_BLOCK) and, per unit, the kept blocks of its decode row
+    const uint8_t *block_mask;
+    int nBm;
+    int32_t *blk_count;
+    uint16_t *blk_list;
     // paged cache (page_size == 0: one contiguous [B][Lmax] cache)
     const int32_t *block_table;
     int64_t bt_stride;
@@ -73,11 +83,15 @@ struct __align__(1024) DecSmem {
 };
 
 // Kept keys of one (b, KV head) unit as at most two contiguous ranges:
-// visited index v < n0 is key v, v >= n0 is key w0 + (v - n0).
+// visited index v < n0 is key v, v >= n0 is key w0 + (v - n0).  A BLOCK unit
+// (blk >= 0 kept blocks) is walked as 64-key tiles instead: two per kept
+// block, the last block cut at L (see block_tiles).
 struct KeySegs {
     int n;
     int n0;
     int w0;
+    int blk;      // kept blocks of a BLOCK unit, -1 otherwise
+    int L;
 };
 
 __device__ __forceinline__ bool unit_keys(const DecodeArgs &a, int b, int h, KeySegs &ks)
@@ -85,9 +99,16 @@ __device__ __forceinline__ bool unit_keys(const DecodeArgs &a, int b, int h, Key
     int L = a.seqlens[b];
     const int mode = a.m[b * a.Hkv + h];
     bool ok = true;
-    if (L < 0 || L > a.Lmax || mode > EA_SSA) {  // BLOCK has no decode reading
+    if (L < 0 || L > a.Lmax || mode > EA_BLOCK || (mode == EA_BLOCK && !a.block_mask)) {
         ok = false;
         L = 0;
+    }
+    ks.L = L;
+    ks.blk = -1;
+    if (mode == EA_BLOCK && ok) {
+        ks.blk = a.blk_count[b * a.Hkv + h];
+        ks.n0 = ks.w0 = ks.n = 0;
+        return true;
     }
     if (mode == EA_SSA) {
         const int ns = a.sink < L ? a.sink : L;
@@ -115,14 +136,54 @@ __device__ __forceinline__ int paged_tiles(const KeySegs &ks, int &TA, int &TB)
     return TA + max(TL - TB, 0);
 }
 
+// 64-key tiles of a BLOCK unit: two per kept block, except that the query's
+// own block (kept or not, the last one listed when kept) only reaches L.
+__device__ __forceinline__ int block_tiles(const DecodeArgs &a, int u, const KeySegs &ks)
+{
+    if (ks.blk <= 0)
+        return 0;
+    const int last = a.blk_list[static_cast<int64_t>(u) * a.nBm + ks.blk - 1];
+    const int tail = ks.L - last * EA_TILE;          // keys of the last block below L
+    return 2 * (ks.blk - 1) + (tail >= EA_TILE ? 2 : (tail + kDecKeys - 1) / kDecKeys);
+}
+
 // Kept keys of a unit as the split kernel walks them (whole tiles for a paged
-// cache).
+// cache or a BLOCK unit).
 __device__ __forceinline__ int unit_work(const DecodeArgs &a, int u, bool &ok)
 {
     KeySegs ks;
     ok = unit_keys(a, u / a.Hkv, u % a.Hkv, ks);
+    if (ks.blk >= 0)
+        return block_tiles(a, u, ks) * kDecKeys;
     int TA, TB;
     return a.page_size ? paged_tiles(ks, TA, TB) * kDecKeys : ks.n;
+}
+
+// One warp per unit: the key blocks kept in the unit's decode row of the block
+// mask (row (L - 1) / 128, blocks 0 .. (L - 1) / 128), ascending.
+__global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
+{
+    const int u = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+    if (u >= a.B * a.Hkv)
+        return;
+    const int b = u / a.Hkv, h = u % a.Hkv;
+    const int L = a.seqlens[b];
+    int count = 0;
+    if (a.m[u] == EA_BLOCK && L > 0 && L <= a.Lmax) {
+        const int qb = (L - 1) / EA_TILE;
+        const uint8_t *row = a.block_mask + ((static_cast<int64_t>(b) * a.Hkv + h) * a.nBm + qb) * a.nBm;
+        uint16_t *list = a.blk_list + static_cast<int64_t>(u) * a.nBm;
+        for (int k0 = 0; k0 <= qb; k0 += 32) {
+            const int kb = k0 + lane;
+            const bool keep = kb <= qb && row[kb] != 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+            if (keep)
+                list[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(kb);
+            count += __popc(bal);
+        }
+    }
+    if (lane == 0)
+        a.blk_count[u] = count;
 }
 
 // One CTA: per-unit chunk counts, their prefix sum, and the chunk list.  The
@@ -187,12 +248,14 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
 // Position of chunk c in the key stream.  Contiguous cache: visited keys
 // [v_begin, v_end) in tiles that start at any key.  Paged cache: the unit's
 // aligned tiles [v_begin, v_end) (tile indices), tile v at key
-// 64 * (v < TA ? v : TB + v - TA).
+// 64 * (v < TA ? v : TB + v - TA).  BLOCK unit (either cache): aligned tiles
+// [v_begin, v_end), tile v at key 128 * list[v / 2] + 64 * (v % 2).
 struct ChunkInfo {
     int b, h, v_begin, v_end;
     KeySegs ks;
     int a_tiles, b_begin, n_tiles;
     int TA, TB;
+    const uint16_t *list;     // BLOCK unit: its kept blocks (NULL otherwise)
 };
 
 __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
@@ -204,6 +267,17 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
     ci.h = u % a.Hkv;
     unit_keys(a, ci.b, ci.h, ci.ks);
     const int ns = a.unit_splits[u];
+    ci.list = nullptr;
+    if (ci.ks.blk >= 0) {
+        ci.list = a.blk_list + static_cast<int64_t>(u) * a.nBm;
+        const int nt = block_tiles(a, u, ci.ks);
+        const int len = (nt + ns - 1) / ns;
+        ci.v_begin = min(sp * len, nt);
+        ci.v_end = min(ci.v_begin + len, nt);
+        ci.n_tiles = ci.v_end - ci.v_begin;
+        ci.a_tiles = ci.b_begin = ci.TA = ci.TB = 0;
+        return ci;
+    }
     if (a.page_size) {
         const int nt = paged_tiles(ci.ks, ci.TA, ci.TB);
         const int len = (nt + ns - 1) / ns;
@@ -232,6 +306,12 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
 __device__ __forceinline__ void tile_rows(const DecodeArgs &a, const ChunkInfo &ci, int t,
                                           int &key0, int &nvalid)
 {
+    if (ci.list) {
+        const int v = ci.v_begin + t;
+        key0 = EA_TILE * ci.list[v >> 1] + kDecKeys * (v & 1);
+        nvalid = min(kDecKeys, ci.ks.L - key0);
+        return;
+    }
     if (a.page_size) {
         const int v = ci.v_begin + t;
         key0 = kDecKeys * (v < ci.TA ? v : ci.TB + (v - ci.TA));
@@ -428,7 +508,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             float x[4] = {sc[0][0] * a.scale_log2, sc[0][1] * a.scale_log2,
                           sc[1][0] * a.scale_log2, sc[1][1] * a.scale_log2};
             const int kcol[4] = {kw + 2 * qd, kw + 2 * qd + 1, kw + 8 + 2 * qd, kw + 9 + 2 * qd};
-            if (a.page_size) {
+            if (a.page_size && !ci.list) {
                 // aligned tile: keep key k iff (k < sink end or k >= window
                 // start) and k < L
                 const int L = ci.ks.w0 + (ci.ks.n - ci.ks.n0);
@@ -644,15 +724,19 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
                                const int64_t q_str[3], const int64_t kv_str[4],
                                const int64_t o_str[3], const int32_t *seqlens, int B, int Hq,
                                int Hkv, int d, int Lmax, float scale, const uint8_t *m, int sink,
-                               int window, int num_splits, void *workspace, size_t ws_bytes,
+                               int window, const uint8_t *block_mask, int block_size,
+                               int num_splits, void *workspace, size_t ws_bytes,
                                const int32_t *block_table, int64_t bt_stride, int page_size,
                                int num_pages, void *stream)
 {
     if (!q || !Kc || !Vc || !O || !q_str || !kv_str || !o_str || !seqlens || !m)
         return EA_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lmax < 1 || sink < 0 || window < 1 ||
-        !(scale > 0.f) || num_splits < 0 || num_splits > 1024)
+        !(scale > 0.f) || num_splits < 0 || num_splits > 1024 || block_size != EA_TILE)
         return EA_ERR_INVALID_ARG;
+    const int64_t nBm = ceil_div(Lmax, EA_TILE);
+    if (block_mask && nBm > 65535)
+        return EA_ERR_UNSUPPORTED;
     if (d != EA_HEAD_DIM || Hq / Hkv > 8 || B > 65535 || Hkv > 65535)
         return EA_ERR_UNSUPPORTED;
     if (q_str[2] != 1 || kv_str[3] != 1 || o_str[2] != 1)
@@ -669,7 +753,7 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     if (static_cast<int64_t>(B) * Hkv >= (int64_t(1) << (31 - kSplitBits)) ||
         static_cast<int64_t>(B) * Hkv * max_splits >= (int64_t(1) << 31))
         return EA_ERR_UNSUPPORTED;
-    const DecodeWs L = decode_ws_layout(B, Hq, Hkv, max_splits);
+    const DecodeWs L = decode_ws_layout(B, Hq, Hkv, max_splits, Lmax);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || ws_bytes < L.total)
         return EA_ERR_WORKSPACE;
 
@@ -708,6 +792,10 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     a.max_splits = max_splits;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.num_sms = 0;   // set below
+    a.block_mask = block_mask;
+    a.nBm = static_cast<int>(nBm);
+    a.blk_count = reinterpret_cast<int32_t *>(ws + L.blk_count);
+    a.blk_list = reinterpret_cast<uint16_t *>(ws + L.blk_list);
     a.block_table = block_table;
     a.bt_stride = bt_stride;
     a.page_size = page_size;
@@ -723,6 +811,10 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     a.num_sms = sms;
     const int64_t max_chunks = static_cast<int64_t>(B) * Hkv * max_splits;
     const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
+    if (block_mask) {
+        const int64_t threads = static_cast<int64_t>(B) * Hkv * 32;
+        decode_blocks_kernel<<<static_cast<unsigned>(ceil_div(threads, 256)), 256, 0, st>>>(a);
+    }
     decode_plan_kernel<<<1, 1024, 0, st>>>(a);
     const cudaError_t e = launch_decode(tk, tv, a, grid, st);
     if (e != cudaSuccess)
@@ -737,12 +829,13 @@ extern "C" ea_status ea_hybrid_attn_decode(const void *q, const void *Kc, const 
                                            const int64_t kv_str[4], const int64_t o_str[3],
                                            const int32_t *seqlens, int B, int Hq, int Hkv, int d,
                                            int Lmax, float scale, const uint8_t *m, int sink,
-                                           int window, int num_splits, void *workspace,
-                                           size_t ws_bytes, void *stream)
+                                           int window, const uint8_t *block_mask, int block_size,
+                                           int num_splits, void *workspace, size_t ws_bytes,
+                                           void *stream)
 {
     return decode_launch(q, Kc, Vc, O, LSE, q_str, kv_str, o_str, seqlens, B, Hq, Hkv, d, Lmax,
-                         scale, m, sink, window, num_splits, workspace, ws_bytes, nullptr, 0, 0, 0,
-                         stream);
+                         scale, m, sink, window, block_mask, block_size, num_splits, workspace,
+                         ws_bytes, nullptr, 0, 0, 0, stream);
 }
 
 extern "C" ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pages,
@@ -753,6 +846,7 @@ extern "C" ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pa
                                                  int num_pages, const int32_t *seqlens, int B,
                                                  int Hq, int Hkv, int d, float scale,
                                                  const uint8_t *m, int sink, int window,
+                                                 const uint8_t *block_mask, int block_size,
                                                  int num_splits, void *workspace, size_t ws_bytes,
                                                  void *stream)
 {
@@ -764,6 +858,7 @@ extern "C" ea_status ea_hybrid_attn_decode_paged(const void *q, const void *K_pa
     if (Lmax >= (int64_t(1) << 31))
         return EA_ERR_UNSUPPORTED;
     return decode_launch(q, K_pages, V_pages, O, LSE, q_str, kv_str, o_str, seqlens, B, Hq, Hkv,
-                         d, static_cast<int>(Lmax), scale, m, sink, window, num_splits, workspace,
-                         ws_bytes, block_table, bt_stride, page_size, num_pages, stream);
+                         d, static_cast<int>(Lmax), scale, m, sink, window, block_mask, block_size,
+                         num_splits, workspace, ws_bytes, block_table, bt_stride, page_size,
+                         num_pages, stream);
 }

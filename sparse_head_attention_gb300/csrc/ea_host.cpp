@@ -47,7 +47,7 @@ PrefillVarlenWs prefill_varlen_ws_layout(int B, int total_tokens, int Hq, int Hk
     return w;
 }
 
-DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits)
+DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits, int Lmax)
 {
     DecodeWs w{};
     const size_t units = static_cast<size_t>(B) * Hkv;
@@ -64,6 +64,10 @@ DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits)
     off = align_up(off + sizeof(float) * chunks * g * EA_HEAD_DIM, 256);
     w.partial_lse = off;
     off = align_up(off + sizeof(float) * chunks * g, 256);
+    w.blk_count = off;
+    off = align_up(off + sizeof(int32_t) * units, 256);
+    w.blk_list = off;
+    off = align_up(off + sizeof(uint16_t) * units * static_cast<size_t>(ceil_div(Lmax, EA_TILE)), 256);
     w.total = off;
     return w;
 }
@@ -221,7 +225,7 @@ extern "C" size_t ea_decode_workspace_size(int B, int Hq, int Hkv, int d, int Lm
     if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || d != EA_HEAD_DIM || Lmax < 1 ||
         num_splits < 0 || num_splits > 1024)
         return 0;
-    return decode_ws_layout(B, Hq, Hkv, decode_max_splits(Lmax, num_splits)).total;
+    return decode_ws_layout(B, Hq, Hkv, decode_max_splits(Lmax, num_splits), Lmax).total;
 }
 
 extern "C" ea_status ea_check_errors(void *workspace, void *stream)

@@ -66,9 +66,11 @@ struct DecodeWs {
     size_t chunks;       // int32 [B*Hkv*max_splits]: unit << 11 | split
     size_t partial_o;    // float [B*Hkv*max_splits][g][128]
     size_t partial_lse;  // float [B*Hkv*max_splits][g]
+    size_t blk_count;    // int32 [B*Hkv]: kept key blocks of a BLOCK unit's decode row
+    size_t blk_list;     // uint16 [B*Hkv][ceil(Lmax / 128)]: those blocks, ascending
     size_t total;
 };
-DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits);
+DecodeWs decode_ws_layout(int B, int Hq, int Hkv, int max_splits, int Lmax);
 // Keys per chunk when the split count is automatic.
 #define EA_DECODE_AUTO_CHUNK 2048
 // Largest automatic decode chunk (kept keys); the planner picks a size between

@@ -94,17 +94,19 @@ def _decode(L, **kw):
     a = dict(q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None, qs=_str(32 * 128, 128, 1),
              kvs=_str(4096 * 8 * 128, 8 * 128, 128, 1), os_=_str(32 * 128, 128, 1), sl=_fake(),
              B=4, Hq=32, Hkv=8, d=128, Lmax=4096, scale=0.088, m=_fake(), sink=128, window=4096,
-             ns=0, ws=_fake(0x100000), wsb=1 << 30, stream=None)
+             bm=None, bs=128, ns=0, ws=_fake(0x100000), wsb=1 << 30, stream=None)
     a.update(kw)
     return L.ea_hybrid_attn_decode(a["q"], a["K"], a["V"], a["O"], a["LSE"], a["qs"], a["kvs"], a["os_"],
                                    a["sl"], a["B"], a["Hq"], a["Hkv"], a["d"], a["Lmax"], a["scale"], a["m"],
-                                   a["sink"], a["window"], a["ns"], a["ws"], a["wsb"], a["stream"])
+                                   a["sink"], a["window"], a["bm"], a["bs"], a["ns"], a["ws"], a["wsb"],
+                                   a["stream"])
 
 
 @pytest.mark.parametrize("kw,expect", [
     (dict(q=None), 1), (dict(sl=None), 1), (dict(Hq=30), 1), (dict(ns=-1), 1), (dict(ns=1025), 1),
     (dict(window=0), 1), (dict(Hkv=2), 2), (dict(d=96), 2), (dict(kvs=_str(4096 * 8 * 128, 8 * 128, 128, 2)), 1),
-    (dict(ws=None), 3), (dict(wsb=1024), 3),
+    (dict(ws=None), 3), (dict(wsb=1024), 3), (dict(bs=64), 1), (dict(bs=64, bm=_fake()), 1),
+    (dict(bm=_fake(), Lmax=65536 * 128), 2),      # more than 65535 blocks per row
 ])
 def test_decode_rejects_bad_arguments_on_host(L, kw, expect):
     assert _decode(L, **kw) == expect
@@ -247,19 +249,20 @@ def test_paged_decode_rejects_bad_arguments(L):
         a = dict(q=_fake(), K=_fake(), V=_fake(), O=_fake(), LSE=None, qs=_str(32 * 128, 128, 1),
                  kvs=_str(256 * 8 * 128, 8 * 128, 128, 1), os_=_str(32 * 128, 128, 1), bt=_fake(),
                  bts=16, maxp=16, ps=256, nump=1024, sl=_fake(), B=4, Hq=32, Hkv=8, d=128,
-                 scale=0.088, m=_fake(), sink=128, window=4096, ns=0, ws=_fake(0x100000),
-                 wsb=1 << 30)
+                 scale=0.088, m=_fake(), sink=128, window=4096, bm=None, bs=128, ns=0,
+                 ws=_fake(0x100000), wsb=1 << 30)
         a.update(kw)
         return L.ea_hybrid_attn_decode_paged(a["q"], a["K"], a["V"], a["O"], a["LSE"], a["qs"], a["kvs"],
                                              a["os_"], a["bt"], a["bts"], a["maxp"], a["ps"], a["nump"],
                                              a["sl"], a["B"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["m"],
-                                             a["sink"], a["window"], a["ns"], a["ws"], a["wsb"], None)
+                                             a["sink"], a["window"], a["bm"], a["bs"], a["ns"], a["ws"],
+                                             a["wsb"], None)
 
     for kw, expect in [(dict(bt=None), 1), (dict(maxp=0), 1), (dict(nump=0), 1), (dict(bts=8), 1),
                        (dict(ps=100), 2), (dict(ps=32), 2), (dict(ps=0), 2),
                        (dict(maxp=1 << 20, bts=1 << 20, ps=1 << 12), 2),   # 2^32 rows per sequence
                        (dict(q=None), 1), (dict(Hq=30), 1), (dict(d=64), 2), (dict(ws=None), 3),
-                       (dict(wsb=1024), 3)]:
+                       (dict(wsb=1024), 3), (dict(bs=0), 1)]:
         assert call(**kw) == expect, kw
 
 

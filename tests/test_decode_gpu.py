@@ -19,13 +19,14 @@ def dev():
     return gpu_device()
 
 
-def run(dev, q, Kc, Vc, sl, modes, sink, window, num_splits=0):
+def run(dev, q, Kc, Vc, sl, modes, sink, window, num_splits=0, bm=None):
     B, Hq, _ = q.shape
     Lmax, Hkv = Kc.shape[1], Kc.shape[2]
     ws = ea.decode_workspace(B, Hq, Hkv, Lmax, num_splits, device=dev)
     O, LSE = ea.ea_hybrid_attn_decode(q.to(dev), Kc.to(dev), Vc.to(dev), sl.to(dev),
                                       torch.as_tensor(modes, dtype=torch.uint8).to(dev),
-                                      sink=sink, window=window, num_splits=num_splits, workspace=ws)
+                                      sink=sink, window=window, num_splits=num_splits, workspace=ws,
+                                      block_mask=None if bm is None else torch.as_tensor(bm).to(dev))
     torch.cuda.synchronize()
     check_no_device_error(ws)
     return O, LSE
@@ -51,7 +52,46 @@ def test_group_sizes(dev, Hq, Hkv):
     assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "g=%d" % (Hq // Hkv))
 
 
-def test_empty_sequence_and_block_rejection(dev):
+def _decode_mask(B, Hkv, Lmax, seqlens, seed):
+    """Random block mask over the decode rows, with one unit's decode row emptied
+    and one unit's diagonal block dropped (its last kept block is then a full one)."""
+    bm = wl.block_mask(B, Hkv, Lmax, density=0.3, seed=seed).numpy()
+    L0 = seqlens[0]
+    bm[0, 0, (L0 - 1) // 128, :] = 0                 # no kept key at all
+    L2 = seqlens[2]
+    bm[2, 1, (L2 - 1) // 128, (L2 - 1) // 128] = 0   # diagonal block dropped
+    return bm
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 7])
+def test_block_heads_match_oracle(dev, num_splits):
+    cfg = wl.DecodeConfig("t", B=4, Hq=8, Hkv=2, d=128, L=5000, sink=128, window=1000)
+    seqlens = [5000, 1, 4097, 1129]
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=seqlens)
+    modes = np.array([[BLOCK, BLOCK], [BLOCK, SSA], [FULL, BLOCK], [BLOCK, FULL]], np.uint8)
+    bm = _decode_mask(4, 2, cfg.L, seqlens, seed=31)
+    O, LSE = run(dev, q, Kc, Vc, sl, modes, cfg.sink, cfg.window, num_splits, bm=bm)
+    Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=cfg.sink, window=cfg.window, block_mask=bm)
+    assert np.isneginf(Lref[0, :4]).all(), "the emptied decode row must have no kept key"
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "splits=%d" % num_splits)
+
+
+def test_block_decode_equals_last_prefill_row_on_gpu(dev):
+    B, S, Hq, Hkv = 1, 1500, 8, 2
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=14)
+    bm = torch.as_tensor(wl.block_mask(B, Hkv, S, density=0.4, seed=15)).to(dev)
+    modes = torch.tensor([[BLOCK, SSA]], dtype=torch.uint8, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Q.to(dev), K.to(dev), V.to(dev), modes, sink=64, window=300,
+                                       block_mask=bm)
+    Od, Ld = ea.ea_hybrid_attn_decode(Q[:, S - 1].contiguous().to(dev), K.to(dev), V.to(dev),
+                                      torch.tensor([S], dtype=torch.int32, device=dev), modes,
+                                      sink=64, window=300, block_mask=bm)
+    torch.cuda.synchronize()
+    assert (Od[0].float() - O[0, S - 1].float()).abs().max().item() <= 1.6e-2
+    assert (Ld[0] - LSE[0, :, S - 1]).abs().max().item() <= 1e-3
+
+
+def test_empty_sequence_and_block_without_mask(dev):
     cfg = wl.DecodeConfig("t", B=2, Hq=8, Hkv=2, d=128, L=256, sink=4, window=16)
     q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=[0, 256])
     O, LSE = run(dev, q, Kc, Vc, sl, [[FULL, SSA], [FULL, SSA]], cfg.sink, cfg.window)

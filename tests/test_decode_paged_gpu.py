@@ -11,7 +11,7 @@ from sparse_head_attention_gb300 import workloads as wl
 from gpu_helpers import assert_close, check_no_device_error, gpu_device
 
 pytestmark = pytest.mark.gpu
-FULL, SSA = ea.FULL, ea.SSA
+FULL, SSA, BLOCK = ea.FULL, ea.SSA, ea.BLOCK
 
 
 @pytest.fixture(scope="module")
@@ -58,6 +58,32 @@ def test_matches_oracle(dev, page_size, num_splits):
     torch.cuda.synchronize()
     check_no_device_error(ws)
     Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=cfg.sink, window=cfg.window)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "page %d" % page_size)
+
+
+@pytest.mark.parametrize("page_size,num_splits", [(64, 0), (256, 0), (128, 5)])
+def test_block_heads_on_a_paged_cache(dev, page_size, num_splits):
+    """BLOCK heads read the kept blocks of their decode row through the block
+    table; the mask spans max_pages * page_size positions."""
+    cfg = wl.DecodeConfig("t", B=4, Hq=8, Hkv=2, d=128, L=3000, sink=100, window=1000)
+    lens = [3000, 1, 2049, 64 * 7]
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=lens)
+    modes = np.array([[BLOCK, SSA], [BLOCK, BLOCK], [FULL, BLOCK], [BLOCK, FULL]], np.uint8)
+    Kp, Vp, table = paged_from_contiguous(Kc, Vc, lens, page_size, seed=70 + page_size)
+    Lp = table.shape[1] * page_size
+    nBp, nBc = (Lp + 127) // 128, (cfg.L + 127) // 128
+    bm = wl.block_mask(cfg.B, cfg.Hkv, Lp, density=0.3, seed=page_size).numpy()
+    bm[2, 1, (lens[2] - 1) // 128, (lens[2] - 1) // 128] = 0     # diagonal block dropped
+    ws = ea.decode_workspace(cfg.B, cfg.Hq, cfg.Hkv, Lp, num_splits, device=dev)
+    O, LSE = ea.ea_hybrid_attn_decode_paged(q.to(dev), Kp.to(dev), Vp.to(dev), table.to(dev), sl.to(dev),
+                                            torch.as_tensor(modes).to(dev), sink=cfg.sink,
+                                            window=cfg.window, num_splits=num_splits, workspace=ws,
+                                            block_mask=torch.as_tensor(bm).to(dev))
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    assert nBp >= nBc
+    bmc = np.ascontiguousarray(bm[:, :, :nBc, :nBc])
+    Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=cfg.sink, window=cfg.window, block_mask=bmc)
     assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "page %d" % page_size)
 
 

@@ -213,20 +213,25 @@ def test_gqa_grouping_and_concatenation():
         np.testing.assert_array_equal(O[:, :, qh], Oh[:, :, 0])
 
 
-@pytest.mark.parametrize("mode", [FULL, SSA])
+@pytest.mark.parametrize("mode", [FULL, SSA, BLOCK])
 def test_decode_is_last_prefill_row(mode):
-    B, Hq, Hkv, d, Lmax, sink, window = 3, 4, 2, 16, 50, 3, 7
+    B, Hq, Hkv, d, Lmax, sink, window, T = 3, 4, 2, 16, 50, 3, 7, 8
     cfg = wl.DecodeConfig("t", B=B, Hq=Hq, Hkv=Hkv, d=d, L=Lmax, sink=sink, window=window)
     seqlens = [50, 1, 23]
     q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=seqlens)
     modes = np.full((B, Hkv), mode, np.uint8)
-    O, LSE = oracle.decode(q, Kc, Vc, sl, modes, sink=sink, window=window)
+    nB = (Lmax + T - 1) // T
+    bm = wl.block_mask(B, Hkv, Lmax, density=0.4, seed=5, T=T).numpy() if mode == BLOCK else None
+    O, LSE = oracle.decode(q, Kc, Vc, sl, modes, sink=sink, window=window, block_mask=bm, T=T)
     for b, L in enumerate(seqlens):
         Qp = torch.zeros(1, L, Hq, d, dtype=torch.bfloat16)
         Qp[0, L - 1] = q[b]
         rows = np.array([[0, qh, L - 1] for qh in range(Hq)])
+        nBL = (L + T - 1) // T
+        bmL = None if bm is None else np.ascontiguousarray(bm[b:b + 1, :, :nBL, :nBL])
         Op, Lp = oracle.prefill_rows(Qp, Kc[b:b + 1, :L].contiguous(), Vc[b:b + 1, :L].contiguous(),
-                                     modes[b:b + 1], rows, sink=sink, window=window)
+                                     modes[b:b + 1], rows, sink=sink, window=window, block_mask=bmL,
+                                     T=T)
         np.testing.assert_array_equal(O[b], Op)
         np.testing.assert_array_equal(LSE[b], Lp)
         # library check on the same row
@@ -235,16 +240,24 @@ def test_decode_is_last_prefill_row(mode):
             k = _f64(Kc[b, :L, qh // g])
             s = (k @ _f64(q[b, qh])) / math.sqrt(d)
             j = torch.arange(L)
-            keep = torch.ones(L, dtype=torch.bool) if mode == FULL else (j < sink) | ((L - 1) - j < window)
+            if mode == FULL:
+                keep = torch.ones(L, dtype=torch.bool)
+            elif mode == SSA:
+                keep = (j < sink) | ((L - 1) - j < window)
+            else:
+                keep = torch.as_tensor(bm[b, qh // g, (L - 1) // T][j // T] != 0)
             p = torch.softmax(s.masked_fill(~keep, -math.inf), 0)
             np.testing.assert_allclose(O[b, qh], (p @ _f64(Vc[b, :L, qh // g])).numpy(), atol=1e-12)
 
 
-def test_decode_rejects_block_heads():
-    cfg = wl.DecodeConfig("t", B=1, Hq=2, Hkv=1, d=8, L=8, sink=1, window=2)
+def test_decode_block_heads_need_a_mask_and_empty_rows_are_zero():
+    cfg = wl.DecodeConfig("t", B=1, Hq=2, Hkv=1, d=8, L=40, sink=1, window=2)
     q, Kc, Vc, sl = wl.decode_inputs(cfg)
     with pytest.raises(ValueError):
         oracle.decode(q, Kc, Vc, sl, np.array([[BLOCK]], np.uint8))
+    bm = np.zeros((1, 1, 5, 5), np.uint8)            # row (L - 1) / 8 keeps nothing
+    O, LSE = oracle.decode(q, Kc, Vc, sl, np.array([[BLOCK]], np.uint8), block_mask=bm, T=8)
+    assert (O == 0).all() and np.isneginf(LSE).all()
 
 
 @pytest.mark.parametrize("S,T,sink,window", [(70, 16, 5, 9), (128, 16, 16, 17), (100, 32, 0, 1),
