@@ -173,13 +173,29 @@ __global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
         const int qb = (L - 1) / EA_TILE;
         const uint8_t *row = a.block_mask + ((static_cast<int64_t>(b) * a.Hkv + h) * a.nBm + qb) * a.nBm;
         uint16_t *list = a.blk_list + static_cast<int64_t>(u) * a.nBm;
-        for (int k0 = 0; k0 <= qb; k0 += 32) {
-            const int kb = k0 + lane;
-            const bool keep = kb <= qb && row[kb] != 0;
-            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-            if (keep)
-                list[count + __popc(bal & ((1u << lane) - 1u))] = static_cast<uint16_t>(kb);
-            count += __popc(bal);
+        // 128 blocks per step: lane l tests blocks k0 + 4l .. k0 + 4l + 3 (four
+        // independent loads), then an exclusive scan of the lanes' counts
+        for (int k0 = 0; k0 <= qb; k0 += 128) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int kb = k0 + 4 * lane + j;
+                bits |= (kb <= qb && row[kb] != 0) ? (1u << j) : 0u;
+            }
+            const int mine = __popc(bits);
+            int incl = mine;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            int pos = count + incl - mine;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if ((bits >> j) & 1u)
+                    list[pos++] = static_cast<uint16_t>(k0 + 4 * lane + j);
+            count += __shfl_sync(0xffffffffu, incl, 31);
         }
     }
     if (lane == 0)
@@ -191,49 +207,69 @@ __global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
 // (fewer, longer chunks mean fewer partial results to write and merge), between
 // EA_DECODE_AUTO_CHUNK and EA_DECODE_MAX_CHUNK kept keys, so that a small
 // batch still spreads over every SM.
-__global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
+constexpr int kPlanThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
 {
-    __shared__ int scan_tmp[1024];
-    __shared__ unsigned long long total_work;
+    __shared__ long long red_work[kPlanThreads / 32];
+    __shared__ int red_chunks[kPlanThreads / 32];
     griddep_launch_dependents();   // the split kernel may start its prologue
     const int units = a.B * a.Hkv;
-    const int tid = threadIdx.x;
-    const int per = (units + blockDim.x - 1) / blockDim.x;
-    const int lo = tid * per, hi = min(lo + per, units);
-    if (tid == 0)
-        total_work = 0;
-    __syncthreads();
-    unsigned long long mine = 0;
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    const int per = (units + kPlanThreads - 1) / kPlanThreads;
+    const int lo = min(tid * per, units), hi = min(lo + per, units);
+    // each unit's work, kept in unit_splits until its split count replaces it
+    long long mine = 0;
+    bool bad = false;
     for (int u = lo; u < hi; ++u) {
         bool ok;
-        mine += static_cast<unsigned long long>(unit_work(a, u, ok));
+        const int work = unit_work(a, u, ok);
+        bad |= !ok;
+        a.unit_splits[u] = work;
+        mine += work;
     }
-    atomicAdd(&total_work, mine);
+    if (bad)
+        raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mine += __shfl_down_sync(0xffffffffu, mine, o);
+    if (lane == 0)
+        red_work[warp] = mine;
     __syncthreads();
+    long long total_work = 0;
+#pragma unroll
+    for (int w = 0; w < kPlanThreads / 32; ++w)
+        total_work += red_work[w];
     const long long target = 4ll * (a.num_sms > 0 ? a.num_sms : 1);
-    long long chunk = (static_cast<long long>(total_work) + target - 1) / target;
+    long long chunk = (total_work + target - 1) / target;
     chunk = chunk < EA_DECODE_AUTO_CHUNK ? EA_DECODE_AUTO_CHUNK
                                          : (chunk > EA_DECODE_MAX_CHUNK ? EA_DECODE_MAX_CHUNK : chunk);
     int local = 0;
     for (int u = lo; u < hi; ++u) {
-        bool ok;
-        const int work = unit_work(a, u, ok);
-        if (!ok)
-            raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+        const int work = a.unit_splits[u];
         int ns = a.num_splits > 0 ? a.num_splits : static_cast<int>((work + chunk - 1) / chunk);
         ns = ns < 1 ? 1 : (ns > a.max_splits ? a.max_splits : ns);
         a.unit_splits[u] = ns;
         local += ns;
     }
-    scan_tmp[tid] = local;
-    __syncthreads();
-    for (int off = 1; off < 1024; off <<= 1) {
-        const int v = tid >= off ? scan_tmp[tid - off] : 0;
-        __syncthreads();
-        scan_tmp[tid] += v;
-        __syncthreads();
+    // exclusive scan of the per-thread chunk counts: lanes, then warps
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
     }
-    int run = scan_tmp[tid] - local;
+    if (lane == 31)
+        red_chunks[warp] = incl;
+    __syncthreads();
+    int base = 0, grand = 0;
+#pragma unroll
+    for (int w = 0; w < kPlanThreads / 32; ++w) {
+        base += w < warp ? red_chunks[w] : 0;
+        grand += red_chunks[w];
+    }
+    int run = base + incl - local;
     for (int u = lo; u < hi; ++u) {
         a.unit_first[u] = run;
         const int ns = a.unit_splits[u];
@@ -241,8 +277,8 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeArgs a)
             a.chunks[run + sp] = (u << kSplitBits) | sp;
         run += ns;
     }
-    if (tid == 1023)
-        a.hdr->n_items = static_cast<uint32_t>(scan_tmp[1023]);
+    if (tid == 0)
+        a.hdr->n_items = static_cast<uint32_t>(grand);
 }
 
 // Position of chunk c in the key stream.  Contiguous cache: visited keys
@@ -815,7 +851,7 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
         const int64_t threads = static_cast<int64_t>(B) * Hkv * 32;
         decode_blocks_kernel<<<static_cast<unsigned>(ceil_div(threads, 256)), 256, 0, st>>>(a);
     }
-    decode_plan_kernel<<<1, 1024, 0, st>>>(a);
+    decode_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
     const cudaError_t e = launch_decode(tk, tv, a, grid, st);
     if (e != cudaSuccess)
         return EA_ERR_CUDA;

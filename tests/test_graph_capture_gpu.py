@@ -115,3 +115,51 @@ def test_varlen_prefill_and_router_replayed(dev):
         torch.cuda.synchronize()
         assert torch.equal(Og, O) and torch.equal(Lg, LSE) and torch.equal(lgg, lg), seed
     check_no_device_error(ws)
+
+
+def test_xa_ssa_estimation_prefill_and_decode_replayed(dev):
+    """XA-SSA in one graph: block-mask estimation from Q and K, the fused prefill
+    on the estimated masks, then a decode step whose BLOCK head reads them."""
+    BLOCK = ea.BLOCK
+    B, S, Hq, Hkv = 1, 2048, 8, 2
+    Qc, Kc = wl.xa_planted_qk(B, S, Hq, Hkv, 128, seed=50)
+    Q, K = Qc.to(dev), Kc.to(dev)
+    V = wl.randn_bf16((B, S, Hkv, 128), seed=51, device=dev)
+    m = torch.tensor([[BLOCK, SSA]], dtype=torch.uint8, device=dev)
+    nB = S // 128
+    xws = ea.xa_workspace(B, S, Hq, Hkv, 1, device=dev)
+    pws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    dws = ea.decode_workspace(B, Hq, Hkv, S, device=dev)
+    bm = torch.zeros(B, Hkv, nB, nB, dtype=torch.uint8, device=dev)
+    sc = torch.zeros(B, Hkv, nB, nB, dtype=torch.float32, device=dev)
+    O = torch.empty_like(Q)
+    LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    q = torch.empty(B, Hq, 128, dtype=torch.bfloat16, device=dev)
+    sl = torch.tensor([S], dtype=torch.int32, device=dev)
+    Od = torch.empty_like(q)
+    Ld = torch.empty(B, Hq, dtype=torch.float32, device=dev)
+
+    def step():
+        ea.ea_xa_estimate(Q, K, m, max_units=1, block_mask=bm, block_scores=sc, workspace=xws)
+        ea.ea_hybrid_attn_prefill(Q, K, V, m, sink=64, window=256, block_mask=bm, O=O, LSE=LSE,
+                                  workspace=pws)
+        ea.ea_hybrid_attn_decode(q, K, V, sl, m, sink=64, window=256, block_mask=bm, O=Od, LSE=Ld,
+                                 workspace=dws)
+
+    q.copy_(Q[:, S - 1])
+    g = capture(step)
+    for seed in (52, 53):
+        Qn, Kn = wl.xa_planted_qk(B, S, Hq, Hkv, 128, seed=seed)
+        Q.copy_(Qn.to(dev))
+        K.copy_(Kn.to(dev))
+        q.copy_(Q[:, S - 1])
+        sl.fill_(S - seed)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (bm, sc, O, LSE, Od, Ld)]
+        step()
+        torch.cuda.synchronize()
+        for a_, b_ in zip(got, (bm, sc, O, LSE, Od, Ld)):
+            assert torch.equal(a_, b_), seed
+    for ws in (xws, pws, dws):
+        check_no_device_error(ws)
