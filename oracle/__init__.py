@@ -62,7 +62,7 @@ def lib():
                                                 P, P, P]
         L.ea_oracle_xa_block_scores.argtypes = [P, P, P, P, i32, i32, i32, i32, f64, i32, i32,
                                                 i32, i32, P, P]
-        L.ea_oracle_xa_select.argtypes = [P, i64, f64, P]
+        L.ea_oracle_xa_select.argtypes = [P, i64, f64, P, P]
         for f in (L.ea_oracle_prefill_rows, L.ea_oracle_decode, L.ea_oracle_visited,
                   L.ea_oracle_route, L.ea_oracle_sparsity_ratios, L.ea_oracle_xa_block_scores,
                   L.ea_oracle_xa_select):
@@ -247,13 +247,18 @@ def xa_block_scores(Q, K, b, h, *, stride=16, T=128, scale=None, qb_rows=None):
     return W
 
 
-def xa_select(W, tau):
-    """XA threshold selection: uint8 [nB, nB] block mask from float64 scores [nB, nB]."""
+def xa_select(W, tau, qb_rows=None):
+    """XA threshold selection: uint8 [nB, nB] block mask from float64 scores [nB, nB]
+    (only the rows qb_rows when given; the others stay zero)."""
     W = np.ascontiguousarray(W, dtype=np.float64)
     nB = W.shape[0]
     assert W.shape == (nB, nB)
     mask = np.zeros((nB, nB), dtype=np.uint8)
-    rc = lib().ea_oracle_xa_select(_ptr(W), nB, float(tau), _ptr(mask))
+    sel = None
+    if qb_rows is not None:
+        sel = np.zeros(nB, dtype=np.uint8)
+        sel[np.asarray(qb_rows, dtype=np.int64)] = 1
+    rc = lib().ea_oracle_xa_select(_ptr(W), nB, float(tau), _ptr(sel), _ptr(mask))
     if rc != 0:
         raise ValueError("oracle xa_select rejected its arguments (rc=%d)" % rc)
     return mask

@@ -552,9 +552,12 @@ static int oracle_xa_cmp(const void *x, const void *y)
  * tau times the row's total.  If rounding leaves every run short of that, every
  * block with a positive score is kept.  The diagonal block is always kept (every
  * query attends to its own key).
- * W: [nB][nB]; mask receives [nB][nB] bytes (1 = keep), zero above the diagonal.
+ * W: [nB][nB]; mask receives [nB][nB] bytes (1 = keep), zero above the diagonal;
+ * when qb_sel (bytes [nB]) is given only the rows with qb_sel[qb] != 0 are
+ * selected (the others stay zero).
  */
-int ea_oracle_xa_select(const double *W, int64_t nB, double tau, uint8_t *mask)
+int ea_oracle_xa_select(const double *W, int64_t nB, double tau, const uint8_t *qb_sel,
+                        uint8_t *mask)
 {
     if (nB <= 0 || !(tau >= 0.0))
         return -1;
@@ -563,6 +566,8 @@ int ea_oracle_xa_select(const double *W, int64_t nB, double tau, uint8_t *mask)
         return -2;
     memset(mask, 0, (size_t)(nB * nB));
     for (int64_t qb = 0; qb < nB; ++qb) {
+        if (qb_sel && !qb_sel[qb])
+            continue;
         const double *row = W + qb * nB;
         uint8_t *out = mask + qb * nB;
         double total = 0.0;

@@ -154,3 +154,23 @@ def test_strided_query_cache_and_output(dev):
     Oref, _ = oracle.decode(q, Kc, Vc, seqlens, modes, sink=32, window=400)
     assert np.abs(Ob[:, 1:1 + Hq].float().cpu().numpy() - Oref).max() <= 1e-2
     assert (Ob[:, 0].float() == 5.0).all() and (Ob[:, 1 + Hq:].float() == 5.0).all()
+
+
+def test_block_decode_at_the_longest_cache(dev):
+    """Lmax = 2^21 keys (16384 mask blocks per row), a sparse decode row."""
+    cfg = wl.DecodeConfig("t", B=1, Hq=4, Hkv=1, d=128, L=1 << 21, sink=0, window=1)
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev, seqlens=[(1 << 21) - 77])
+    nB = cfg.L // 128
+    row = torch.rand(nB, generator=torch.Generator().manual_seed(3)) < 0.01
+    row[(int(sl[0]) - 1) // 128] = True
+    bm = torch.zeros(1, 1, nB, nB, dtype=torch.uint8)
+    bm[0, 0, (int(sl[0]) - 1) // 128] = row.to(torch.uint8)
+    m = torch.tensor([[BLOCK]], dtype=torch.uint8)
+    ws = ea.decode_workspace(1, 4, 1, cfg.L, device=dev)
+    O, LSE = ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m.to(dev), sink=0, window=1,
+                                      block_mask=bm.to(dev), workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Oref, Lref = oracle.decode(q.cpu(), Kc.cpu(), Vc.cpu(), sl.cpu(), m, sink=0, window=1,
+                               block_mask=bm)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "Lmax=2^21")

@@ -84,8 +84,9 @@ def check_masks(mask, sc, W, tau, rows, what):
     assert (np.triu(mask, 1) == 0).all(), what + ": kept blocks above the diagonal"
     assert (np.diagonal(mask)[rows] == 1).all(), what + ": diagonal not kept"
     # the selection rule, bit for bit, on the kernel's own scores
-    own = oracle.xa_select(np.tril(sc.astype(np.float64)), tau)
-    ref = oracle.xa_select(W, tau)
+    rows = list(rows)
+    own = oracle.xa_select(np.tril(sc.astype(np.float64)), tau, qb_rows=rows)
+    ref = oracle.xa_select(W, tau, qb_rows=rows)
     n_diff = 0
     for qb in rows:
         if not np.array_equal(mask[qb], own[qb]):
@@ -208,3 +209,21 @@ def test_xa_ssa_256k_sampled_rows(dev):
         W = oracle.xa_block_scores(Qc, Kc, 0, h, stride=16, qb_rows=rows)
         check_scores(sc[0, h], W, rows, "256K h=%d" % h)
         check_masks(bm[0, h], sc[0, h], W, 0.9, rows, "256K h=%d" % h)
+
+
+def test_maximum_sequence_sampled_rows(dev):
+    """S = 2^21 (the largest supported length), one KV head read by two query
+    heads: sampled query-block rows against the oracle, the row totals and the
+    diagonal on every row."""
+    S, Hq, Hkv = 1 << 21, 2, 1
+    Q, K = wl.xa_planted_qk(1, S, Hq, Hkv, 128, seed=23, device=dev)
+    m = np.array([[BLOCK]], dtype=np.uint8)
+    bm, sc, _ = run(dev, Q, K, m, max_units=1)
+    nB = S // 128
+    tot = np.tril(sc[0, 0]).sum(axis=1)
+    np.testing.assert_allclose(tot, 2 * 8, rtol=1e-3)
+    assert (np.diagonal(bm[0, 0]) == 1).all() and (np.triu(bm[0, 0], 1) == 0).all()
+    rows = [0, 5, nB - 1]
+    W = oracle.xa_block_scores(Q.cpu(), K.cpu(), 0, 0, stride=16, qb_rows=rows)
+    check_scores(sc[0, 0], W, rows, "S=2^21")
+    check_masks(bm[0, 0], sc[0, 0], W, 0.9, rows, "S=2^21")
