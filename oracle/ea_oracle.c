@@ -15,7 +15,7 @@
  *         (Chinese reading notes; the only page with eqs. 4-5 written out)
  *   [HA]  hyper.ai summary page "Elastic Attention" (arXiv 2601.17367)
  *
- * Conventions (readings of points the pages leave open, listed in the design doc):
+ * Conventions (readings of points the pages leave open):
  *   - scores are scale * <q, k> with scale given by the caller (1/sqrt(d));
  *   - every mode is causal (j <= i);
  *   - SSA (streaming sparse attention = attention sink + local window, [EN]
@@ -453,9 +453,8 @@ int ea_oracle_sparsity_ratios(const uint8_t *r, const uint8_t *m, int L, int Hkv
  * The pages name XA as XAttention, a training-free block-sparse attention that
  * picks key blocks by antidiagonal scoring ([EN] Glossary "XA"; [ZH] glossary
  * "XA"), with stride 16 and threshold 0.9 ([EN] §07 Table 8, "stride/threshold
- * 16/0.9"; [EN] §01 "XA, tau=0.9"), but do not write the scoring out.  This
- * follows the plainest reading of those words (listed with the other readings
- * in the design doc):
+ * 16/0.9"; [HA] experiments, "XA, tau=0.9"), but do not write the scoring out.
+ * This follows the plainest reading of those words:
  *   - the score matrix is cut into s x s cells (s = stride): cell (a, c) holds
  *     queries a*s .. a*s+s-1 and keys c*s .. c*s+s-1;
  *   - a cell's score is the mean of the scaled logits on its antidiagonal
