@@ -30,11 +30,11 @@
  *     that ran out) set an error word in the workspace, which
  *     ea_check_errors() reads back.
  *   - Every function returns an ea_status; no exception or abort crosses the ABI.
- *   - ea_route, ea_hybrid_attn_prefill, ea_hybrid_attn_prefill_varlen and
- *     ea_hybrid_attn_decode enqueue kernels only (no allocation, no host
- *     synchronisation): after one call on the device (which raises the
- *     kernels' shared-memory limits), a call can be captured into a CUDA
- *     graph and replayed with new contents in the same buffers.
+ *   - ea_route, ea_hybrid_attn_prefill, ea_hybrid_attn_prefill_varlen,
+ *     ea_hybrid_attn_decode and ea_xa_estimate enqueue kernels only (no
+ *     allocation, no host synchronisation): after one call on the device
+ *     (which raises the kernels' shared-memory limits), a call can be captured
+ *     into a CUDA graph and replayed with new contents in the same buffers.
  */
 #ifndef EA_H
 #define EA_H
