@@ -6,7 +6,7 @@
 // A decode step reads every kept cache entry once, so it is bound by HBM
 // bandwidth.  The design reads each (b, KV head)'s kept keys exactly once and
 // shares every K/V row among the query heads of the GQA group:
-//   decode_blocks_kernel (only when a block mask is given): one warp per
+//   decode_blocks_kernel (only when a block mask is given): one CTA per
 //     unit; for EA_BLOCK units the list of key blocks kept in the mask row of
 //     the query's block ((L - 1) / 128), ascending.
 //   decode_plan_kernel: per (b, KV head) unit the number of kept keys (FULL:
@@ -159,13 +159,16 @@ __device__ __forceinline__ int unit_work(const DecodeArgs &a, int u, bool &ok)
     return a.page_size ? paged_tiles(ks, TA, TB) * kDecKeys : ks.n;
 }
 
-// One warp per unit: the key blocks kept in the unit's decode row of the block
-// mask (row (L - 1) / 128, blocks 0 .. (L - 1) / 128), ascending.
-__global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
+// One CTA per unit: the key blocks kept in the unit's decode row of the block
+// mask (row (L - 1) / 128, blocks 0 .. (L - 1) / 128), ascending.  Each pass
+// covers 1024 blocks: thread t tests blocks 4t .. 4t + 3 (independent loads),
+// and a block-wide exclusive scan of the counts places them.
+constexpr int kBlkThreads = 256;
+
+__global__ void __launch_bounds__(kBlkThreads) decode_blocks_kernel(DecodeArgs a)
 {
-    const int u = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
-    if (u >= a.B * a.Hkv)
-        return;
+    __shared__ int warp_tot[kBlkThreads / 32];
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
     const int b = u / a.Hkv, h = u % a.Hkv;
     const int L = a.seqlens[b];
     int count = 0;
@@ -173,13 +176,11 @@ __global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
         const int qb = (L - 1) / EA_TILE;
         const uint8_t *row = a.block_mask + ((static_cast<int64_t>(b) * a.Hkv + h) * a.nBm + qb) * a.nBm;
         uint16_t *list = a.blk_list + static_cast<int64_t>(u) * a.nBm;
-        // 128 blocks per step: lane l tests blocks k0 + 4l .. k0 + 4l + 3 (four
-        // independent loads), then an exclusive scan of the lanes' counts
-        for (int k0 = 0; k0 <= qb; k0 += 128) {
+        for (int k0 = 0; k0 <= qb; k0 += 4 * kBlkThreads) {
             uint32_t bits = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const int kb = k0 + 4 * lane + j;
+                const int kb = k0 + 4 * tid + j;
                 bits |= (kb <= qb && row[kb] != 0) ? (1u << j) : 0u;
             }
             const int mine = __popc(bits);
@@ -190,15 +191,25 @@ __global__ void __launch_bounds__(256) decode_blocks_kernel(DecodeArgs a)
                 if (lane >= o)
                     incl += v;
             }
-            int pos = count + incl - mine;
+            if (lane == 31)
+                warp_tot[warp] = incl;
+            __syncthreads();
+            int before = 0, total = 0;
+#pragma unroll
+            for (int w = 0; w < kBlkThreads / 32; ++w) {
+                before += w < warp ? warp_tot[w] : 0;
+                total += warp_tot[w];
+            }
+            int pos = count + before + incl - mine;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 if ((bits >> j) & 1u)
-                    list[pos++] = static_cast<uint16_t>(k0 + 4 * lane + j);
-            count += __shfl_sync(0xffffffffu, incl, 31);
+                    list[pos++] = static_cast<uint16_t>(k0 + 4 * tid + j);
+            count += total;
+            __syncthreads();   // warp_tot is rewritten by the next pass
         }
     }
-    if (lane == 0)
+    if (tid == 0)
         a.blk_count[u] = count;
 }
 
@@ -643,43 +654,62 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 }
 
-// One CTA of 128 threads per (q head, b): log-sum-exp merge of the unit's
-// chunks.  Warp 0 computes the maximum and the weight sum of the partial LSEs
-// (lanes over chunks); then each thread (one head dimension) sums the
-// weighted partial outputs with eight loads in flight.
-__global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a)
+// One CTA per (q head, b): log-sum-exp merge of the unit's chunks.  Warp 0
+// computes the maximum and the weight sum of the partial LSEs in one online
+// pass (lanes over chunks, then a pairwise merge across lanes); then four
+// groups of 128 threads (one thread per head dimension) each sum the weighted
+// partial outputs of a quarter of the chunks with eight loads in flight, and
+// the four group sums are added in a fixed order.
+constexpr int kMergeGroups = 4;
+
+__global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM) decode_merge_kernel(const DecodeArgs a)
 {
     __shared__ float stat[2];
+    __shared__ float part[kMergeGroups][EA_HEAD_DIM];
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float LOG2E = 1.4426950408889634f;
-    const int qh = blockIdx.x, b = blockIdx.y, dd = threadIdx.x;
+    const int qh = blockIdx.x, b = blockIdx.y;
+    const int dd = threadIdx.x % EA_HEAD_DIM, grp = threadIdx.x / EA_HEAD_DIM;
     griddep_wait();   // the partials of the split kernel launched just before
     const int u = b * a.Hkv + qh / a.g, hh = qh % a.g;
     const int first = a.unit_first[u], ns = a.unit_splits[u];
     const int64_t base = static_cast<int64_t>(first) * a.g + hh;
-    if (dd < 32) {
-        float M = NEG_INF;
-        for (int s = dd; s < ns; s += 32)
-            M = fmaxf(M, a.part_lse[base + static_cast<int64_t>(s) * a.g]);
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float wsum = 0.f;
-        if (M > NEG_INF)
-            for (int s = dd; s < ns; s += 32)
-                wsum += ex2((a.part_lse[base + static_cast<int64_t>(s) * a.g] - M) * LOG2E);
-        for (int o = 16; o > 0; o >>= 1)
-            wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-        if (dd == 0) {
-            stat[0] = M;
-            stat[1] = wsum;
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        float m = NEG_INF, w = 0.f;      // running max and sum of exp(lse - m)
+        for (int s = lane; s < ns; s += 32) {
+            const float x = a.part_lse[base + static_cast<int64_t>(s) * a.g];
+            if (x == NEG_INF)
+                continue;
+            if (x > m) {
+                w = (m == NEG_INF ? 0.f : w * ex2((m - x) * LOG2E)) + 1.f;
+                m = x;
+            } else {
+                w += ex2((x - m) * LOG2E);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float w2 = __shfl_xor_sync(0xffffffffu, w, o);
+            const float M = fmaxf(m, m2);
+            w = (m == NEG_INF ? 0.f : w * ex2((m - M) * LOG2E)) +
+                (m2 == NEG_INF ? 0.f : w2 * ex2((m2 - M) * LOG2E));
+            m = M;
+        }
+        if (lane == 0) {
+            stat[0] = m;
+            stat[1] = w;
         }
     }
     __syncthreads();
     const float M = stat[0], wsum = stat[1];
     float osum = 0.f;
     if (M > NEG_INF) {
-        int s = 0;
-        for (; s + 8 <= ns; s += 8) {
+        const int per = (ns + kMergeGroups - 1) / kMergeGroups;
+        const int s0 = min(grp * per, ns), s1 = min(s0 + per, ns);
+        int s = s0;
+        for (; s + 8 <= s1; s += 8) {
             float l[8], o[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -690,14 +720,22 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const DecodeArgs a)
             for (int k = 0; k < 8; ++k)
                 osum += ex2((l[k] - M) * LOG2E) * o[k];
         }
-        for (; s < ns; ++s) {
+        for (; s < s1; ++s) {
             const int64_t pidx = base + static_cast<int64_t>(s) * a.g;
             osum += ex2((a.part_lse[pidx] - M) * LOG2E) * a.part_o[pidx * EA_HEAD_DIM + dd];
         }
     }
-    a.O[b * a.o_sb + qh * a.o_sh + dd] = __float2bfloat16_rn(wsum > 0.f ? osum / wsum : 0.f);
-    if (dd == 0 && a.LSE)
-        a.LSE[static_cast<int64_t>(b) * a.Hq + qh] = wsum > 0.f ? M + __logf(wsum) : NEG_INF;
+    part[grp][dd] = osum;
+    __syncthreads();
+    if (grp == 0) {
+        float o = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMergeGroups; ++k)
+            o += part[k][dd];
+        a.O[b * a.o_sb + qh * a.o_sh + dd] = __float2bfloat16_rn(wsum > 0.f ? o / wsum : 0.f);
+        if (dd == 0 && a.LSE)
+            a.LSE[static_cast<int64_t>(b) * a.Hq + qh] = wsum > 0.f ? M + __logf(wsum) : NEG_INF;
+    }
 }
 
 static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
@@ -739,7 +777,7 @@ static cudaError_t launch_merge(const DecodeArgs &a, int Hq, int B, cudaStream_t
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(Hq, B);
-    cfg.blockDim = dim3(EA_HEAD_DIM);
+    cfg.blockDim = dim3(kMergeGroups * EA_HEAD_DIM);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -847,10 +885,8 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     a.num_sms = sms;
     const int64_t max_chunks = static_cast<int64_t>(B) * Hkv * max_splits;
     const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
-    if (block_mask) {
-        const int64_t threads = static_cast<int64_t>(B) * Hkv * 32;
-        decode_blocks_kernel<<<static_cast<unsigned>(ceil_div(threads, 256)), 256, 0, st>>>(a);
-    }
+    if (block_mask)
+        decode_blocks_kernel<<<static_cast<unsigned>(static_cast<int64_t>(B) * Hkv), kBlkThreads, 0, st>>>(a);
     decode_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
     const cudaError_t e = launch_decode(tk, tv, a, grid, st);
     if (e != cudaSuccess)
