@@ -227,3 +227,17 @@ def test_maximum_sequence_sampled_rows(dev):
     W = oracle.xa_block_scores(Q.cpu(), K.cpu(), 0, 0, stride=16, qb_rows=rows)
     check_scores(sc[0, 0], W, rows, "S=2^21")
     check_masks(bm[0, 0], sc[0, 0], W, 0.9, rows, "S=2^21")
+
+
+@pytest.mark.parametrize("S", [16, 144, 400])
+def test_short_sequences(dev, S):
+    """S = 16 (one cell, one block), 144 (a last block of one cell), 400."""
+    Q, K = wl.xa_planted_qk(2, S, 4, 2, 128, seed=S)
+    m = np.array([[BLOCK, BLOCK], [SSA, BLOCK]], dtype=np.uint8)
+    bm, sc, _ = run(dev, Q, K, m)
+    W, _ = oracle_all(Q, K, m, 0.9)
+    nB = (S + 127) // 128
+    for b, h in ((0, 0), (0, 1), (1, 1)):
+        check_scores(sc[b, h], W[b, h], range(nB), "S=%d b=%d h=%d" % (S, b, h))
+        check_masks(bm[b, h], sc[b, h], W[b, h], 0.9, range(nB), "S=%d b=%d h=%d" % (S, b, h))
+    assert (bm[1, 0] == 0).all()
