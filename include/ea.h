@@ -495,9 +495,11 @@ ea_status ea_sparsity_ratios(const uint8_t *r, const uint8_t *m, int L, int Hkv,
 
 /*
  * ea_check_errors - synchronise `stream`, then read and clear the device error
- * word at the start of a prefill or decode workspace.  Returns EA_OK,
- * EA_ERR_DEVICE_CHECK, EA_ERR_TIMEOUT, or EA_ERR_CUDA.  This is the only
- * entry point that blocks the host.
+ * word at the start of a prefill, decode or XA workspace.  Returns EA_OK,
+ * EA_ERR_DEVICE_CHECK (an invalid device-side argument, or, in the
+ * bounds-checked build of the library, an index found out of range and not
+ * used), EA_ERR_TIMEOUT, or EA_ERR_CUDA.  This is the only entry point that
+ * blocks the host.
  */
 ea_status ea_check_errors(void *workspace, void *stream);
 

@@ -57,6 +57,16 @@ class _Policy(ctypes.Structure):
     _fields_ = [("fa_impl", ctypes.c_uint8), ("sa_impl", ctypes.c_uint8)]
 
 
+def use_library(path):
+    """Route every later call through the library at `path` (for example the
+    bounds-checked build, _lib/libea_checked.so); returns the previous path."""
+    global _lib, LIB_PATH
+    prev = LIB_PATH
+    LIB_PATH = path
+    _lib = None
+    return prev
+
+
 def lib():
     """The loaded C library (raises if it has not been built)."""
     global _lib

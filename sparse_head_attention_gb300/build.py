@@ -3,6 +3,11 @@
 Translation units are compiled in parallel, then linked into one shared library
 (CUDA runtime linked statically; the driver's tensor-map encoder is looked up at
 run time, so the library loads on a machine without a GPU driver).
+
+``build(checked=True)`` builds the bounds-checked variant ``_lib/libea_checked.so``
+(``-DEA_CHECKS``: every global access whose index depends on data or on the work
+decomposition is tested first and reported in the workspace error word instead
+of being made), which the tests run in place of a memory checker.
 """
 import concurrent.futures as cf
 import os
@@ -13,6 +18,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libea.so")
+CHECKED_LIB = os.path.join(OUT_DIR, "libea_checked.so")
 ROOT = os.path.dirname(HERE)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -28,8 +34,8 @@ def _deps():
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "ea.h")]
 
 
-def _compile(src, extra):
-    obj = os.path.join(OUT_DIR, os.path.basename(src) + ".o")
+def _compile(src, extra, obj_dir=OUT_DIR):
+    obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
     cmd = [NVCC] + ARCH + COMMON + extra + ["-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -37,28 +43,31 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra=None) -> str:
-    """Compile every source under csrc/ and link libea.so; returns its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=None, checked: bool = False) -> str:
+    """Compile every source under csrc/ and link libea.so (libea_checked.so with
+    checked=True); returns its path."""
+    lib = CHECKED_LIB if checked else LIB
+    obj_dir = os.path.join(OUT_DIR, "checked") if checked else OUT_DIR
+    os.makedirs(obj_dir, exist_ok=True)
     newest = max(os.path.getmtime(p) for p in _deps())
-    if not force and extra is None and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest:
-        return LIB
-    extra = list(extra or [])
+    if not force and extra is None and os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return lib
+    extra = list(extra or []) + (["-DEA_CHECKS"] if checked else [])
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
+        results = list(ex.map(lambda s: _compile(s, extra, obj_dir), srcs))
     if verbose:
         for (obj, err) in results:
             if err.strip():
                 print(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [NVCC] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

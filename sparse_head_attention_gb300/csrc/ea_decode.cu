@@ -181,7 +181,8 @@ __global__ void __launch_bounds__(kBlkThreads) decode_blocks_kernel(DecodeArgs a
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int kb = k0 + 4 * tid + j;
-                bits |= (kb <= qb && row[kb] != 0) ? (1u << j) : 0u;
+                bits |= (kb <= qb && in_bounds(kb, a.nBm, &a.hdr->error) && row[kb] != 0) ? (1u << j)
+                                                                                         : 0u;
             }
             const int mine = __popc(bits);
             int incl = mine;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kBlkThreads) decode_blocks_kernel(DecodeArgs a
             int pos = count + before + incl - mine;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                if ((bits >> j) & 1u)
+                if (((bits >> j) & 1u) && in_bounds(pos, a.nBm, &a.hdr->error))
                     list[pos++] = static_cast<uint16_t>(k0 + 4 * tid + j);
             count += total;
             __syncthreads();   // warp_tot is rewritten by the next pass
@@ -285,7 +286,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
         a.unit_first[u] = run;
         const int ns = a.unit_splits[u];
         for (int sp = 0; sp < ns; ++sp)
-            a.chunks[run + sp] = (u << kSplitBits) | sp;
+            if (in_bounds(static_cast<int64_t>(run) + sp,
+                          static_cast<int64_t>(units) * a.max_splits, &a.hdr->error))
+                a.chunks[run + sp] = (u << kSplitBits) | sp;
         run += ns;
     }
     if (tid == 0)
@@ -471,7 +474,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     if (t + lane < ci.n_tiles) {
                         int k0, nv;
                         tile_rows(a, ci, t + lane, k0, nv);
-                        my_page = a.block_table[ci.b * a.bt_stride + k0 / a.page_size];
+                        if (in_bounds(k0 / a.page_size, a.Lmax / a.page_size, &a.hdr->error))
+                            my_page = a.block_table[ci.b * a.bt_stride + k0 / a.page_size];
                     }
                 }
                 const int page = a.page_size ? __shfl_sync(0xffffffffu, my_page, t & 31) : 0;
@@ -644,6 +648,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                     osum += sm.red_o[w][hh][dd] * f;
                 }
             const int64_t pidx = static_cast<int64_t>(c) * a.g + hh;
+            if (!in_bounds(pidx, static_cast<int64_t>(a.B) * a.Hkv * a.max_splits * a.g,
+                           &a.hdr->error))
+                continue;
             a.part_o[pidx * EA_HEAD_DIM + dd] = lsum > 0.f ? osum / lsum : 0.f;
             if (dd == 0)
                 a.part_lse[pidx] = lsum > 0.f ? (M + __log2f(lsum)) * 0.69314718055994531f : NEG_INF;
@@ -672,7 +679,11 @@ __global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM) decode_merge_kerne
     const int dd = threadIdx.x % EA_HEAD_DIM, grp = threadIdx.x / EA_HEAD_DIM;
     griddep_wait();   // the partials of the split kernel launched just before
     const int u = b * a.Hkv + qh / a.g, hh = qh % a.g;
-    const int first = a.unit_first[u], ns = a.unit_splits[u];
+    const int first = a.unit_first[u];
+    int ns = a.unit_splits[u];
+    if (!in_bounds(static_cast<int64_t>(first) + ns - 1,
+                   static_cast<int64_t>(a.B) * a.Hkv * a.max_splits, &a.hdr->error))
+        ns = 0;
     const int64_t base = static_cast<int64_t>(first) * a.g + hh;
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;

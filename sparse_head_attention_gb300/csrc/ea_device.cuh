@@ -30,6 +30,23 @@ __device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bits)
         atomicOr(err, bits);
 }
 
+// Bounds-checked builds (compiled with -DEA_CHECKS): every global access whose
+// index depends on data or on the work decomposition is tested first; an index
+// outside [0, n) raises EA_DEVERR_BOUNDS in the workspace error word and the
+// access is skipped.  In the normal build the test is the constant true.
+#ifdef EA_CHECKS
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, uint32_t *err)
+{
+    if (i >= 0 && i < n)
+        return true;
+    if (err)
+        raise_error(err, EA_DEVERR_BOUNDS);
+    return false;
+}
+#else
+__device__ __forceinline__ bool in_bounds(int64_t, int64_t, uint32_t *) { return true; }
+#endif
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {

@@ -242,7 +242,7 @@ extern "C" ea_status ea_check_errors(void *workspace, void *stream)
         return EA_ERR_CUDA;
     if (word & EA_DEVERR_TIMEOUT)
         return EA_ERR_TIMEOUT;
-    if (word & EA_DEVERR_CHECK)
+    if (word & (EA_DEVERR_CHECK | EA_DEVERR_BOUNDS))
         return EA_ERR_DEVICE_CHECK;
     return EA_OK;
 }

@@ -14,6 +14,7 @@
 // Device error bits in the workspace error word.
 #define EA_DEVERR_CHECK 1u    // invalid mode / missing block mask / bad seqlen
 #define EA_DEVERR_TIMEOUT 2u  // a bounded wait ran out
+#define EA_DEVERR_BOUNDS 4u   // bounds-checked builds (-DEA_CHECKS): an index out of range
 
 // A bounded device wait gives up after this long (ns).
 #define EA_WAIT_TIMEOUT_NS 2000000000ull

@@ -84,6 +84,9 @@ struct PrefillArgs {
     int64_t o_sb, o_ss, o_sh;
     float *LSE;
     int64_t lse_sb, lse_sh;      // LSE[b * lse_sb + qh * lse_sh + token]
+    int64_t lse_elems;           // LSE elements (bounds-checked builds)
+    int64_t mask_elems;          // block-mask bytes, -1: mask_off[B] (bounds-checked builds)
+    int64_t visited_bits;        // bits of the visited bitmap (bounds-checked builds)
     int o_v8;                    // every O row starts 32-byte aligned: 256-bit stores
     const uint8_t *m;
     const uint8_t *block_mask;
@@ -112,6 +115,12 @@ struct RowInfo {
     int b, h, qb, tok0, S, nB, tma_b;
     int64_t mask_row;
 };
+
+// Block-mask bytes the kernels may read (bounds-checked builds).
+__device__ __forceinline__ int64_t mask_limit(const PrefillArgs &a)
+{
+    return a.mask_elems >= 0 ? a.mask_elems : a.mask_off[a.B];
+}
 
 // Fields of a variable-length row once b, h and qb are known.
 __device__ __forceinline__ void varlen_row_fields(const PrefillArgs &a, RowInfo &x)
@@ -177,7 +186,7 @@ __device__ __forceinline__ void decode_row(int row, const PrefillArgs &a, RowInf
         decode_row_dense(row, a, x);
         return;
     }
-    const int2 d = a.row_desc[row];
+    const int2 d = in_bounds(row, a.n_rows, &a.hdr->error) ? a.row_desc[row] : make_int2(0, 0);
     x.b = d.x;
     x.h = static_cast<int>(static_cast<uint32_t>(d.y) >> 16);
     x.qb = d.y & 0xFFFF;
@@ -250,7 +259,8 @@ __global__ void plan_costs_kernel(PrefillArgs a)
     } else if (mode == EA_BLOCK && a.block_mask) {
         const uint8_t *row = a.block_mask + x.mask_row;
         for (int kb = lane; kb <= qb; kb += 32)
-            n += row[kb] != 0;
+            if (in_bounds(x.mask_row + kb, mask_limit(a), &a.hdr->error))
+                n += row[kb] != 0;
         for (int o = 16; o > 0; o >>= 1)
             n += __shfl_xor_sync(0xffffffffu, n, o);
     } else {
@@ -331,7 +341,8 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
             if (valid) {
                 const int pos = start + __popc(peers & lt);
                 for (int p = 0; p < a.npairs; ++p)
-                    a.items[static_cast<uint64_t>(pos) * a.npairs + p] = r * a.npairs + p;
+                    if (in_bounds(static_cast<int64_t>(pos) * a.npairs + p, a.n_items, &a.hdr->error))
+                        a.items[static_cast<uint64_t>(pos) * a.npairs + p] = r * a.npairs + p;
             }
         }
     }
@@ -420,6 +431,8 @@ __device__ __forceinline__ int item_head(const ItemInfo &x, int t, const Prefill
 // order: each lane tests 16 mask bytes of a 512-byte window per refill.
 struct BlockScan {
     const uint8_t *row;
+    int64_t avail;  // mask bytes from row on (bounds-checked builds)
+    uint32_t *err;
     int limit;      // qb + 1
     int base;       // first key tile of the current window
     int cur_lane;
@@ -432,14 +445,16 @@ struct BlockScan {
         const int k0 = base + lane * 16;
 #pragma unroll
         for (int j = 0; j < 16; ++j)
-            if (k0 + j < limit && row[k0 + j] != 0)
+            if (k0 + j < limit && in_bounds(k0 + j, avail, err) && row[k0 + j] != 0)
                 mine |= 1u << j;
         cur_lane = 0;
         bits = __shfl_sync(0xffffffffu, mine, 0);
     }
-    __device__ void init(const uint8_t *r, int lim, int lane)
+    __device__ void init(const uint8_t *r, int64_t av, uint32_t *e, int lim, int lane)
     {
         row = r;
+        avail = av;
+        err = e;
         limit = lim;
         base = 0;
         refill(lane);
@@ -495,7 +510,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
         if (item < 0)
             break;
         const ItemInfo x = decode_item<kVarlen>(item, a);
-        const int N = a.costs[x.row];
+        const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
         if (N == 0)
             continue;
         const int mode = a.m[x.b * a.Hkv + x.h];
@@ -520,7 +535,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         BlockScan scan;
         if (mode == EA_BLOCK)
-            scan.init(a.block_mask + x.mask_row, x.qb + 1, lane);
+            scan.init(a.block_mask + x.mask_row, mask_limit(a) - x.mask_row, err, x.qb + 1, lane);
         for (int n = 0; n < N && ok; ++n) {
             const int kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
 #pragma unroll 1
@@ -540,7 +555,8 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
                     if (which == 0 && a.visited) {
                         const uint64_t bit =
                             (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(kb);
-                        atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
+                        if (in_bounds(static_cast<int64_t>(bit), a.visited_bits, err))
+                            atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
                     }
                 }
                 __syncwarp();
@@ -627,7 +643,7 @@ __device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, 
             mbar_arrive(&sm.item_empty[slot]);
         if (item < 0)
             break;
-        const int N = a.costs[item / a.npairs];
+        const int N = in_bounds(item / a.npairs, a.n_rows, err) ? a.costs[item / a.npairs] : 0;
         if (N == 0)
             continue;
         if (!mbar_wait(&sm.q_full, q_it & 1, &sm.abort, err))
@@ -714,14 +730,15 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         const ItemInfo x = decode_item<kVarlen>(item, a);
         bool store;
         const int qh = item_head(x, t, a, store);
-        const int N = a.costs[x.row];
+        const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
         const int mode = a.m[x.b * a.Hkv + x.h];
         int n_sink = 0, kb_lo = 0;
         if (mode == EA_SSA)
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         bool diag_kept = false;
         if (mode == EA_BLOCK && N > 0)
-            diag_kept = a.block_mask[x.mask_row + x.qb] != 0;
+            diag_kept = in_bounds(x.mask_row + x.qb, mask_limit(a), err) &&
+                        a.block_mask[x.mask_row + x.qb] != 0;
         const int i = x.qb * T + r;
         float m_run = NEG_INF, l_run = 0.f;
         bool ok = true;
@@ -849,7 +866,9 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         // none of them stays live across the tile loop
         RowInfo e;
         decode_row<kVarlen>(x.row, a, e);
-        const bool row_ok = store && i < e.S;
+        const bool row_ok = store && i < e.S &&
+                            in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
+                            in_bounds(qh, a.Hq, err);
         const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
         __nv_bfloat16 *orow =
             a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh;
@@ -914,7 +933,8 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                 bulk_commit_group();
             }
         }
-        if (row_ok && a.LSE)
+        if (row_ok && a.LSE &&
+            in_bounds(e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i, a.lse_elems, err))
             a.LSE[e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
                 l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
         tc_fence_before();
@@ -1041,6 +1061,9 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
     a.qb_end = qb_end;
     a.lse_sb = static_cast<int64_t>(Hq) * S;
     a.lse_sh = S;
+    a.lse_elems = static_cast<int64_t>(B) * Hq * S;
+    a.mask_elems = block_mask ? static_cast<int64_t>(B) * Hkv * nB * nB : 0;
+    a.visited_bits = static_cast<int64_t>(B) * Hkv * nB * nB;
     a.n_rows = static_cast<uint32_t>(n_rows);
     a.n_items = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * (qb_end - qb_begin) * npairs);
     return EA_OK;
@@ -1237,6 +1260,9 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.LSE = LSE;
     a.lse_sb = 0;
     a.lse_sh = total_tokens;
+    a.lse_elems = static_cast<int64_t>(Hq) * total_tokens;
+    a.mask_elems = block_mask ? -1 : 0;   // the masks' total is mask_off[B], known on the device
+    a.visited_bits = 0;
     a.visited = nullptr;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.cu_seqlens = cu_seqlens;

@@ -339,15 +339,18 @@ __device__ __forceinline__ void xa_softmax(const XaArgs &a, XaSmem &sm, uint32_t
                 gsum[gq] = sum;
                 tile_sum += sum;
             }
-            if (valid)
+            if (valid && in_bounds(slot_q * a.tri + xa_row_off(row) + kXBlocksPerTile * x.ct + 4 * q + 3,
+                                   static_cast<int64_t>(a.max_units) * a.g * a.tri, err))
                 dst[q] = make_float4(gsum[0], gsum[1], gsum[2], gsum[3]);
         }
         tc_fence_before();
         mbar_arrive(&sm.s_free[t]);
         if (valid) {
             const int64_t k = (slot_q * a.nA + row) * a.nct + x.ct;
-            a.rmax[k] = m_t;
-            a.tsum[k] = tile_sum;
+            if (in_bounds(k, static_cast<int64_t>(a.max_units) * a.g * a.nA * a.nct, err)) {
+                a.rmax[k] = m_t;
+                a.tsum[k] = tile_sum;
+            }
         }
     }
 }
@@ -493,8 +496,11 @@ __global__ void __launch_bounds__(kSelThreads) xa_select_kernel(XaArgs a)
 #pragma unroll
             for (int r = 0; r < kXCellsPerBlock; ++r) {
                 const bool in = a0 + r < a1;
-                ev[r] = in ? *reinterpret_cast<const float4 *>(e + roff[r])
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+                ev[r] = in && in_bounds(slot_q * a.tri + roff[r] + kb0 + 3,
+                                        static_cast<int64_t>(a.max_units) * a.g * a.tri,
+                                        &a.hdr->error)
+                            ? *reinterpret_cast<const float4 *>(e + roff[r])
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
                 mv[r] = in ? mxp[static_cast<int64_t>(r) * a.nct] : 0.f;
             }
 #pragma unroll
@@ -584,6 +590,8 @@ __global__ void __launch_bounds__(kSelThreads) xa_select_kernel(XaArgs a)
             else if (mode == 2)
                 keep = score > 0.f;
         }
+        if (!in_bounds(row_base + kb, static_cast<int64_t>(a.B) * a.Hkv * a.nB * a.nB, &a.hdr->error))
+            continue;
         a.block_mask[row_base + kb] = keep;
         if (a.block_scores)
             a.block_scores[row_base + kb] = score;

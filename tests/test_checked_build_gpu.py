@@ -1,0 +1,132 @@
+"""The bounds-checked build (libea_checked.so, compiled with -DEA_CHECKS) on odd
+sizes: every global access whose index depends on data or on the work
+decomposition is tested before it is made, and a failing test is reported in the
+workspace error word instead of touching memory.  Each case must leave the error
+word clear and still match the fp64 oracle.  This stands in for a memory checker,
+which this pool does not offer."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_head_attention_gb300 as ea
+from sparse_head_attention_gb300 import build as ea_build
+from sparse_head_attention_gb300 import workloads as wl
+from gpu_helpers import assert_close, check_no_device_error, gpu_device
+
+pytestmark = pytest.mark.gpu
+FULL, SSA, BLOCK = ea.FULL, ea.SSA, ea.BLOCK
+
+
+@pytest.fixture(scope="module")
+def dev():
+    d = gpu_device()
+    prev = ea.use_library(ea_build.build(checked=True))
+    yield d
+    ea.use_library(prev)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", [(3, 129, 6, 2), (1, 1000, 8, 2), (2, 300, 4, 4)])
+def test_prefill_odd_sizes(dev, B, S, Hq, Hkv):
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=S)
+    modes = np.array([[[FULL, SSA, BLOCK, SSA][(b + h) % 4] for h in range(Hkv)] for b in range(B)],
+                     np.uint8)
+    bm = wl.block_mask(B, Hkv, S, density=0.3, seed=S).numpy()
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    nB = (S + 127) // 128
+    vis = torch.zeros((B * Hkv * nB * nB + 31) // 32, dtype=torch.int32, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill(Q.to(dev), K.to(dev), V.to(dev), torch.as_tensor(modes).to(dev),
+                                       sink=16, window=100, block_mask=torch.as_tensor(bm).to(dev),
+                                       workspace=ws, visited_bitmap=vis)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Oref, Lref = oracle.prefill_full(Q, K, V, modes, sink=16, window=100, block_mask=bm)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "S=%d" % S)
+
+
+def test_varlen_prefill(dev):
+    lens = [129, 1, 700, 256]
+    Hq, Hkv = 8, 2
+    total = sum(lens)
+    Q = wl.randn_bf16((total, Hq, 128), seed=1)
+    K = wl.randn_bf16((total, Hkv, 128), seed=2)
+    V = wl.randn_bf16((total, Hkv, 128), seed=3)
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    m = torch.tensor([[FULL, SSA], [SSA, FULL], [FULL, FULL], [SSA, SSA]], dtype=torch.uint8)
+    ws = ea.prefill_varlen_workspace(len(lens), total, max(lens), Hq, Hkv, device=dev)
+    O, LSE = ea.ea_hybrid_attn_prefill_varlen(Q.to(dev), K.to(dev), V.to(dev), cu.to(dev), m.to(dev),
+                                              max_seqlen=max(lens), sink=16, window=64, workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    for b, L in enumerate(lens):
+        t0 = int(cu[b])
+        Oref, Lref = oracle.prefill_full(Q[None, t0:t0 + L], K[None, t0:t0 + L], V[None, t0:t0 + L],
+                                         m[b:b + 1], sink=16, window=64)
+        assert_close(O[t0:t0 + L].float().cpu().numpy()[None], LSE[:, t0:t0 + L].cpu().numpy()[None],
+                     Oref, Lref, "sequence %d" % b)
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_decode_all_modes(dev, paged):
+    cfg = wl.DecodeConfig("t", B=3, Hq=6, Hkv=2, d=128, L=1000, sink=16, window=200)
+    lens = [1000, 1, 513]
+    q, Kc, Vc, sl = wl.decode_inputs(cfg, seqlens=lens)
+    modes = np.array([[BLOCK, SSA], [FULL, BLOCK], [SSA, BLOCK]], np.uint8)
+    bm = wl.block_mask(3, 2, 1024, density=0.3, seed=9).numpy()      # 8 blocks: Lmax rounded to pages
+    ws = ea.decode_workspace(3, 6, 2, 1024, num_splits=0 if paged else 3, device=dev)
+    if paged:
+        Kp = torch.zeros(3 * 4 + 2, 256, 2, 128, dtype=torch.bfloat16)
+        Vp = torch.zeros_like(Kp)
+        table = torch.arange(12, dtype=torch.int32).view(3, 4) + 2
+        for b in range(3):
+            for p in range(4):
+                r0, r1 = p * 256, min((p + 1) * 256, 1000)
+                if r0 < r1:
+                    Kp[table[b, p], : r1 - r0] = Kc[b, r0:r1]
+                    Vp[table[b, p], : r1 - r0] = Vc[b, r0:r1]
+        O, LSE = ea.ea_hybrid_attn_decode_paged(q.to(dev), Kp.to(dev), Vp.to(dev), table.to(dev), sl.to(dev),
+                                                torch.as_tensor(modes).to(dev), sink=16, window=200,
+                                                block_mask=torch.as_tensor(bm).to(dev), workspace=ws)
+    else:
+        Kc2 = torch.zeros(3, 1024, 2, 128, dtype=torch.bfloat16)
+        Vc2 = torch.zeros_like(Kc2)
+        Kc2[:, :1000], Vc2[:, :1000] = Kc, Vc
+        O, LSE = ea.ea_hybrid_attn_decode(q.to(dev), Kc2.to(dev), Vc2.to(dev), sl.to(dev),
+                                          torch.as_tensor(modes).to(dev), sink=16, window=200,
+                                          block_mask=torch.as_tensor(bm).to(dev), num_splits=3,
+                                          workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Kc2 = torch.zeros(3, 1024, 2, 128, dtype=torch.bfloat16)
+    Vc2 = torch.zeros_like(Kc2)
+    Kc2[:, :1000], Vc2[:, :1000] = Kc, Vc
+    Oref, Lref = oracle.decode(q, Kc2, Vc2, sl, modes, sink=16, window=200, block_mask=bm)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "paged" if paged else "contiguous")
+
+
+def test_xa_estimation(dev):
+    B, S, Hq, Hkv = 2, 1200, 6, 2
+    Q, K = wl.xa_planted_qk(B, S, Hq, Hkv, 128, seed=5)
+    m = np.array([[BLOCK, SSA], [BLOCK, BLOCK]], np.uint8)
+    nB = (S + 127) // 128
+    ws = ea.xa_workspace(B, S, Hq, Hkv, 3, device=dev)
+    bm, sc = ea.ea_xa_estimate(Q.to(dev), K.to(dev), torch.as_tensor(m).to(dev), max_units=3,
+                               want_scores=True, workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    W, _ = oracle.xa_estimate(Q, K, m, stride=16, tau=0.9)
+    sc = sc.cpu().numpy()
+    for b, h in ((0, 0), (1, 0), (1, 1)):
+        tot = W[b, h].sum(axis=1, keepdims=True)
+        assert (np.abs(sc[b, h] - W[b, h]) <= 1e-3 * np.abs(W[b, h]) + 1e-6 * tot).all()
+        assert (np.diagonal(bm.cpu().numpy()[b, h]) == 1).all()
+
+
+def test_router(dev):
+    K = wl.randn_bf16((2, 700, 4, 128), seed=7)
+    Ws, bs = wl.router_weights(0)
+    r, m, logits = ea.ea_route(K.to(dev), [w.to(dev) for w in Ws], [x.to(dev) for x in bs])
+    torch.cuda.synchronize()
+    rr, mm, lg, _ = oracle.route(K, Ws, bs)
+    assert np.array_equal(r.cpu().numpy(), rr)
+    np.testing.assert_array_equal(logits.cpu().numpy(), lg)
