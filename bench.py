@@ -424,7 +424,8 @@ def run_ours(args, rank, world, dev):
         "router": router,
         "xa": xa,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    # the CPU baseline is reported by rank 0 of a single-GPU run only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, Q, K, V, m_cpu, bm_cpu, args)
     return line
 
