@@ -367,7 +367,14 @@ def run_ours(args, rank, world, dev):
             return statistics.median(per_step)
 
         n_e2e = max(5, min(args.steps, 10))
+        if world > 1:
+            torch.distributed.barrier()
         e_ms = time_steps(e2e_step, n_e2e)
+        if world > 1:
+            # whole-job figure: the slowest replica's step
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
         if ea.ea_check_errors(buf) != 0:
             raise RuntimeError("device error in the end-to-end prefill")
         dQ, dK, dV, dm = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V), torch.empty_like(m)
