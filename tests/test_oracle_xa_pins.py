@@ -152,3 +152,30 @@ def test_estimate_touches_block_heads_only():
     assert np.all(W[0, 0] == 0) and np.all(M[0, 0] == 0)
     assert np.all(np.diag(M[0, 1]) == 1)
     np.testing.assert_allclose(W[0, 1], oracle.xa_block_scores(Q, K, 0, 1, stride=16))
+
+
+def test_ragged_last_cell():
+    """S = 410 with stride 16: the last cell holds 10 tokens.  Zero queries give
+    the uniform closed form over ceil(S/16) = 26 cells; a pair inside the last
+    cell on its antidiagonal (query offset 2, key offset 13: both below S) moves
+    only that cell, by the closed form."""
+    S, s, T, d = 410, 16, 128, 128
+    Q = torch.zeros(1, S, 1, d, dtype=torch.bfloat16)
+    K = _bf16(1, S, 1, d, seed=12)
+    W = oracle.xa_block_scores(Q, K, 0, 0, stride=s, T=T)
+    np.testing.assert_allclose(W, _uniform_scores(S, s, T, 1), rtol=1e-13, atol=1e-13)
+    a0 = c0 = S // s                      # the partial cell, 25 (tokens 400 .. 409)
+    Q = torch.zeros(1, S, 1, d, dtype=torch.bfloat16)
+    K = torch.zeros(1, S, 1, d, dtype=torch.bfloat16)
+    Q[0, a0 * s + 2, 0, :] = 1.0          # its antidiagonal partner in cell 25 (token 413) does not exist
+    W = oracle.xa_block_scores(Q, K, 0, 0, stride=s, T=T)
+    np.testing.assert_allclose(W, _uniform_scores(S, s, T, 1), rtol=1e-13, atol=1e-13)
+    K[0, (c0 - 1) * s + 13, 0, :] = 1.0   # the partner one cell to the left (token 397)
+    W = oracle.xa_block_scores(Q, K, 0, 0, stride=s, T=T)
+    x = (1.0 / np.sqrt(d)) * d / s
+    ref = _uniform_scores(S, s, T, 1)
+    qb = a0 * s // T
+    for c in range(a0 + 1):
+        hit = c == c0 - 1
+        ref[qb, c * s // T] += (np.exp(x) if hit else 1.0) / (np.exp(x) + a0) - 1.0 / (a0 + 1)
+    np.testing.assert_allclose(W, ref, rtol=1e-13, atol=1e-13)
