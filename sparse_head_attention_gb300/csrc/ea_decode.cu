@@ -15,7 +15,7 @@
 //     chunk count (about 2048 keys each unless the caller fixes the count),
 //     and the list of chunks.  Short SSA units get few chunks, long FA units
 //     many, so no CTA is spent on a handful of keys.
-//   decode_split_kernel: persistent, one CTA per SM walking the chunk list.
+//   decode_split_kernel: persistent, one CTA per SM taking chunks from a queue.
 //     Each chunk's keys stream through a 6-stage shared-memory ring filled by
 //     TMA (64 keys x 256 B per K or V box); the group's query heads share each
 //     K/V row; fp32 online softmax per head.  Output: a partial (O / l, LSE)
@@ -79,7 +79,9 @@ struct __align__(1024) DecSmem {
     float red_l[kDecWarps][8];
     uint64_t full[kDecStages];
     uint64_t empty[kDecStages];
-    int abort;   // set by a timed-out wait; every warp then leaves without further barriers
+    uint64_t chunk_full[2], chunk_empty[2];
+    int chunk[2];  // chunk index handed from the producer to the compute warps (-1: none left)
+    int abort;     // set by a timed-out wait; every warp then leaves without further barriers
 };
 
 // Kept keys of one (b, KV head) unit as at most two contiguous ranges:
@@ -291,8 +293,10 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
                 a.chunks[run + sp] = (u << kSplitBits) | sp;
         run += ns;
     }
-    if (tid == 0)
+    if (tid == 0) {
         a.hdr->n_items = static_cast<uint32_t>(grand);
+        a.hdr->work_counter = 0;   // the split kernel's chunk queue
+    }
 }
 
 // Position of chunk c in the key stream.  Contiguous cache: visited keys
@@ -422,7 +426,8 @@ __device__ __forceinline__ uint32_t sw_off(int row, int cb)
     return (cb >> 3) * kDecHalfBytes + row * 128 + (((cb & 7) ^ (row & 7)) << 4);
 }
 
-// Persistent: CTA x handles chunks x, x + grid, x + 2 grid, ...
+// Persistent: each CTA takes chunks from a queue (an atomic counter that the
+// planner resets), so CTAs that drew short chunks take more of them.
 // Warp w (of 4) owns keys [16w, 16w + 16) of every 64-key tile; the query
 // heads of the GQA group are the rows of the MMA (padded to 16 with zeros):
 //   S (16 x 16 keys) = Q K^T : 2 key blocks x 8 head-dim steps
@@ -447,6 +452,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kDecWarps);
         }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.chunk_full[s], 1);
+            mbar_init(&sm.chunk_empty[s], kDecWarps);
+        }
         fence_barrier_init();
         fence_proxy_async_smem();
     }
@@ -465,7 +474,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         // Paged cache: lane j holds the page of the chunk's tile 32 * k + j,
         // looked up a group of 32 tiles ahead of the copies that need it.
         uint32_t issued = 0;
-        for (int c = blockIdx.x; c < total; c += gridDim.x) {
+        for (int it = 0;; ++it) {
+            // next chunk from the queue, handed to the compute warps in slot it % 2
+            const int slot = it & 1;
+            if (!mbar_wait(&sm.chunk_empty[slot], ((it >> 1) & 1) ^ 1, abort, &a.hdr->error))
+                return;
+            int c = -1;
+            if (lane == 0) {
+                const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
+                c = x < static_cast<uint32_t>(total) ? static_cast<int>(x) : -1;
+                sm.chunk[slot] = c;
+                mbar_arrive(&sm.chunk_full[slot]);
+            }
+            c = __shfl_sync(0xffffffffu, c, 0);
+            if (c < 0)
+                break;
             const ChunkInfo ci = chunk_info(a, c);
             int my_page = 0;
             for (int t = 0; t < ci.n_tiles; ++t) {
@@ -509,7 +532,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
     // ---------------------------------------------------------------- compute
     uint32_t consumed = 0;
-    for (int c = blockIdx.x; c < total; c += gridDim.x) {
+    for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!mbar_wait(&sm.chunk_full[slot], (it >> 1) & 1, abort, &a.hdr->error))
+            return;
+        const int c = sm.chunk[slot];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.chunk_empty[slot]);
+        if (c < 0)
+            break;
         const ChunkInfo ci = chunk_info(a, c);
         // Q as the A operand: rows r < g are query heads, the rest zero
         uint32_t qa[8][2];   // per head-dim step j: (r, 16j + 2q..), (r, 16j + 8 + 2q..)
