@@ -12,9 +12,10 @@
 //   decode_plan_kernel: per (b, KV head) unit the number of kept keys (FULL:
 //     [0, L); SSA: the sink [0, sink) and the window [L - window, L); BLOCK:
 //     the kept blocks' keys below L, walked as 64-key tiles), its
-//     chunk count (about 2048 keys each unless the caller fixes the count),
-//     and the list of chunks.  Short SSA units get few chunks, long FA units
-//     many, so no CTA is spent on a handful of keys.
+//     chunk count (chunks of 2048 to 8192 kept keys, sized so that the step
+//     has about four per SM, unless the caller fixes the count), and the list
+//     of chunks.  Short SSA units get few chunks, long FA units many, so no
+//     CTA is spent on a handful of keys.
 //   decode_split_kernel: persistent, one CTA per SM taking chunks from a queue.
 //     Each chunk's keys stream through a 6-stage shared-memory ring filled by
 //     TMA (64 keys x 256 B per K or V box); the group's query heads share each
