@@ -1,7 +1,6 @@
 """Multi-replica bookkeeping of bench.py on two gloo ranks (CPU): the timed
 region is the slowest rank's, the throughput counts every rank's work."""
 import os
-import socket
 
 import pytest
 import torch
@@ -9,16 +8,11 @@ import torch.distributed as dist
 import torch.multiprocessing as mp
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _worker(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+def _worker(rank, world, store_file, out):
+    # a file rendezvous: no port to race for with other processes on the machine
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", init_method="file://" + store_file, rank=rank,
+                            world_size=world)
     import bench
     local_ms = [12.0, 20.0][rank]
     ms, value = bench.job_throughput(local_ms, world, 3.0e12, 5, torch.device("cpu"))
@@ -27,11 +21,12 @@ def _worker(rank, world, port, out):
     dist.destroy_process_group()
 
 
-def test_two_rank_throughput_uses_max_time_and_all_work():
+def test_two_rank_throughput_uses_max_time_and_all_work(tmp_path):
     world = 2
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
-    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
+    store_file = str(tmp_path / "rendezvous")
+    mp.start_processes(_worker, args=(world, store_file, out), nprocs=world, join=True,
                        start_method="spawn")
     for rank in range(world):
         ms, value = out[rank]
