@@ -19,7 +19,10 @@ Parity status of each function (what pins it, see ``tests/test_oracle_pins.py``)
   decode         - pinned: equals the prefill oracle's last row (FA, SSA and BLOCK
                    with the same block mask); library SDPA.
   visited        - pinned: closed-form tile sets for FA/SSA, block mask for BLOCK.
-  route          - pinned: hand-computed integer examples (tests/golden).
+  route          - pinned: hand-computed examples (tests/golden), exact in binary:
+                   symmetric and square layers, plus non-square asymmetric layers
+                   with negative final logits, chosen so that a transposed weight
+                   read or an activation after the last layer changes the result.
   sparsity_ratios- pinned: hand-counted masks (tests/golden), closed form for SSA.
   xa_block_scores- pinned: stride 1 equals block sums of library softmax attention
                    probabilities; a single nonzero query/key pair lights exactly the

@@ -303,6 +303,54 @@ def test_router_hand_examples(case):
     np.testing.assert_array_equal(m2[0], np.where(np.array(case["r"]) == 1, SSA, BLOCK))
 
 
+def _mlp_variant(x, Ws, bs, transpose_layer=None, trailing_relu=False):
+    # dense layers on a pooled vector with one planted mistake: weights of one
+    # layer read as W[c][o] (the flat [out][in] array indexed the other way) or
+    # a ReLU after the last layer
+    for li, (W, b) in enumerate(zip(Ws, bs)):
+        nout, nin = W.shape
+        flat = W.reshape(-1)
+        y = []
+        for o in range(nout):
+            acc = float(b[o])
+            for c in range(nin):
+                w = flat[c * nout + o] if li == transpose_layer else flat[o * nin + c]
+                acc += float(w) * x[c]
+            y.append(acc)
+        if li + 1 < len(Ws) or trailing_relu:
+            y = [v if v > 0 else 0.0 for v in y]
+        x = y
+    return x
+
+
+@pytest.mark.parametrize("case", [c for c in _golden("router_hand_examples.json")["cases"]
+                                  if "_catches" in c], ids=lambda c: c["name"])
+def test_router_hand_examples_catch_planted_mistakes(case):
+    """The non-square, asymmetric cases are chosen so that each plausible slip
+    in the dense-layer evaluation changes the expected result: a ReLU after the
+    last layer (negative logits become 0 and the SA head ties, so r flips to FA),
+    the second layer's weights read transposed (r flips), the first layer's read
+    transposed (the logits change).  Evaluated here on the hand-pooled vectors,
+    so each mistake is shown to fail the oracle pin above."""
+    Ws = [np.array(w, np.float64) for w in case["W"]]
+    bs = [np.array(b, np.float64) for b in case["b"]]
+    want = np.array(case["logits"], np.float64)
+    r_want = np.array(case["r"])
+    flips = {"trailing": False, "t1": False, "t0": False}
+    for h, x in enumerate(case["pooled"]):
+        ok = _mlp_variant(list(map(float, x)), Ws, bs)
+        np.testing.assert_array_equal(ok, want[h])   # the hand working is self-consistent
+        for key, kw in (("trailing", dict(trailing_relu=True)), ("t1", dict(transpose_layer=1)),
+                        ("t0", dict(transpose_layer=0))):
+            z = _mlp_variant(list(map(float, x)), Ws, bs, **kw)
+            assert not np.array_equal(z, want[h]) or key == "t0"
+            flips[key] |= int(z[1] > z[0]) != r_want[h]
+    # across the heads: each planted mistake changes some logit, the first two flip a decision
+    assert flips["trailing"] and flips["t1"]
+    assert any(not np.array_equal(_mlp_variant(list(map(float, x)), Ws, bs, transpose_layer=0), want[h])
+               for h, x in enumerate(case["pooled"]))
+
+
 def test_router_pools_only_boundary_tokens():
     # changing a middle token leaves the decision inputs unchanged; changing a
     # boundary token moves the pooled mean by exactly delta / 200
