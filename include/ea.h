@@ -259,13 +259,18 @@ ea_status ea_hybrid_attn_prefill_varlen(const void *Q, const void *K, const void
  * workspace.  The planner's scratch lives in a fixed 4 MiB device array
  * inside the library (one per device that loads it, kept until the process
  * exits).  It holds the plan of any problem with
- * ea_prefill_workspace_size(B, S, Hq, Hkv, d) <= 4 MiB (for example B = 1,
- * 8 KV heads, 32 query heads, S up to 1M); larger problems return
- * EA_ERR_UNSUPPORTED without enqueueing anything.  Nothing is allocated.
+ * ea_prefill_workspace_size(B, S, Hq, Hkv, d) <= 4 MiB, i.e. about
+ * B * Hkv * ceil(S / 128) * (4 + 4 * ceil(Hq / Hkv / 2)) bytes: with 32 query
+ * heads over 8 KV heads, every length up to the 2^21 limit at B = 1 (1.6 MB),
+ * and up to about 349K (b, KV head, 128-query block) rows in all (B = 2 at
+ * S = 2^21 fits, B = 3 does not).  Larger problems, and every other invalid
+ * argument, return an error without enqueueing anything.  Nothing is
+ * allocated.
  *
  * The first call on a device looks up that array's device address (with the
- * device current) and caches it; make that first call before any stream
- * capture.  Every call reuses the same array and clears its header first, so
+ * device current) and caches it for the rest of the process; make that first
+ * call before any stream capture.  A device reset between calls leaves the
+ * cached address stale and is not supported.  Every call reuses the same array and clears its header first, so
  * calls whose executions overlap on the GPU (different streams, or different
  * host threads without ordering) race and must be serialised by the caller.
  * Device-side checks (invalid mode, missing block mask, a timed-out wait)

@@ -277,9 +277,10 @@ def ea_prefill_attend(Q, K, V, m, *, sink, window, workspace, **kw):
 def ea_hybrid_attn_prefill_noalloc(Q, K, V, m, *, sink, window, block_mask=None, scale=None,
                                    O=None, LSE=None, visited_bitmap=None, stream=None,
                                    want_lse=True):
-    """ea_hybrid_attn_prefill without a workspace: for callers that cannot
-    allocate device memory for the library (the planner's scratch is a fixed
-    4 MiB array inside it; see include/ea.h).  Returns (O, LSE)."""
+    """ea_hybrid_attn_prefill without a workspace, for callers that cannot
+    allocate device memory for the library: the planner's scratch is a fixed
+    4 MiB array inside it, shared by every call (calls that overlap on the GPU
+    race).  Returns (O, LSE)."""
     _dev(Q, "Q", torch.bfloat16)
     _dev(K, "K", torch.bfloat16)
     _dev(V, "V", torch.bfloat16)
@@ -294,6 +295,10 @@ def ea_hybrid_attn_prefill_noalloc(Q, K, V, m, *, sink, window, block_mask=None,
         O = torch.empty_like(Q)
     if LSE is None and want_lse:
         LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=Q.device)
+    if block_mask is not None:
+        _dev(block_mask, "block_mask", torch.uint8)
+        if not block_mask.is_contiguous():
+            raise ValueError("block_mask must be contiguous")
     st = lib().ea_hybrid_attn_prefill_noalloc(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _strides(Q), _strides(K), _strides(O),
         B, S, Hq, Hkv, d, float(scale), _ptr(m), int(sink), int(window), _ptr(block_mask), TILE,

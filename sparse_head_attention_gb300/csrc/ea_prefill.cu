@@ -1306,16 +1306,15 @@ extern "C" ea_status ea_prefill_attend(const void *Q, const void *K, const void 
                                 visited_bitmap, 0, -1, stream);
 }
 
-extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, void *O,
-                                            float *LSE, const int64_t q_str[4],
-                                            const int64_t kv_str[4], const int64_t o_str[4], int B,
-                                            int S, int Hq, int Hkv, int d, float scale,
-                                            const uint8_t *m, int sink, int window,
-                                            const uint8_t *block_mask, int block_size,
-                                            void *workspace, size_t ws_bytes,
-                                            uint32_t *visited_bitmap, void *stream)
+// Every host-side check of a fixed-length prefill call (tensors included),
+// so that a rejected call enqueues nothing.
+static ea_status prefill_validate(const void *Q, const void *K, const void *V, void *O,
+                                  const int64_t q_str[4], const int64_t kv_str[4],
+                                  const int64_t o_str[4], int B, int S, int Hq, int Hkv, int d,
+                                  float scale, const uint8_t *m, int sink, int window,
+                                  const uint8_t *block_mask, int block_size, void *workspace,
+                                  size_t ws_bytes)
 {
-    // Validate everything (tensors included) before enqueueing the planner.
     if (!Q || !K || !V || !O || !q_str || !kv_str || !o_str || !(scale > 0.f))
         return EA_ERR_INVALID_ARG;
     PrefillArgs a;
@@ -1331,6 +1330,23 @@ extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const 
             return EA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
         return EA_ERR_INVALID_ARG;
+    return EA_OK;
+}
+
+extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const void *V, void *O,
+                                            float *LSE, const int64_t q_str[4],
+                                            const int64_t kv_str[4], const int64_t o_str[4], int B,
+                                            int S, int Hq, int Hkv, int d, float scale,
+                                            const uint8_t *m, int sink, int window,
+                                            const uint8_t *block_mask, int block_size,
+                                            void *workspace, size_t ws_bytes,
+                                            uint32_t *visited_bitmap, void *stream)
+{
+    // Validate everything (tensors included) before enqueueing the planner.
+    ea_status s = prefill_validate(Q, K, V, O, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale, m,
+                                   sink, window, block_mask, block_size, workspace, ws_bytes);
+    if (s != EA_OK)
+        return s;
     s = ea_prefill_plan(B, S, Hq, Hkv, d, m, sink, window, block_mask, block_size, workspace,
                         ws_bytes, stream);
     if (s != EA_OK)
@@ -1353,8 +1369,9 @@ extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const 
 
 static __device__ __align__(256) uint8_t g_noalloc_prefill_scratch[EA_NOALLOC_PREFILL_SCRATCH_BYTES];
 
-// Device address of the array, resolved once per device (host code only sees a
-// host-side stand-in under that name).
+// Device address of the array, resolved once per process and device (host
+// code only sees a host-side stand-in under that name).  A device reset
+// (cudaDeviceReset) between calls would leave it stale and is not supported.
 static void *g_noalloc_scratch_ptr[64] = {};
 static std::mutex g_noalloc_mutex;
 
@@ -1386,6 +1403,12 @@ extern "C" ea_status ea_hybrid_attn_prefill_noalloc(const void *Q, const void *K
         }
         scratch = g_noalloc_scratch_ptr[dev];
     }
+    // Every argument check first, so that a rejected call enqueues nothing.
+    const ea_status s = prefill_validate(Q, K, V, O, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale,
+                                         m, sink, window, block_mask, block_size, scratch,
+                                         EA_NOALLOC_PREFILL_SCRATCH_BYTES);
+    if (s != EA_OK)
+        return s;
     // The array keeps the previous call's contents: clear the header (error
     // word and queue counters) before planning.
     if (cudaMemsetAsync(scratch, 0, sizeof(ea_ws_header), static_cast<cudaStream_t>(stream)) !=

@@ -7,9 +7,15 @@ import oracle
 import sparse_head_attention_gb300 as ea
 from sparse_head_attention_gb300 import build as ea_build
 
-# Tolerances: bf16 output max abs error 1e-2, LSE abs error 1e-3 (fp32 vs fp64).
+# Tolerances (the benchmark configuration's figures): bf16 output max abs error
+# 1e-2, LSE abs error 1e-3 (fp32 vs fp64).
 O_TOL = 1e-2
 LSE_TOL = 1e-3
+
+# Every assert_close call records (what, elements above a flat O_TOL, elements
+# compared, max |O - oracle|); tests/conftest.py prints the non-zero counts at
+# the end of the run.
+FLAT_EXCESS = []
 
 
 def bf16_half_ulp(x):
@@ -29,13 +35,21 @@ def gpu_device():
     return torch.device("cuda:0")
 
 
-def assert_close(O, LSE, Oref, Lref, what=""):
+def assert_close(O, LSE, Oref, Lref, what="", flat=False):
     """O: bf16/float array vs float64 reference; LSE: -inf must match -inf.
 
-    O is stored in bf16, whose own rounding alone reaches 1e-2 once |O| > 2.5
-    (a step of 2^-6 on [2, 4)), so each element may differ from the reference
-    by O_TOL plus half a bf16 step at the reference's magnitude; below
-    |O| = 2 that adds at most 0.0039."""
+    The output is bf16, and the correctly rounded bf16 value of O is only
+    within half a bf16 step of O: half a step is 2^-8 = 0.0039 on [1, 2),
+    2^-7 = 0.0078 on [2, 4) and 2^-6 = 0.0156 on [4, 8).  From |O| = 4 on, exact
+    arithmetic followed by correct rounding can therefore miss a flat 1e-2.
+    Below 4 a flat 1e-2 is attainable, but the kernels' own arithmetic error
+    (the bf16 probabilities of the P V product, about 2^-9 relative each) can
+    add a few thousandths on rows that keep only a few keys, enough to cross
+    1e-2 on [2, 4).  The bound checked by default is therefore 1e-2 plus half a
+    bf16 step at the oracle's magnitude (a stated departure from a flat 1e-2);
+    every call also counts the elements above a flat 1e-2, records the count in
+    FLAT_EXCESS and prints it, and with flat=True (the benchmark workloads) that
+    count must be zero."""
     O = np.asarray(O, dtype=np.float64)
     LSE = np.asarray(LSE, dtype=np.float64)
     assert O.shape == Oref.shape, (O.shape, Oref.shape)
@@ -43,11 +57,17 @@ def assert_close(O, LSE, Oref, Lref, what=""):
     diff = np.abs(O - Oref)
     err_o = diff.max() if O.size else 0.0
     excess = (diff - (O_TOL + bf16_half_ulp(Oref))).max() if O.size else -1.0
+    n_flat = int(np.count_nonzero(diff > O_TOL))
+    FLAT_EXCESS.append((what, n_flat, int(O.size), float(err_o)))
+    print("%s: %d of %d elements above a flat 1e-2 (max |O - oracle| %.5f)" % (
+        what, n_flat, O.size, err_o))
     ninf = np.isneginf(Lref)
     assert (np.isneginf(LSE) == ninf).all(), what + ": -inf LSE pattern differs"
     err_l = np.abs(LSE[~ninf] - Lref[~ninf]).max() if (~ninf).any() else 0.0
     assert excess <= 0.0, "%s: max |O - oracle| = %g exceeds 1e-2 + half a bf16 step by %g" % (
         what, err_o, excess)
+    if flat:
+        assert n_flat == 0, "%s: %d elements above a flat 1e-2 (max %g)" % (what, n_flat, err_o)
     assert err_l <= LSE_TOL, "%s: max |LSE - oracle| = %g" % (what, err_l)
     return err_o, err_l
 

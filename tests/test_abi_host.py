@@ -56,6 +56,12 @@ def test_workspace_sizes(L):
     assert L.ea_decode_workspace_size(32, 32, 8, 128, 131072, 2000) == 0
     # bigger problems never need less
     assert L.ea_prefill_workspace_size(1, 32768, 32, 8, 128) > L.ea_prefill_workspace_size(1, 1024, 32, 8, 128)
+    # the allocation-free prefill's fixed 4 MiB plan array: every length up to
+    # 2^21 fits at B = 1 with 32 query heads over 8 KV heads, and B = 2 still
+    # does; B = 3 is rejected
+    assert L.ea_prefill_workspace_size(1, 1 << 21, 32, 8, 128) == 1573120
+    assert L.ea_prefill_workspace_size(2, 1 << 21, 32, 8, 128) <= 4 << 20
+    assert L.ea_prefill_workspace_size(3, 1 << 21, 32, 8, 128) > 4 << 20
 
 
 def _fake(n=0x1000):

@@ -130,7 +130,7 @@ def test_full_workload_sampled_sequences(dev):
         Oref, Lref = oracle.decode(q[b:b + 1].cpu(), Kc[b:b + 1].cpu(), Vc[b:b + 1].cpu(),
                                    sl[b:b + 1].cpu(), m[b:b + 1], sink=cfg.sink, window=cfg.window)
         assert_close(O[b:b + 1].float().cpu().numpy(), LSE[b:b + 1].cpu().numpy(), Oref, Lref,
-                     "b=%d" % b)
+                     "b=%d" % b, flat=True)
 
 
 def test_strided_query_cache_and_output(dev):
