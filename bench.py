@@ -21,6 +21,11 @@ GB/s of the kept KV-cache bytes reported beside it.
             step / step time.
   roofline  the attention kernel alone (CUDA events around its launch):
             visited-tile flops / its duration against the measured bf16 peak.
+  xa256k_seeded_mask, routed64k_36_layers
+            the other two prefill workloads, each with its own clock record:
+            the 256K XA-SSA layer (2 BLOCK heads on the seeded density-0.2
+            block mask, 6 SSA heads at 128/4096) and the Qwen3-8B-shaped
+            36-layer 64K stack whose modes come from the router pre-pass.
 
 --impl reference runs the fp64 CPU oracle (the only independent implementation
 of this method here) on a bounded row sample of the same workload.
@@ -405,6 +410,15 @@ def run_ours(args, rank, world, dev):
     if not args.no_xa:
         xa = run_xa(args, dev, peaks, flush)
 
+    # ---- the other two prefill workloads: the 256K XA-SSA layer on the seeded
+    # block mask, and the 36-layer router-driven 64K stack
+    xa256k = None
+    if not args.no_xa256k and cfg.name != get_cfg("xa256k").name:
+        xa256k = run_seeded_layer(args, dev, peaks, flush, "xa256k")
+    routed = None
+    if not args.no_routed:
+        routed = run_routed_layers(args, dev, peaks, flush)
+
     # ---- sparsity ratios of the timed layer (host)
     msr, esr = ea.ea_sparsity_ratios(
         (m_cpu.numpy() == cfg.sa_impl).astype(np.uint8), m_cpu.numpy(), cfg.S, sink=cfg.sink,
@@ -430,6 +444,8 @@ def run_ours(args, rank, world, dev):
         "varlen": varlen,
         "router": router,
         "xa": xa,
+        "xa256k_seeded_mask": xa256k,
+        "routed64k_36_layers": routed,
     }
     # the CPU baseline is reported by rank 0 of a single-GPU run only
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -856,16 +872,20 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ 36-layer routed workload
-def run_routed_layers(args, dev):
+def run_routed_layers(args, dev, peaks=None, flush=None):
     """Qwen3-8B-shaped attention stack: 36 layers, S=65536, 32/8 heads, SSA
     128/2048.  One step = for every layer: the router pre-pass on that layer's K
     (pool -> 128-64-2 MLP -> argmax -> mode), the planner and the fused prefill
     driven by those modes.  The output bias beta of the router is set once,
     before timing, by bisection on the device so that the model-level share of
-    SA heads is 0.75 (the pages report 0.63-0.85 at test time)."""
+    SA heads is 0.75 (the pages report 0.63-0.85 at test time).  Every layer has
+    its own resident Q/K/V (36 x 768 MB); L2 is flushed before every timed
+    step.  The attention kernels are also timed alone (CUDA events around each
+    layer's launch) for the roofline fraction."""
     import sparse_head_attention_gb300 as ea
     from sparse_head_attention_gb300 import workloads as wl
     cfg = wl.QWEN_64K_36L
+    peaks = peaks or measured_peaks()
     L = cfg.layers if args.layers is None else args.layers
     layers = []
     for l in range(L):
@@ -897,14 +917,21 @@ def run_routed_layers(args, dev):
     m_buf = [torch.empty(cfg.B, cfg.Hkv, dtype=torch.uint8, device=dev) for _ in range(L)]
     stream = torch.cuda.current_stream()
 
-    def step():
+    def step(kev=None):
         for l in range(L):
             W, b = weights[l]
             ea.ea_route(layers[l], W, b, r_out=r_buf[l], m_out=m_buf[l])
-            ea.ea_hybrid_attn_prefill(Qs[l], layers[l], Vs[l], m_buf[l], sink=cfg.sink,
-                                      window=cfg.window, O=O, LSE=LSE, workspace=ws)
+            ea.ea_prefill_plan(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, m_buf[l], sink=cfg.sink,
+                               window=cfg.window, workspace=ws)
+            if kev is not None:
+                kev[l][0].record(stream)
+            ea.ea_prefill_attend(Qs[l], layers[l], Vs[l], m_buf[l], sink=cfg.sink, window=cfg.window,
+                                 O=O, LSE=LSE, workspace=ws)
+            if kev is not None:
+                kev[l][1].record(stream)
 
-    step()
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
     torch.cuda.synchronize()
     if ea.ea_check_errors(ws) != 0:
         raise RuntimeError("device error in the routed workload")
@@ -916,23 +943,117 @@ def run_routed_layers(args, dev):
         useful += u
         tile += t
     msr, esr = ea.ea_sparsity_ratios(r_all, m_all, cfg.S, sink=cfg.sink, window=cfg.window)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    ts = []
-    for _ in range(max(1, args.steps // 10)):
+    ranges = [(a, min(a + 12, L)) for a in range(0, L, 12)]
+    msr_ranges = {"layers %d-%d" % (a, b - 1): ea.ea_sparsity_ratios(r_all[a:b], m_all[a:b], cfg.S,
+                                                                    sink=cfg.sink, window=cfg.window)[0]
+                  for a, b in ranges}
+    if flush is None:
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    n_steps = max(3, min(args.steps // 6, 5))
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    ts, kts = [], []
+    for _ in range(n_steps):
         flush.zero_()
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
         a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        step()
+        step(kev)
         e.record(stream)
         torch.cuda.synchronize()
         ts.append(a.elapsed_time(e))
+        kts.append(sum(x.elapsed_time(y) for x, y in kev))
+    clk = clocks.stop()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in the routed workload")
     ms = statistics.median(ts)
+    kms = statistics.median(kts)
+    del Qs, Vs, layers, O, LSE
     return {"workload": cfg.name, "layers": L, "ms_per_step": round(ms, 3),
+            "steps_timed": n_steps, "estimator": "median of %d steps" % n_steps,
             "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 1),
             "visited_tile_tflops": round(tile / (ms * 1e-3) / 1e12, 1),
-            "omega_msr": msr, "omega_esr": round(esr, 4), "router_output_bias_beta": beta,
-            "step": "per layer: ea_route -> ea_hybrid_attn_prefill (planner + fused kernel)",
-            "gpu_launches_per_step": 4 * L}
+            "frac_of_bf16_peak": round(tile / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "kernels_ms_per_step": round(kms, 3),
+            "kernels_visited_tile_tflops": round(tile / (kms * 1e-3) / 1e12, 1),
+            "kernels_frac_of_bf16_peak": round(tile / (kms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "useful_flops_per_step": useful, "visited_tile_flops_per_step": tile,
+            "omega_msr": msr, "omega_msr_by_layers": msr_ranges, "omega_esr": round(esr, 4),
+            "router_output_bias_beta": beta,
+            "step": "per layer: ea_route -> ea_prefill_plan -> ea_prefill_attend (fused kernel)",
+            "gpu_launches_per_step": 4 * L,
+            "l2": "flushed before every timed step (256 MB memset, outside the events)",
+            "clocks": clk}
+
+
+def run_seeded_layer(args, dev, peaks, flush, name):
+    """One prefill layer of another benchmark workload (planner + fused kernel
+    per step, inputs resident, L2 flushed before every timed step), with its own
+    clock record: the 256K XA-SSA layer on the seeded density-0.2 block mask."""
+    import sparse_head_attention_gb300 as ea
+    cfg = get_cfg(name)
+    Q, K, V, m_cpu, bm_cpu = make_prefill_inputs(cfg, dev)
+    m = m_cpu.to(dev)
+    bm = None if bm_cpu is None else bm_cpu.to(dev)
+    useful, tile = prefill_work(cfg, m_cpu.numpy(), None if bm_cpu is None else bm_cpu.numpy())
+    O = torch.empty_like(Q)
+    LSE = torch.empty(cfg.B, cfg.Hq, cfg.S, dtype=torch.float32, device=dev)
+    ws = ea.prefill_workspace(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        ea.ea_prefill_plan(cfg.B, cfg.S, cfg.Hq, cfg.Hkv, m, sink=cfg.sink, window=cfg.window,
+                           block_mask=bm, workspace=ws)
+        if ev is not None:
+            ev[0].record(stream)
+        ea.ea_prefill_attend(Q, K, V, m, sink=cfg.sink, window=cfg.window, block_mask=bm,
+                             O=O, LSE=LSE, workspace=ws)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    n = max(5, min(args.steps, 10))
+    clocks = ClockSampler(dev.index or 0)
+    clocks.start()
+    evs = []
+    for _ in range(n):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        k = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        a.record(stream)
+        step(k)
+        b.record(stream)
+        evs.append((a, b, k))
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if ea.ea_check_errors(ws) != 0:
+        raise RuntimeError("device error in the %s layer" % name)
+    ms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    kms = statistics.mean(k[0].elapsed_time(k[1]) for _, _, k in evs)
+    msr, esr = ea.ea_sparsity_ratios(
+        (m_cpu.numpy() == cfg.sa_impl).astype(np.uint8), m_cpu.numpy(), cfg.S, sink=cfg.sink,
+        window=cfg.window, block_masks=None if bm_cpu is None else [bm_cpu.numpy()[0]])
+    dens = None
+    if bm_cpu is not None:
+        nB = (cfg.S + 127) // 128
+        dens = [round(float(np.tril(bm_cpu[0, h].numpy()).sum()) / (nB * (nB + 1) / 2), 4)
+                for h in range(cfg.Hkv) if int(m_cpu[0, h]) == BLOCK_MODE]
+    del Q, K, V, O, LSE
+    return {"workload": cfg.name, "B": cfg.B, "seq_len": cfg.S, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+            "sink": cfg.sink, "window": cfg.window, "block_density_seeded": cfg.block_density,
+            "block_density_kept": dens, "steps_timed": n,
+            "ms_per_step": round(ms, 4), "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 1),
+            "kernel_ms": round(kms, 4),
+            "visited_tile_tflops": round(tile / (kms * 1e-3) / 1e12, 1),
+            "frac_of_bf16_peak": round(tile / (kms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "useful_flops_per_step": useful, "visited_tile_flops_per_step": tile,
+            "omega_msr": msr, "omega_esr": round(esr, 6),
+            "step": "ea_prefill_plan + ea_prefill_attend (2 launches)",
+            "l2": "flushed before every timed step (256 MB memset, outside the events)",
+            "clocks": clk}
 
 
 # ------------------------------------------------------------------ Algorithm 1(a) comparison
@@ -1031,6 +1152,9 @@ def main():
     ap.add_argument("--routed-layers", action="store_true",
                     help="time the 36-layer router-driven 64K workload instead of the benchmark")
     ap.add_argument("--layers", type=int, default=None, help="layers of --routed-layers (default 36)")
+    ap.add_argument("--no-routed", action="store_true", help="skip the 36-layer routed 64K line")
+    ap.add_argument("--no-xa256k", action="store_true",
+                    help="skip the 256K XA-SSA layer on the seeded block mask")
     ap.add_argument("--serial-sweep", action="store_true",
                     help="fused single launch vs Serial Dispatch (Algorithm 1(a)) sweep instead of the benchmark")
     ap.add_argument("--serial-lengths", type=int, nargs="+", default=[16384, 32768, 65536, 131072])
@@ -1059,7 +1183,7 @@ def main():
     ea_build.build()
     if args.routed_layers:
         if rank == 0:
-            print(json.dumps(run_routed_layers(args, dev)), flush=True)
+            print(json.dumps(run_routed_layers(args, dev, measured_peaks())), flush=True)
         return 0
     if args.serial_sweep:
         if rank == 0:

@@ -31,7 +31,8 @@ def sources():
 
 
 def _deps():
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "ea.h")]
+    inc = os.path.join(ROOT, "include")
+    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(inc, f) for f in os.listdir(inc)]
 
 
 def _compile(src, extra, obj_dir=OUT_DIR):

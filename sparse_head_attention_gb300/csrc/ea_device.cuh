@@ -376,6 +376,159 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// A cluster of two CTAs on two SMs that share one 2-SM tensor-core
+// instruction (tcgen05 with cta_group::2).  Rank 0 issues the MMAs; the
+// operands and accumulators are split between the two CTAs' shared and tensor
+// memories.  Every tcgen05 instruction of a kernel that uses pairs must carry
+// cta_group::2.
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of the location at shared::cta address `saddr` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive (once, release at cluster scope) on an mbarrier given by its
+// shared::cluster address (this CTA's or the peer's): for a hand-off of data
+// written to the other CTA's shared memory before the arrival.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+                 : "memory");
+}
+
+// Arrive (once, release at CTA scope) on an mbarrier given by its
+// shared::cluster address: a signal that carries no generic-memory data (the
+// tcgen05 operations it orders are ordered by tcgen05 fences around it).  The
+// cluster-scope release costs a memory barrier per arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cl_addr)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cl_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+// Store a 32-bit word into a shared::cluster address (the peer CTA's smem).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
+}
+
+// Set bits of a word in a shared::cluster address (relaxed, cluster scope).
+__device__ __forceinline__ void red_or_cluster(uint32_t cl_addr, uint32_t v)
+{
+    asm volatile("red.relaxed.cluster.shared::cluster.or.b32 [%0], %1;" ::"r"(cl_addr), "r"(v)
+                 : "memory");
+}
+
+// All threads of both CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named barrier among `count` threads (id 1..15; 0 is __syncthreads), and its
+// non-waiting arrival.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Tiled TMA load into this CTA's shared memory whose completion (bytes) is
+// reported to an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_4d_pair(void *smem_dst, const void *tmap, int c0, int c1,
+                                                 int c2, int c3, uint32_t bar_cl)
+{
+    asm volatile("cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+                 "r"(bar_cl)
+                 : "memory");
+}
+
+// TMEM allocation shared by the pair: one warp of EACH CTA executes it; both
+// CTAs get the same column range.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// 2-SM MMA, D[tmem] (+)= A[smem] * B[smem]: M = 256 rows, 128 in each CTA's
+// shared and tensor memory; B's N columns split in halves, the first in rank
+// 0's shared memory.  Issued by one thread of rank 0.
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// 2-SM MMA with A read from each CTA's tensor memory (128 rows each).
+__device__ __forceinline__ void tc_mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Arrive (once) on the mbarrier at shared::cta offset `bar` in every CTA of
+// `cta_mask` when all tcgen05 operations issued so far by this thread have
+// completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;" ::"r"(smem_u32(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+
 // Programmatic dependent launch.  griddep_wait blocks until the grids this
 // one depends on (launched before it on the stream) have completed and their
 // memory is visible; griddep_launch_dependents lets the next grid of the

@@ -12,21 +12,23 @@
 //   1. plan_costs: visited key tiles per (b, KV head, 128-query block).
 //   2. plan_sort : one CTA, counting sort of those rows, longest first, into
 //                  a work queue of (row, head pair) items.
-//   3. hybrid_prefill_kernel: persistent, one CTA per SM, items taken from an
-//      atomic queue head.  An item is two query heads of one GQA group over one
-//      128-query block, so each K/V tile in shared memory feeds two MMAs.
-//        warp 8     TMA producer: Q tiles, then K/V tiles in MMA order
-//        warp 9     tcgen05 issuer: S_t = Q_t K^T (smem x smem) and O_t += P_t V
-//                   (P from TMEM, V from smem) into TMEM
-//        warps 0-7  two softmax warpgroups (one per head of the pair): read S
-//                   from TMEM, mask edge tiles only, online softmax in fp32
-//                   (exp2 domain, lazy rescale of O when the max grows by
-//                   more than 2^8), write P (bf16) back into TMEM over S, and
-//                   finally normalise O and store O / LSE.
-//      TMEM: 512 columns = per head t: S_t / P_t (128 fp32 columns) + O_t (128);
-//      the PV MMA reads P straight from TMEM, so P never touches shared memory.
-//      Shared memory: Q (2 x 32 KB), a 3-stage K/V ring (3 x 32 KB) and the O
-//      tiles of both heads on their way out (2 x 32 KB, stored by TMA).
+//   3. hybrid_prefill_kernel: persistent, one cluster of two CTAs (two SMs)
+//      per work item at a time, items taken from an atomic queue head.  An item
+//      is two query heads of one GQA group over one 128-query block, one head
+//      per CTA; every MMA is a 2-SM tcgen05 instruction (M = 256) whose K/V
+//      operand is split between the two CTAs, so each SM loads half of every
+//      K/V tile.
+//        warps 0-7  two softmax warpgroups, each half of the 128 columns of
+//                   every S row: online softmax in fp32 (exp2 domain, lazy
+//                   rescale of O when the max grows by more than 2^8), P (bf16)
+//                   written back into TMEM over S; finally O / l and LSE.
+//        warp 8     TMA producer: this CTA's Q tile and K/V halves
+//        warp 9     rank 0: tcgen05 issuer, S = Q K^T (smem x smem) and
+//                   O += P V (P from TMEM, V from smem) into TMEM
+//      TMEM (each CTA): O (128 columns) + three S/P buffers (3 x 128), so the
+//      next tiles' S = Q K^T products run while the softmax works.
+//      Shared memory (each CTA): Q (2 x 32 KB, two items in flight), a 7-stage
+//      ring of 16 KB K/V halves, and the O tile on its way out (32 KB).
 //   Batches are either B sequences of one length S ([B][S][heads][d] tensors)
 //   or sequences of different lengths packed back to back (cu_seqlens); the
 //   attention kernel is compiled once for each, so that the fixed-length one
@@ -38,46 +40,16 @@
 
 #include "ea_device.cuh"
 #include "ea_internal.h"
+#ifdef EA_CHECKS
+#include "ea_checked.h"
+#endif
 
 namespace ea {
 
 constexpr int T = EA_TILE;
 constexpr int D = EA_HEAD_DIM;
-constexpr int kStages = 3;
 constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
-constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 384;   // warpgroups: softmax head 0, softmax head 1, producer + MMA
-// Register split: launched at kLaunchRegs per thread (12 warps: 3 per SM sub-
-// partition); the producer/MMA warpgroup drops to kCtrlRegs and the two softmax
-// warpgroups grow to kSoftmaxRegs.  2 * kSoftmaxRegs + kCtrlRegs must not
-// exceed 3 * kLaunchRegs, or the increase would wait forever; the host
-// launcher checks the compiled register count before every launch.
-constexpr int kLaunchRegs = 168;
-constexpr uint32_t kCtrlRegs = 88;
-constexpr uint32_t kSoftmaxRegs = 208;
-static_assert(2 * kSoftmaxRegs + kCtrlRegs <= 3 * kLaunchRegs, "register split exceeds the launch budget");
-constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;    // log2 units: rescale when max grows > 2^8
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);  // Q, K both K-major
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);   // V is MN-major
-
-struct __align__(1024) PrefillSmem {
-    uint8_t q[2][kTileBytes];
-    uint8_t kv[kStages][kTileBytes];
-    uint8_t ostage[2][kTileBytes];   // per head: 4 warps x (32 rows x two 64-column boxes)
-    uint64_t kv_full[kStages];
-    uint64_t kv_empty[kStages];
-    uint64_t q_full, q_empty;
-    uint64_t s_full[2], p_ready[2], o_done[2];
-    uint64_t item_full[2], item_empty[2];
-    uint64_t teardown;
-    int item[2];
-    uint32_t tmem_base;
-    int abort;
-};
-constexpr size_t kPrefillSmemBytes = sizeof(PrefillSmem) + 1024;  // + alignment slack
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box of 128 rows
 
 struct PrefillArgs {
     __nv_bfloat16 *O;
@@ -106,6 +78,8 @@ struct PrefillArgs {
     int64_t *mask_off;
     int2 *row_desc;              // per planned row: {b, h << 16 | qb}, written by the planner
     int max_seqlen, total_tokens;
+    uint64_t wait_timeout_ns;    // bounded device waits give up after this long
+    int64_t test_skip_load;      // bounds-checked builds' tests: a K/V load left out (-1: none)
 };
 
 // One (b, KV head, query block) row of the plan.  tok0 is the sequence's first
@@ -404,6 +378,76 @@ __global__ void __launch_bounds__(1024) varlen_setup_kernel(PrefillArgs a)
 }
 
 // ------------------------------------------------------------ attention
+//
+// CTA pairs.  A cluster of two CTAs on two SMs computes one work item, rank r
+// holding query head 2 * pair + r of the item's GQA group, and every MMA is
+// one 2-SM tcgen05 instruction (cta_group::2, M = 256 = each CTA's 128 query
+// rows) issued by rank 0:
+//   S = Q K^T : A = Q (each CTA its own head), B = the key tile split by keys
+//               (rank r holds keys 64r .. 64r + 63 of the tile);
+//   O += P V  : A = P read from each CTA's tensor memory, B = the value tile
+//               split by head dim (rank r holds dims 64r .. 64r + 63).
+// Each SM therefore loads half of every K/V tile, and its 512 TMEM columns
+// hold O (128) and three S/P buffers (3 x 128): S of tile j + 2 is computed
+// while the softmax works on tile j.  A buffer is written again only after the
+// P V product that read its P has completed (an mbarrier wait): no ordering
+// between MMAs into different accumulators is assumed.
+//
+// Roles (320 threads per CTA):
+//   warps 0-7  softmax.  Warpgroup w handles columns 64w .. 64w + 63 of every
+//              S row (one query row per thread); the two threads of a row
+//              exchange their partial row maxima through shared memory and a
+//              named barrier of their two warps.  P (bf16 pairs) is written
+//              over the warpgroup's own S columns.  Epilogue: O / l of the
+//              warpgroup's 64 head dims, stored by TMA (or directly for
+//              variable-length batches), and LSE.
+//   warp 8     TMA producer (both CTAs): this CTA's Q and its halves of the
+//              K/V tiles, tile by tile, into a 3-slot K ring and a 4-slot V
+//              ring; completion is reported to rank 0's barriers.  Rank 0's
+//              producer also takes items from the work queue and hands them to
+//              rank 1.
+//   warps 9, 10  rank 0, one thread each: the S = Q K^T issuer and the
+//              O += P V issuer; warp 9 of both ranks: the pair's TMEM allocation.
+// A tcgen05.mma holds its issuing thread for about its own execution time, so
+// whatever an issuer does between MMAs (barrier waits, commits) leaves the
+// tensor pipe idle unless another thread is issuing meanwhile: hence two
+// issuers, each waiting on two barriers and committing once per tile.
+constexpr int kKSlots = 3;                    // K ring: slot of tile j is j % 3 (as its S/P buffer)
+constexpr int kVSlots = 4;                    // V ring: slot of tile j is j % 4
+constexpr int kHalf = 64 * D * 2;             // 16 KB: half a K tile or half a V tile
+constexpr int kPThreads = 352;
+constexpr int kPProducerWarp = 8;
+constexpr int kPMmaWarp = 9;                  // QK issuer (and TMEM allocation)
+constexpr int kPPvWarp = 10;                  // PV issuer
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;                 // O: columns 0..127
+constexpr uint32_t kColS = 128;               // S/P buffer b: columns 128 + 128 b
+constexpr uint32_t kIdescQK2 = idesc_bf16_f32(256, 128, false, false);  // Q, K both K-major
+constexpr uint32_t kIdescPV2 = idesc_bf16_f32(256, 128, false, true);   // V is MN-major
+constexpr uint16_t kBothCtas = 3;             // multicast mask: both CTAs of the pair
+constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
+
+struct __align__(1024) PairSmem {
+    uint8_t q[2][kTileBytes];      // this CTA's query tile, two items in flight
+    uint8_t k[kKSlots][kHalf];     // this CTA's halves of the key tiles (64 keys)
+    uint8_t v[kVSlots][kHalf];     // this CTA's halves of the value tiles (64 dims)
+    uint8_t ostage[kTileBytes];    // O on its way out: 8 warps x (32 rows x 64 columns)
+    uint64_t kv_full[kVSlots];     // tile j's K and V halves of both CTAs landed
+    uint64_t v_empty[kVSlots];     // P V of tile j done: V slot free, O updated
+    uint64_t q_full[2], q_empty[2];
+    uint64_t s_full[3], p_ready[3];   // S ready (and the K slot free); P written
+    uint64_t o_done;
+    uint64_t item_full[2], item_empty[2];
+    uint64_t teardown;
+    float red_max[2][2][T];        // [tile parity][warpgroup][row]
+    float red_l[2][2][T];          // [item parity][warpgroup][row]
+    int item[2];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr size_t kPairSmemBytes = sizeof(PairSmem) + 1024;  // + alignment slack
+static_assert(kPairSmemBytes <= 227 * 1024, "prefill shared memory exceeds 227 KB");
+
 struct ItemInfo : RowInfo {
     int pair, row;
 };
@@ -418,7 +462,7 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const PrefillArgs &a)
     return x;
 }
 
-// Query head of tile t of an item; an odd group size pairs its last head with
+// Query head of rank t of an item; an odd group size pairs its last head with
 // itself (second copy computed but not stored).
 __device__ __forceinline__ int item_head(const ItemInfo &x, int t, const PrefillArgs &a, bool &store)
 {
@@ -480,33 +524,123 @@ struct BlockScan {
     }
 };
 
-template <bool kVarlen>
-__device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                                              const CUtensorMap *tm_v, const PrefillArgs &a,
-                                              PrefillSmem &sm, int lane)
+// What every role of a CTA of the pair needs to wait and to abort.
+struct PairCtx {
+    uint32_t rank;           // 0: issues the MMAs and takes items from the queue
+    uint32_t peer_abort;     // shared::cluster address of the other CTA's abort flag
+    volatile int *abort;     // this CTA's abort flag
+    uint32_t *err;           // workspace error word
+    uint64_t timeout_ns;
+};
+
+// shared::cluster address of a barrier of rank 0 (this CTA's own on rank 0).
+__device__ __forceinline__ uint32_t lead_bar(const uint64_t *bar)
 {
-    uint32_t *err = &a.hdr->error;
-    uint32_t kv_it = 0, q_it = 0;
+    return mapa_shared(smem_u32(bar), 0);
+}
+
+// Bounded wait of the pair kernel, called by every lane of a warp; the result
+// is the same in all lanes.  It fails at once when the CTA is aborting
+// (checked first, so that no role passes another wait after an abort) and
+// after the timeout (raising EA_DEVERR_TIMEOUT and aborting both CTAs).
+// Acquire at CTA scope, or at cluster scope (`cl`) for the item hand-off from
+// the other CTA.
+__device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, const PairCtx &c,
+                                      bool cl = false)
+{
+    bool ok = false;
+    if (!*c.abort) {
+        const uint32_t a = smem_u32(bar);
+        ok = cl ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+        if (!ok) {
+            const uint64_t t0 = globaltimer_ns();
+            while (true) {
+                bool done = false;
+                for (int i = 0; i < 32 && !done; ++i)
+                    done = cl ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+                if (done) {
+                    ok = true;
+                    break;
+                }
+                if (*c.abort)
+                    break;
+                if (globaltimer_ns() - t0 > c.timeout_ns) {
+                    raise_error(c.err, EA_DEVERR_TIMEOUT);
+                    *c.abort = 1;
+                    red_or_cluster(c.peer_abort, 1u);
+                    break;
+                }
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// The same for one thread (the MMA issuer).
+__device__ __forceinline__ bool pwait1(uint64_t *bar, uint32_t parity, const PairCtx &c)
+{
+    if (*c.abort)
+        return false;
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(a, parity))
+                return true;
+        if (*c.abort)
+            return false;
+        if (globaltimer_ns() - t0 > c.timeout_ns) {
+            raise_error(c.err, EA_DEVERR_TIMEOUT);
+            *c.abort = 1;
+            red_or_cluster(c.peer_abort, 1u);
+            return false;
+        }
+    }
+}
+
+template <bool kVarlen>
+__device__ __forceinline__ void pair_producer(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
+                                              const CUtensorMap *tm_v, const PrefillArgs &a,
+                                              PairSmem &sm, const PairCtx &c, int lane)
+{
+    uint32_t *err = c.err;
+    const bool lead = c.rank == 0;
     const uint32_t n_items = a.hdr->n_items;   // written by the planner
+    const uint32_t n_clusters = gridDim.x / 2;
+    uint32_t jt = 0, q_it = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
         const int slot = it & 1;
-        if (!mbar_wait(&sm.item_empty[slot], ((it >> 1) & 1) ^ 1, &sm.abort, err))
-            break;
+        const uint32_t par = (it >> 1) & 1;
         int item = -1;
-        if (lane == 0) {
-            const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
-            item = x < n_items ? static_cast<int>(a.items[x]) : -1;
-            // Every CTA sees the empty queue exactly once; the last one resets
-            // the head so the same plan can feed another launch.
-            if (item < 0 && atomicAdd(&a.hdr->drained, 1u) == gridDim.x - 1) {
-                a.hdr->work_counter = 0;
-                a.hdr->drained = 0;
+        if (lead) {
+            if (!pwait(&sm.item_empty[slot], par ^ 1, c))
+                break;
+            if (lane == 0) {
+                const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
+                item = x < n_items ? static_cast<int>(a.items[x]) : -1;
+                // Every pair sees the empty queue exactly once; the last one
+                // resets the head so the same plan can feed another launch.
+                if (item < 0 && atomicAdd(&a.hdr->drained, 1u) == n_clusters - 1) {
+                    a.hdr->work_counter = 0;
+                    a.hdr->drained = 0;
+                }
+                sm.item[slot] = item;
+                st_cluster_u32(mapa_shared(smem_u32(&sm.item[slot]), 1), static_cast<uint32_t>(item));
+                mbar_arrive(&sm.item_full[slot]);
+                mbar_arrive_cluster(mapa_shared(smem_u32(&sm.item_full[slot]), 1));
             }
-            sm.item[slot] = item;
-            mbar_arrive(&sm.item_full[slot]);
+            item = __shfl_sync(0xffffffffu, item, 0);
+        } else {
+            if (!pwait(&sm.item_full[slot], par, c, true))
+                break;
+            item = sm.item[slot];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(lead_bar(&sm.item_empty[slot]));
         }
-        item = __shfl_sync(0xffffffffu, item, 0);
         if (item < 0)
             break;
         const ItemInfo x = decode_item<kVarlen>(item, a);
@@ -514,222 +648,191 @@ __device__ __forceinline__ void producer_role(const CUtensorMap *tm_q, const CUt
         if (N == 0)
             continue;
         const int mode = a.m[x.b * a.Hkv + x.h];
-        // Q tiles of both heads
-        if (!mbar_wait(&sm.q_empty, (q_it & 1) ^ 1, &sm.abort, err))
+        // this CTA's query tile
+        const int qbuf = q_it & 1;
+        if (!pwait(&sm.q_empty[qbuf], ((q_it >> 1) & 1) ^ 1, c))
             break;
         ++q_it;
         if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.q_full, 2 * kTileBytes);
-            for (int t = 0; t < 2; ++t) {
-                bool st;
-                const int qh = item_head(x, t, a, st);
-                tma_load_4d(sm.q[t], tm_q, 0, qh, x.tok0 + x.qb * T, x.tma_b, &sm.q_full);
-                tma_load_4d(sm.q[t] + kHalfBytes, tm_q, 64, qh, x.tok0 + x.qb * T, x.tma_b,
-                            &sm.q_full);
-            }
+            const uint32_t qbar = lead_bar(&sm.q_full[qbuf]);
+            if (lead)
+                mbar_arrive_expect_tx(&sm.q_full[qbuf], 2 * kTileBytes);
+            bool st;
+            const int qh = item_head(x, static_cast<int>(c.rank), a, st);
+            const int row0 = x.tok0 + x.qb * T;
+            tma_load_4d_pair(sm.q[qbuf], tm_q, 0, qh, row0, x.tma_b, qbar);
+            tma_load_4d_pair(sm.q[qbuf] + kHalfBytes, tm_q, 64, qh, row0, x.tma_b, qbar);
         }
         __syncwarp();
-        // K/V tiles in the order the MMA warp consumes them: K0, V0, K1, V1, ...
+        // K and V halves of every tile, in tile order; tile jt (counted over
+        // this CTA's items) goes to K slot jt % 3, freed by QK(jt - 3) (its
+        // s_full commit), and V slot jt % 4, freed by PV(jt - 4)
         int n_sink = 0, kb_lo = 0;
         if (mode == EA_SSA)
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         BlockScan scan;
         if (mode == EA_BLOCK)
             scan.init(a.block_mask + x.mask_row, mask_limit(a) - x.mask_row, err, x.qb + 1, lane);
-        for (int n = 0; n < N && ok; ++n) {
+        for (int n = 0; n < N && ok; ++n, ++jt) {
             const int kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
-                const int s = kv_it % kStages;
-                if (!mbar_wait(&sm.kv_empty[s], ((kv_it / kStages) & 1) ^ 1, &sm.abort, err)) {
-                    ok = false;
-                    break;
-                }
-                ++kv_it;
-                if (lane == 0) {
-                    const CUtensorMap *tm = which == 0 ? tm_k : tm_v;
-                    mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
-                    tma_load_4d(sm.kv[s], tm, 0, x.h, x.tok0 + kb * T, x.tma_b, &sm.kv_full[s]);
-                    tma_load_4d(sm.kv[s] + kHalfBytes, tm, 64, x.h, x.tok0 + kb * T, x.tma_b,
-                                &sm.kv_full[s]);
-                    if (which == 0 && a.visited) {
-                        const uint64_t bit =
-                            (static_cast<uint64_t>(x.row)) * a.nB + static_cast<uint64_t>(kb);
-                        if (in_bounds(static_cast<int64_t>(bit), a.visited_bits, err))
-                            atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
-                    }
-                }
-                __syncwarp();
+            const uint32_t ks = jt % kKSlots, vs = jt % kVSlots;
+            if (jt >= kKSlots && !pwait(&sm.s_full[ks], ((jt / kKSlots) & 1) ^ 1, c)) {
+                ok = false;
+                break;
             }
+            if (jt >= kVSlots && !pwait(&sm.v_empty[vs], ((jt / kVSlots) & 1) ^ 1, c)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                const uint32_t fbar = lead_bar(&sm.kv_full[vs]);
+                if (lead)
+                    mbar_arrive_expect_tx(&sm.kv_full[vs], 4 * kHalf);
+                bool issue = true;
+#ifdef EA_CHECKS
+                // fault injection of the bounds-checked build's tests: one
+                // tile's loads left out, so that a consumer's bounded wait runs out
+                issue = !(lead && static_cast<int64_t>(jt) == a.test_skip_load);
+#endif
+                const int key0 = x.tok0 + kb * T;
+                const int r64 = 64 * static_cast<int>(c.rank);
+                if (issue) {
+                    tma_load_4d_pair(sm.k[ks], tm_k, 0, x.h, key0 + r64, x.tma_b, fbar);
+                    tma_load_4d_pair(sm.k[ks] + kHalf / 2, tm_k, 64, x.h, key0 + r64, x.tma_b, fbar);
+                    tma_load_4d_pair(sm.v[vs], tm_v, r64, x.h, key0, x.tma_b, fbar);
+                }
+                if (lead && a.visited) {
+                    const uint64_t bit = static_cast<uint64_t>(x.row) * a.nB + static_cast<uint64_t>(kb);
+                    if (in_bounds(static_cast<int64_t>(bit), a.visited_bits, err))
+                        atomicOr(&a.visited[bit >> 5], 1u << (bit & 31));
+                }
+            }
+            __syncwarp();
         }
     }
-    // Before leaving on an abort, let the copies already issued land.
-    if (sm.abort) {
-        for (uint32_t k = kv_it > kStages ? kv_it - kStages : 0; k < kv_it; ++k) {
-            volatile int no_abort = 0;
-            mbar_wait(&sm.kv_full[k % kStages], (k / kStages) & 1, &no_abort, nullptr);
+    // Before leaving on an abort, let the copies already issued land (they
+    // target this CTA's shared memory and rank 0's barriers); none takes
+    // anywhere near this long.
+    if (*c.abort) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
         }
     }
 }
 
-// MMA issue order per item (head t in {0, 1}):
-//   QK_0(0), QK_0(1), then for every tile n:
-//   PV_n(0), QK_{n+1}(0), PV_n(1), QK_{n+1}(1).
-// P_n(t) lives in TMEM over S_t and QK_{n+1}(t) overwrites those columns.  It
-// is issued right behind PV_n(t) by the same thread, relying on tcgen05.mma
-// operations of one thread executing in issue order (PV_n(t) has read its A
-// operand before QK_{n+1}(t) writes its accumulator); the GPU parity tests
-// cover every tile of this hand-off.
-__device__ __forceinline__ void mma_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem, int lane)
+// Rank 0's MMA issuers: two threads in two warps, one for the S = Q K^T
+// products and one for the O += P V products, so that each one's barrier waits
+// and commits overlap the other's MMAs (a tcgen05.mma holds its issuing
+// thread for about its execution time).  Every ordering the products need is
+// carried by a barrier: QK(j) into S/P buffer j % 3 waits for PV(j - 3), the
+// last reader of that buffer (v_empty); PV(j) waits for P(j) (p_ready) and
+// for its V half (kv_full, long complete).  Tile j: K slot and S/P buffer
+// j % 3, V slot j % 4; j counts the tiles of this pair's items.
+template <bool kIsQK>
+__device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uint32_t tmem,
+                                         const PairCtx &c)
 {
-    uint32_t *err = &a.hdr->error;
-    uint32_t kv_it = 0, q_it = 0;
-    uint32_t p_cnt0 = 0, p_cnt1 = 0;
-    const uint32_t q_addr0 = smem_u32(sm.q[0]), q_addr1 = smem_u32(sm.q[1]);
+    uint32_t q_it = 0, j = 0;
     bool ok = true;
-
-    auto wait_kv = [&](int &s) -> bool {
-        s = kv_it % kStages;
-        if (!mbar_wait(&sm.kv_full[s], (kv_it / kStages) & 1, &sm.abort, err))
-            return false;
-        ++kv_it;
-        tc_fence_after();
-        return true;
-    };
-    // S_t = Q_t K^T (behind PV_{n-1}(t) in issue order)
-    auto issue_qk = [&](int t, int sK) -> bool {
-        if (lane == 0) {
-            const uint32_t kaddr = smem_u32(sm.kv[sK]);
-            const uint32_t qaddr = t ? q_addr1 : q_addr0;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                tc_mma(tmem + t * 256, sdesc_sw128(qaddr + off, 16, 1024),
-                       sdesc_sw128(kaddr + off, 16, 1024), kIdescQK, k > 0);
-            }
-            tc_commit(&sm.s_full[t]);
-        }
-        __syncwarp();
-        return true;
-    };
-    // O_t += P_t V once the softmax has written P_t
-    auto issue_pv = [&](int t, int sV, bool acc, bool last) -> bool {
-        uint32_t &p_cnt = t ? p_cnt1 : p_cnt0;
-        if (!mbar_wait(&sm.p_ready[t], p_cnt & 1, &sm.abort, err))
-            return false;
-        ++p_cnt;
-        tc_fence_after();
-        if (lane == 0) {
-            const uint32_t vaddr = smem_u32(sm.kv[sV]);
-#pragma unroll
-            for (int k = 0; k < T / 16; ++k)
-                tc_mma_ts(tmem + t * 256 + 128, tmem + t * 256 + k * 8,
-                          sdesc_sw128(vaddr + k * 2048, kHalfBytes, 1024), kIdescPV,
-                          (acc || k > 0) ? 1u : 0u);
-            if (last)
-                tc_commit(&sm.o_done[t]);
-        }
-        __syncwarp();
-        return true;
-    };
-
+    const uint32_t q_addr[2] = {smem_u32(sm.q[0]), smem_u32(sm.q[1])};
     for (int it = 0; ok; ++it) {
         const int slot = it & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it >> 1) & 1, &sm.abort, err))
-            break;
-        const int item = sm.item[slot];
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sm.item_empty[slot]);
-        if (item < 0)
-            break;
-        const int N = in_bounds(item / a.npairs, a.n_rows, err) ? a.costs[item / a.npairs] : 0;
-        if (N == 0)
-            continue;
-        if (!mbar_wait(&sm.q_full, q_it & 1, &sm.abort, err))
-            break;
-        ++q_it;
-        tc_fence_after();
-        int sK, sV;
-        if (!wait_kv(sK) || !issue_qk(0, sK) || !issue_qk(1, sK)) {
-            ok = false;
-            break;
-        }
-        if (lane == 0) {
-            tc_commit(&sm.kv_empty[sK]);
-            if (N == 1)
-                tc_commit(&sm.q_empty);
-        }
-        __syncwarp();
-        for (int n = 0; n < N && ok; ++n) {
-            const bool more = n + 1 < N;
-            if (!wait_kv(sV) || !issue_pv(0, sV, n > 0, !more)) {
-                ok = false;
-                break;
-            }
-            if (more && (!wait_kv(sK) || !issue_qk(0, sK))) {
-                ok = false;
-                break;
-            }
-            if (!issue_pv(1, sV, n > 0, !more)) {
-                ok = false;
-                break;
-            }
-            if (lane == 0)
-                tc_commit(&sm.kv_empty[sV]);
-            __syncwarp();
-            if (more) {
-                if (!issue_qk(1, sK)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    tc_commit(&sm.kv_empty[sK]);
-                    if (n + 2 == N)
-                        tc_commit(&sm.q_empty);
-                }
-                __syncwarp();
-            }
-        }
-        __syncwarp();
-    }
-    // All MMAs must have completed before TMEM is released.
-    if (lane == 0)
-        tc_commit(&sm.teardown);
-    __syncwarp();
-    volatile int no_abort = 0;
-    mbar_wait(&sm.teardown, 0, &no_abort, err);
-}
-
-// One warpgroup per head of the pair; thread r owns query row r of the tile.
-// Per visited tile: S (fp32, 128 TMEM columns) -> registers, edge-tile mask,
-// online softmax in the exp2 domain, P (bf16) written back over the first 64
-// columns of S for the PV MMA.  S_n(t) being ready implies PV_{n-1}(t) has
-// completed, so O_t can be rescaled in place without another wait.
-template <bool kVarlen>
-__device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &sm, uint32_t tmem,
-                                             int warp, const CUtensorMap *tm_o)
-{
-    uint32_t *err = &a.hdr->error;
-    const int t = warp >> 2;                    // head of the pair handled by this warpgroup
-    const int r = threadIdx.x & 127;            // query row within the 128-row tile
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + t * 256;
-    const uint32_t tO = tS + 128;
-    uint32_t s_cnt = 0, o_cnt = 0;
-    const float NEG_INF = -__int_as_float(0x7f800000);
-
-    for (int it = 0;; ++it) {
-        const int slot = it & 1;
-        if (!mbar_wait(&sm.item_full[slot], (it >> 1) & 1, &sm.abort, err))
+        if (!pwait1(&sm.item_full[slot], (it >> 1) & 1, c))
             break;
         const int item = sm.item[slot];
         mbar_arrive(&sm.item_empty[slot]);
         if (item < 0)
             break;
+        const int row = item / a.npairs;
+        const int N = in_bounds(row, a.n_rows, c.err) ? a.costs[row] : 0;
+        if (N == 0)
+            continue;
+        if (kIsQK) {
+            const int qbuf = q_it & 1;
+            if (!pwait1(&sm.q_full[qbuf], (q_it >> 1) & 1, c))
+                break;
+            ++q_it;
+            tc_fence_after();
+            const uint32_t qaddr = q_addr[qbuf];
+            for (int n = 0; n < N && ok; ++n) {
+                const uint32_t jj = j + n, b = jj % 3, vs = jj % kVSlots;
+                // the S/P buffer's last reader, and the tile's K/V halves
+                if ((jj >= 3 && !pwait1(&sm.v_empty[(jj - 3) % kVSlots], ((jj - 3) / kVSlots) & 1, c)) ||
+                    !pwait1(&sm.kv_full[vs], (jj / kVSlots) & 1, c)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t kaddr = smem_u32(sm.k[b]);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k & 3) * 32;
+                    tc_mma_pair(tmem + kColS + 128 * b,
+                                sdesc_sw128(qaddr + (k >> 2) * kHalfBytes + off, 16, 1024),
+                                sdesc_sw128(kaddr + (k >> 2) * (kHalf / 2) + off, 16, 1024),
+                                kIdescQK2, k > 0);
+                }
+                tc_commit_pair(&sm.s_full[b], kBothCtas);
+                if (n == N - 1)
+                    tc_commit_pair(&sm.q_empty[qbuf], kBothCtas);
+            }
+        } else {
+            for (int n = 0; n < N && ok; ++n) {
+                const uint32_t jj = j + n, b = jj % 3, vs = jj % kVSlots;
+                if (!pwait1(&sm.p_ready[b], (jj / 3) & 1, c) ||
+                    !pwait1(&sm.kv_full[vs], (jj / kVSlots) & 1, c)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t vaddr = smem_u32(sm.v[vs]);
+                const uint32_t tp = tmem + kColS + 128 * b;
+#pragma unroll
+                for (int k = 0; k < T / 16; ++k)
+                    tc_mma_ts_pair(tmem + kColO, tp + (k < 4 ? 8 * k : 64 + 8 * (k - 4)),
+                                   sdesc_sw128(vaddr + k * 2048, kHalf, 1024), kIdescPV2,
+                                   (n > 0 || k > 0) ? 1u : 0u);
+                tc_commit_pair(&sm.v_empty[vs], kBothCtas);
+                if (n == N - 1)
+                    tc_commit_pair(&sm.o_done, kBothCtas);
+            }
+        }
+        j += N;
+    }
+    // All of this thread's MMAs must have completed before TMEM is released.
+    tc_commit_pair(&sm.teardown, 1);
+}
+
+// Softmax warps: warpgroup wg, thread = query row r, columns 64 wg .. +63 of
+// every S tile of this CTA's head.
+template <bool kVarlen>
+__device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm, uint32_t tmem,
+                                             int warp, const CUtensorMap *tm_o, const PairCtx &c)
+{
+    uint32_t *err = c.err;
+    const int wg = warp >> 2;
+    const int quad = warp & 3;
+    const int lane = threadIdx.x & 31;
+    const int r = quad * 32 + lane;                       // query row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bar_id = 1 + quad;                     // this row quad's two warps
+    const uint32_t tO = tmem + lane_base + kColO + 64 * wg;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    uint32_t j = 0, o_cnt = 0;
+
+    for (int it = 0;; ++it) {
+        const int slot = it & 1;
+        if (!pwait(&sm.item_full[slot], (it >> 1) & 1, c, c.rank != 0))
+            break;
+        const int item = sm.item[slot];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive_remote(lead_bar(&sm.item_empty[slot]));
+        if (item < 0)
+            break;
         const ItemInfo x = decode_item<kVarlen>(item, a);
         bool store;
-        const int qh = item_head(x, t, a, store);
+        const int qh = item_head(x, static_cast<int>(c.rank), a, store);
         const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
         const int mode = a.m[x.b * a.Hkv + x.h];
         int n_sink = 0, kb_lo = 0;
@@ -744,29 +847,27 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         bool ok = true;
 
         for (int n = 0; n < N; ++n) {
+            const uint32_t jj = j + n;
+            const uint32_t b = jj % 3;
             int kb;
             if (mode == EA_BLOCK)
                 kb = (n == N - 1 && diag_kept) ? x.qb : -1;  // only the diagonal needs its index
             else
                 kb = seq_kb(mode, n, n_sink, kb_lo);
-            if (!mbar_wait(&sm.s_full[t], s_cnt & 1, &sm.abort, err)) {
+            if (!pwait(&sm.s_full[b], (jj / 3) & 1, c)) {
                 ok = false;
                 break;
             }
-            ++s_cnt;
             tc_fence_after();
-            uint32_t s[128];
+            const uint32_t tS = tmem + lane_base + kColS + 128 * b + 64 * wg;
+            uint32_t s[64];
             tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
             tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-            tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
             tmem_wait_ld();
 
-            // mask edge tiles only: key j = j0 + c is kept when c <= hi (causal)
-            // and, for SSA, when c < sk (sink) or c > lo (inside the window).
-            // Each 32-column chunk gets one keep word built from three prefix
-            // masks; testing a bit against a constant column costs far less
-            // than re-deriving the three comparisons per column.
+            // mask edge tiles only: key j0 + c is kept when c <= hi (causal)
+            // and, for SSA, when c < sk (sink) or c > lo (inside the window);
+            // one keep word per 32 columns, built from three prefix masks
             const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
             if (edge) {
                 const int j0 = kb * T;
@@ -777,27 +878,31 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
                     lo = i - a.window - j0;
                 }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t w = low_bits(hi + 1 - 32 * q) &
-                                       (low_bits(sk - 32 * q) | ~low_bits(lo + 1 - 32 * q));
+                for (int q = 0; q < 2; ++q) {
+                    const int co = 64 * wg + 32 * q;
+                    const uint32_t w = low_bits(hi + 1 - co) & (low_bits(sk - co) | ~low_bits(lo + 1 - co));
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (!((w >> c) & 1u))
-                            s[32 * q + c] = __float_as_uint(NEG_INF);
+                    for (int cc = 0; cc < 32; ++cc)
+                        if (!((w >> cc) & 1u))
+                            s[32 * q + cc] = __float_as_uint(NEG_INF);
                 }
             }
-            // row max: eight independent 3-input chains
+            // partial row max over this warpgroup's 64 columns (eight 3-input
+            // chains), then the row's max with the other warpgroup's
             float mxa[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mxa[k] = max3f(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]), NEG_INF);
 #pragma unroll
-            for (int c = 16; c < 128; c += 16)
+            for (int cc = 16; cc < 64; cc += 16)
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mxa[k] = max3f(mxa[k], __uint_as_float(s[c + 2 * k]), __uint_as_float(s[c + 2 * k + 1]));
-            float mx = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
-                             fmaxf(mxa[6], mxa[7]));
+                    mxa[k] = max3f(mxa[k], __uint_as_float(s[cc + 2 * k]), __uint_as_float(s[cc + 2 * k + 1]));
+            const float pm = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
+                                   fmaxf(mxa[6], mxa[7]));
+            sm.red_max[jj & 1][wg][r] = pm;
+            named_bar_sync(bar_id, 64);
+            float mx = fmaxf(pm, sm.red_max[jj & 1][wg ^ 1][r]);
             mx *= a.scale_log2;
             const float m_new = fmaxf(m_run, mx);
             float factor = 1.f;
@@ -812,56 +917,65 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
             }
             const float mb = m_run > NEG_INF ? m_run : 0.f;
             // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
-            // the row sum in four independent packed accumulators, P packed to
-            // bf16 pairs in place (s[c/2] once s[c], s[c+1] are consumed)
+            // the row sum in four packed accumulators, P packed to bf16 pairs
+            // in place (s[c/2] once s[c], s[c+1] are consumed)
             const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
             const uint64_t nm2 = f2_pack(-mb, -mb);
             uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-            for (int c = 0; c < 128; c += 2) {
+            for (int cc = 0; cc < 64; cc += 2) {
                 float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sc2, nm2),
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])), sc2, nm2),
                           x0, x1);
                 const float p0 = ex2(x0), p1 = ex2(x1);
-                acc[(c >> 1) & 3] = f2_add(acc[(c >> 1) & 3], f2_pack(p0, p1));
-                s[c >> 1] = pack_bf16x2(p0, p1);
+                acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
+                s[cc >> 1] = pack_bf16x2(p0, p1);
             }
             float l0, l1, l2, l3;
             f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
             f2_unpack(f2_add(acc[2], acc[3]), l2, l3);
             l_run += (l0 + l1) + (l2 + l3);
 
-            // O rescale (PV_{n-1} is complete: it preceded QK_n in issue order
-            // and QK_n waited for it)
+            // O rescale: PV of the previous tile must have completed
             if (__any_sync(0xffffffffu, rescale_o)) {
+                if (!pwait(&sm.v_empty[(jj - 1) % kVSlots], ((jj - 1) / kVSlots) & 1, c)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 2; ++ch) {
                     uint32_t o[32];
                     tmem_ld32(tO + ch * 32, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        o[c] = __float_as_uint(__uint_as_float(o[c]) * factor);
+                    for (int cc = 0; cc < 32; ++cc)
+                        o[cc] = __float_as_uint(__uint_as_float(o[cc]) * factor);
                     tmem_st32(tO + ch * 32, o);
                 }
             }
-            // P (bf16 pairs) over the first 64 columns of S
-            tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+            // P (bf16 pairs) over the first 32 of this warpgroup's S columns
+            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&sm.p_ready[t]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_remote(lead_bar(&sm.p_ready[b]));
         }
         if (!ok)
             break;
+        j += N;
 
         // epilogue: O / l -> bf16, LSE = ln(2^m * l)
         if (N > 0) {
-            if (!mbar_wait(&sm.o_done[t], o_cnt & 1, &sm.abort, err))
+            if (!pwait(&sm.o_done, o_cnt & 1, c))
                 break;
             ++o_cnt;
             tc_fence_after();
         }
+        sm.red_l[it & 1][wg][r] = l_run;
+        named_bar_sync(bar_id, 64);
+        const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
         // the row's sequence, length and offsets, decoded again here so that
         // none of them stays live across the tile loop
         RowInfo e;
@@ -869,45 +983,45 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         const bool row_ok = store && i < e.S &&
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
                             in_bounds(qh, a.Hq, err);
-        const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
         __nv_bfloat16 *orow =
-            a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh;
-        // Fixed-length batches: each warp stages its 32 rows in shared memory
-        // (128-byte swizzle, as the tensor map expects) and its lane 0 stores
-        // them with TMA, which skips rows past S.  Variable-length batches
-        // store directly: the rows past a sequence belong to the next one.
+            a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh + 64 * wg;
+        // Fixed-length batches: each warp stages its 32 rows x 64 columns in
+        // shared memory (128-byte swizzle, as the tensor map expects) and its
+        // lane 0 stores them with TMA, which skips rows past S.  Variable-
+        // length batches store directly: the rows past a sequence belong to
+        // the next one.
         const bool staged = !kVarlen && store;
         const int wrow = r & 31;
-        uint8_t *wstage = sm.ostage[t] + (warp & 3) * (kTileBytes / 4);
+        uint8_t *wstage = sm.ostage + warp * (kTileBytes / 8);
         if (staged) {
-            if ((r & 31) == 0)
+            if (lane == 0)
                 bulk_wait_read_all();     // the previous item's store has read the stage
             __syncwarp();
         }
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < 2; ++ch) {
             uint32_t o[32];
             if (N > 0) {
                 tmem_ld32(tO + ch * 32, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                    o[c] = 0u;
+                for (int cc = 0; cc < 32; ++cc)
+                    o[cc] = 0u;
             }
             uint32_t w[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-                w[c] = pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                   __uint_as_float(o[2 * c + 1]) * inv_l);
+            for (int cc = 0; cc < 16; ++cc)
+                w[cc] = pack_bf16x2(__uint_as_float(o[2 * cc]) * inv_l,
+                                    __uint_as_float(o[2 * cc + 1]) * inv_l);
             if (staged) {
-                // columns ch*32 .. +31: box ch/2, 16-byte chunks (ch%2)*4 .. +3
-                uint8_t *box = wstage + (ch >> 1) * (kTileBytes / 8);
+                // columns ch*32 .. +31 of the warp's 64: 16-byte chunks ch*4 .. +3
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c16 = (ch & 1) * 4 + j;
-                    *reinterpret_cast<uint4 *>(box + wrow * 128 + ((c16 ^ (wrow & 7)) << 4)) =
-                        make_uint4(w[j * 4], w[j * 4 + 1], w[j * 4 + 2], w[j * 4 + 3]);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int c16 = ch * 4 + q4;
+                    *reinterpret_cast<uint4 *>(wstage + wrow * 128 + ((c16 ^ (wrow & 7)) << 4)) =
+                        make_uint4(w[q4 * 4], w[q4 * 4 + 1], w[q4 * 4 + 2], w[q4 * 4 + 3]);
                 }
             } else if (row_ok) {
                 if (a.o_v8) {
@@ -926,85 +1040,103 @@ __device__ __forceinline__ void softmax_role(const PrefillArgs &a, PrefillSmem &
         if (staged) {
             fence_proxy_async_smem();     // the stage's writes -> the TMA unit
             __syncwarp();
-            if ((r & 31) == 0) {
-                const int row0 = x.qb * T + (warp & 3) * 32;
-                tma_store_4d(tm_o, wstage, 0, qh, row0, e.b);
-                tma_store_4d(tm_o, wstage + kTileBytes / 8, 64, qh, row0, e.b);
+            if (lane == 0) {
+                tma_store_4d(tm_o, wstage, 64 * wg, qh, x.qb * T + quad * 32, e.b);
                 bulk_commit_group();
             }
         }
-        if (row_ok && a.LSE &&
+        if (wg == 0 && row_ok && a.LSE &&
             in_bounds(e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i, a.lse_elems, err))
             a.LSE[e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
-                l_run > 0.f ? (m_run + __log2f(l_run)) * 0.69314718055994531f : NEG_INF;
+                l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : NEG_INF;
         tc_fence_before();
     }
+    // On an abort this thread may have left its row partner waiting at their
+    // named barrier: one arrival releases it (its next wait then fails too).
+    if (*c.abort)
+        named_bar_arrive(bar_id, 64);
     // the last stores must be complete before the CTA (and its shared memory) goes
-    if ((threadIdx.x & 31) == 0)
+    if (lane == 0)
         bulk_wait_all();
 }
 
 template <bool kVarlen>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     hybrid_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
-    PrefillSmem &sm = *reinterpret_cast<PrefillSmem *>(
+    PairSmem &sm = *reinterpret_cast<PairSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_rank();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.kv_full[s], 1);
-            mbar_init(&sm.kv_empty[s], 1);
+        for (int s = 0; s < kVSlots; ++s) {
+            mbar_init(&sm.kv_full[s], 1);      // rank 0's producer; bytes from both CTAs
+            mbar_init(&sm.v_empty[s], 1);      // MMA commit (multicast)
         }
-        mbar_init(&sm.q_full, 1);
-        mbar_init(&sm.q_empty, 1);
         for (int t = 0; t < 2; ++t) {
-            mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.p_ready[t], 128);
-            mbar_init(&sm.o_done[t], 1);
+            mbar_init(&sm.q_full[t], 1);
+            mbar_init(&sm.q_empty[t], 1);
             mbar_init(&sm.item_full[t], 1);
-            mbar_init(&sm.item_empty[t], 1 + 256);
+            // rank 0: its two MMA issuers and 8 softmax warps, rank 1's producer and 8 softmax warps
+            mbar_init(&sm.item_empty[t], 19);
         }
-        mbar_init(&sm.teardown, 1);
+        for (int t = 0; t < 3; ++t) {
+            mbar_init(&sm.s_full[t], 1);
+            mbar_init(&sm.p_ready[t], 16);     // 8 softmax warps of each CTA
+        }
+        mbar_init(&sm.o_done, 1);
+        mbar_init(&sm.teardown, 2);            // one commit from each MMA issuer
         sm.abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
     }
-    if (warp == kMmaWarp) {
-        tmem_alloc(&sm.tmem_base, kTmemCols);
-        tmem_relinquish();
+    if (warp == kPMmaWarp) {
+        tmem_alloc_pair(&sm.tmem_base, kTmemCols);
+        tmem_relinquish_pair();
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kPProducerWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();     // both CTAs' barriers initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    PairCtx c;
+    c.rank = rank;
+    c.peer_abort = mapa_shared(smem_u32(&sm.abort), rank ^ 1u);
+    c.abort = &sm.abort;
+    c.err = &a.hdr->error;
+    c.timeout_ns = a.wait_timeout_ns;
 
-    if (warp >= 8) {
-        regs_dec<kCtrlRegs>();
-        if (warp == kProducerWarp)
-            producer_role<kVarlen>(&tm_q, &tm_k, &tm_v, a, sm, lane);
-        else if (warp == kMmaWarp)
-            mma_role(a, sm, tmem, lane);
-    } else {
-        regs_inc<kSoftmaxRegs>();
-        softmax_role<kVarlen>(a, sm, tmem, warp, &tm_o);
+    if (warp < 8)
+        pair_softmax<kVarlen>(a, sm, tmem, warp, &tm_o, c);
+    else if (warp == kPProducerWarp)
+        pair_producer<kVarlen>(&tm_q, &tm_k, &tm_v, a, sm, c, lane);
+    else if (warp == kPMmaWarp && rank == 0 && lane == 0)
+        pair_mma<true>(a, sm, tmem, c);
+    else if (warp == kPPvWarp && rank == 0 && lane == 0)
+        pair_mma<false>(a, sm, tmem, c);
+    // every MMA has completed before TMEM is released
+    if (rank == 0 && (warp == kPMmaWarp || warp == kPPvWarp) && lane == 0) {
+        volatile int no_abort = 0;
+        mbar_wait(&sm.teardown, 0, &no_abort, c.err);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    cluster_sync_all();     // no remote arrival or MMA into this CTA is still to come
+    if (warp == kPMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -1066,10 +1198,13 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
     a.visited_bits = static_cast<int64_t>(B) * Hkv * nB * nB;
     a.n_rows = static_cast<uint32_t>(n_rows);
     a.n_items = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * (qb_end - qb_begin) * npairs);
+    a.wait_timeout_ns = EA_WAIT_TIMEOUT_NS;
+    a.test_skip_load = -1;
     return EA_OK;
 }
 
 static bool g_attr_done[64] = {};
+static int g_max_clusters[64] = {};   // co-resident CTA pairs of the attention kernel, per device
 
 static ea_status ensure_attributes()
 {
@@ -1080,17 +1215,55 @@ static ea_status ensure_attributes()
         return EA_OK;
     if (cudaFuncSetAttribute(hybrid_prefill_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPrefillSmemBytes)) != cudaSuccess ||
+                             static_cast<int>(kPairSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(hybrid_prefill_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPrefillSmemBytes)) != cudaSuccess ||
+                             static_cast<int>(kPairSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(int) * (EA_MAX_SEQ / T + 2))) != cudaSuccess)
         return EA_ERR_CUDA;
-    if (dev < 64)
+    // How many CTA pairs fit on the device at once (one CTA per SM; an odd SM
+    // count or pair placement rules can leave SMs out).
+    int clusters = 0;
+    {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * 1024, 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPairSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&clusters, hybrid_prefill_kernel<false>, &cfg) !=
+                cudaSuccess ||
+            clusters < 1)
+            return EA_ERR_CUDA;
+    }
+    if (dev < 64) {
+        g_max_clusters[dev] = clusters;
         g_attr_done[dev] = true;
+    }
     return EA_OK;
 }
+
+#ifdef EA_CHECKS
+// Fault injection of the bounds-checked build's tests: the next attention
+// launch leaves out one K/V load and uses a short wait limit.
+static int64_t g_test_skip_load = -1;
+static uint64_t g_test_timeout_ns = 0;
+
+extern "C" ea_status ea_checked_inject_prefill_timeout(int64_t skip_load, uint64_t timeout_ns)
+{
+    if (skip_load < 0 || timeout_ns == 0)
+        return EA_ERR_INVALID_ARG;
+    g_test_skip_load = skip_load;
+    g_test_timeout_ns = timeout_ns;
+    return EA_OK;
+}
+#endif
 
 namespace ea {
 
@@ -1141,7 +1314,7 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
         return EA_ERR_INVALID_ARG;
     alignas(64) CUtensorMap tq, tk, tv, to;
     if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, S, B, q_str, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tk, K, d, Hkv, S, B, kv_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tk, K, d, Hkv, S, B, kv_str, 64, T / 2, true) ||
         !encode_tmap_bf16_4d(&tv, V, d, Hkv, S, B, kv_str, 64, T, true) ||
         !encode_tmap_bf16_4d(&to, O, d, Hq, S, B, o_str, 64, 32, true))
         return EA_ERR_INVALID_ARG;
@@ -1157,35 +1330,32 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
     return launch_attend(tq, tk, tv, to, a, stream);
 }
 
-// The persistent attention launch over a plan made with the same arguments.
+// The persistent attention launch over a plan made with the same arguments:
+// as many CTA pairs as fit on the device (or as there are items).
 static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const CUtensorMap &to, const PrefillArgs &a, void *stream)
+                               const CUtensorMap &to, const PrefillArgs &a_in, void *stream)
 {
     ea_status s;
     if ((s = ensure_attributes()) != EA_OK)
         return s;
-    // The register split inside the kernel assumes this launch size.
-    const bool varlen = a.cu_seqlens != nullptr;
-    cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, varlen ? reinterpret_cast<const void *>(hybrid_prefill_kernel<true>)
-                                          : reinterpret_cast<const void *>(hybrid_prefill_kernel<false>)) !=
-        cudaSuccess)
-        return EA_ERR_CUDA;
-    if (fa.numRegs != kLaunchRegs)
-        return EA_ERR_UNSUPPORTED;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return EA_ERR_CUDA;
-    const int sms = num_sms(dev);
-    if (sms <= 0)
-        return EA_ERR_CUDA;
-    const unsigned grid =
-        static_cast<unsigned>(a.n_items < static_cast<uint32_t>(sms) ? a.n_items : sms);
+    PrefillArgs a = a_in;
+#ifdef EA_CHECKS
+    if (g_test_skip_load >= 0) {
+        a.test_skip_load = g_test_skip_load;
+        a.wait_timeout_ns = g_test_timeout_ns;
+        g_test_skip_load = -1;
+    }
+#endif
+    const uint32_t clusters = static_cast<uint32_t>(g_max_clusters[dev]);
+    const unsigned grid = 2u * (a.n_items < clusters ? (a.n_items > 0 ? a.n_items : 1u) : clusters);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (varlen)
-        hybrid_prefill_kernel<true><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, to, a);
+    if (a.cu_seqlens)
+        hybrid_prefill_kernel<true><<<grid, kPThreads, kPairSmemBytes, st>>>(tq, tk, tv, to, a);
     else
-        hybrid_prefill_kernel<false><<<grid, kThreads, kPrefillSmemBytes, st>>>(tq, tk, tv, to, a);
+        hybrid_prefill_kernel<false><<<grid, kPThreads, kPairSmemBytes, st>>>(tq, tk, tv, to, a);
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
@@ -1227,7 +1397,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     const int64_t o4[4] = {static_cast<int64_t>(total_tokens) * o_str[0], o_str[0], o_str[1], 1};
     alignas(64) CUtensorMap tq, tk, tv, to;
     if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, total_tokens, 1, q4, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tk, K, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tk, K, d, Hkv, total_tokens, 1, kv4, 64, T / 2, true) ||
         !encode_tmap_bf16_4d(&tv, V, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
         !encode_tmap_bf16_4d(&to, O, d, Hq, total_tokens, 1, o4, 64, 32, true))
         return EA_ERR_INVALID_ARG;
@@ -1271,6 +1441,8 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.row_desc = reinterpret_cast<int2 *>(ws + L.row_desc);
     a.max_seqlen = max_seqlen;
     a.total_tokens = total_tokens;
+    a.wait_timeout_ns = EA_WAIT_TIMEOUT_NS;
+    a.test_skip_load = -1;
 
     ea_status s;
     if ((s = ensure_attributes()) != EA_OK)

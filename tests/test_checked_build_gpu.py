@@ -130,3 +130,31 @@ def test_router(dev):
     rr, mm, lg, _ = oracle.route(K, Ws, bs)
     assert np.array_equal(r.cpu().numpy(), rr)
     np.testing.assert_array_equal(logits.cpu().numpy(), lg)
+
+
+def test_bounded_wait_runs_out_and_the_next_call_recovers(dev):
+    """A device wait made to run out, in the accepted form: the checked build's
+    hook leaves out one K/V load of the next prefill launch and shortens every
+    wait to 1 ms.  The MMA issuer's wait for that load expires, the kernel
+    reports EA_ERR_TIMEOUT through the workspace error word and every role of
+    both CTAs of each pair leaves (nothing faults or hangs); the next normal
+    call on the same stream and workspace matches the oracle."""
+    import ctypes
+    L = ea.lib()
+    assert hasattr(L, "ea_checked_inject_prefill_timeout")
+    L.ea_checked_inject_prefill_timeout.argtypes = [ctypes.c_int64, ctypes.c_uint64]
+    L.ea_checked_inject_prefill_timeout.restype = ctypes.c_int
+    B, S, Hq, Hkv = 1, 1000, 8, 2
+    Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=91)
+    m = torch.tensor([[FULL, SSA]], dtype=torch.uint8)
+    Qd, Kd, Vd, md = Q.to(dev), K.to(dev), V.to(dev), m.to(dev)
+    ws = ea.prefill_workspace(B, S, Hq, Hkv, device=dev)
+    assert L.ea_checked_inject_prefill_timeout(3, 1_000_000) == 0
+    ea.ea_hybrid_attn_prefill(Qd, Kd, Vd, md, sink=16, window=100, workspace=ws)
+    torch.cuda.synchronize()
+    assert ea.ea_check_errors(ws) == 5        # EA_ERR_TIMEOUT, read and cleared
+    O, LSE = ea.ea_hybrid_attn_prefill(Qd, Kd, Vd, md, sink=16, window=100, workspace=ws)
+    torch.cuda.synchronize()
+    check_no_device_error(ws)
+    Oref, Lref = oracle.prefill_full(Q, K, V, m, sink=16, window=100)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "after a timeout")
