@@ -418,6 +418,9 @@ def run_ours(args, rank, world, dev):
     routed = None
     if not args.no_routed:
         routed = run_routed_layers(args, dev, peaks, flush)
+    multi = None
+    if not args.no_multi_layer:
+        multi = run_multi_layer(args, dev, peaks, flush)
 
     # ---- sparsity ratios of the timed layer (host)
     msr, esr = ea.ea_sparsity_ratios(
@@ -446,6 +449,7 @@ def run_ours(args, rank, world, dev):
         "xa": xa,
         "xa256k_seeded_mask": xa256k,
         "routed64k_36_layers": routed,
+        "multi_layer_launch": multi,
     }
     # the CPU baseline is reported by rank 0 of a single-GPU run only
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1056,6 +1060,76 @@ def run_seeded_layer(args, dev, peaks, flush, name):
             "clocks": clk}
 
 
+def run_multi_layer(args, dev, peaks, flush):
+    """36 layers of the Llama-3.1-8B-shaped layer (32/8 heads, SSA 128/2048, per
+    layer a seeded choice of about 6 SSA KV heads of 8) at S = 4K and 16K:
+    the per-layer loop (ea_hybrid_attn_prefill per layer: planner + launch, and
+    the pipeline drains at every layer's end) against one
+    ea_hybrid_attn_prefill_layers call (one planner and one launch whose
+    longest-first queue mixes every layer's items)."""
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    L = 36
+    out = {"workload": "36 layers, B=1, Hq=32, Hkv=8, d=128, SSA 128/2048, seeded modes per layer",
+           "l2": "flushed before every timed step (256 MB memset, outside the events)"}
+    stream = torch.cuda.current_stream()
+    for S in (4096, 16384):
+        cfg = dataclasses.replace(wl.LLAMA_32K, S=S, name="llama_s%d" % S)
+        Qs = [wl.randn_bf16((1, S, 32, 128), seed=3 * l, device=dev) for l in range(L)]
+        Ks = [wl.randn_bf16((1, S, 8, 128), seed=3 * l + 1, device=dev) for l in range(L)]
+        Vs = [wl.randn_bf16((1, S, 8, 128), seed=3 * l + 2, device=dev) for l in range(L)]
+        g = torch.Generator().manual_seed(S)
+        m_cpu = [(torch.rand(1, 8, generator=g) < 0.75).to(torch.uint8) for _ in range(L)]
+        ms = [m.to(dev) for m in m_cpu]
+        tile = sum(prefill_work(cfg, m.numpy(), None)[1] for m in m_cpu)
+        Os = [torch.empty_like(Qs[0]) for _ in range(L)]
+        LSEs = [torch.empty(1, 32, S, dtype=torch.float32, device=dev) for _ in range(L)]
+        ws1 = ea.prefill_workspace(1, S, 32, 8, device=dev)
+        wsl = ea.prefill_layers_workspace(L, 1, S, 32, 8, device=dev)
+
+        def per_layer():
+            for l in range(L):
+                ea.ea_hybrid_attn_prefill(Qs[l], Ks[l], Vs[l], ms[l], sink=128, window=2048, O=Os[l],
+                                          LSE=LSEs[l], workspace=ws1)
+
+        def one_launch():
+            ea.ea_hybrid_attn_prefill_layers(Qs, Ks, Vs, ms, sink=128, window=2048, Os=Os, LSEs=LSEs,
+                                             workspace=wsl)
+
+        def timed(fn):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(5):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return statistics.median(x.elapsed_time(y) for x, y in ts)
+
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
+        t_loop = timed(per_layer)
+        t_one = timed(one_launch)
+        clk = clocks.stop()
+        if ea.ea_check_errors(ws1) != 0 or ea.ea_check_errors(wsl) != 0:
+            raise RuntimeError("device error in the multi-layer prefill")
+        out["s%d" % S] = {
+            "per_layer_loop_ms": round(t_loop, 3), "one_launch_ms": round(t_one, 3),
+            "speedup": round(t_loop / t_one, 3),
+            "one_launch_visited_tile_tflops": round(tile / (t_one * 1e-3) / 1e12, 1),
+            "one_launch_frac_of_bf16_peak": round(tile / (t_one * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "per_layer_visited_tile_tflops": round(tile / (t_loop * 1e-3) / 1e12, 1),
+            "visited_tile_flops": tile, "gpu_launches": {"per_layer_loop": 3 * L, "one_launch": 3},
+            "clocks": clk}
+        del Qs, Ks, Vs, Os, LSEs, ws1, wsl
+    return out
+
+
 # ------------------------------------------------------------------ Algorithm 1(a) comparison
 def serial_dispatch(ea, Q, K, V, m_cpu, sink, window, O, LSE, ws_fa, ws_sa):
     """Serial Dispatch ("Paper Reading - Elastic Attention" (English notes),
@@ -1153,6 +1227,8 @@ def main():
                     help="time the 36-layer router-driven 64K workload instead of the benchmark")
     ap.add_argument("--layers", type=int, default=None, help="layers of --routed-layers (default 36)")
     ap.add_argument("--no-routed", action="store_true", help="skip the 36-layer routed 64K line")
+    ap.add_argument("--no-multi-layer", action="store_true",
+                    help="skip the 36-layer one-launch vs per-layer comparison (4K and 16K)")
     ap.add_argument("--no-xa256k", action="store_true",
                     help="skip the 256K XA-SSA layer on the seeded block mask")
     ap.add_argument("--serial-sweep", action="store_true",

@@ -248,6 +248,47 @@ ea_status ea_hybrid_attn_prefill_varlen(const void *Q, const void *K, const void
                                         void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Several layers in one launch.  The pages' single launch ([EN] §04
+ * Deployment, Algorithm 1(b): the per-head routing metadata drives one kernel
+ * whose grid is left intact, instead of the per-group launches of Algorithm
+ * 1(a)) taken across layers: one planner over the rows of every layer, one
+ * longest-first work queue mixing the layers, one persistent launch.  Per
+ * layer the result is exactly ea_hybrid_attn_prefill's on that layer (the same
+ * items, computed the same way; bit for bit).  Every layer has the same B, S,
+ * head counts and strides (a transformer's layers).
+ *
+ * ea_prefill_layer describes one layer; every pointer is device memory laid
+ * out as for ea_hybrid_attn_prefill (Q, K, V, O with the shared strides q_str,
+ * kv_str, o_str; LSE [B][Hq][S] or NULL; m [B][Hkv]; block_mask
+ * [B][Hkv][nB][nB] or NULL).  `layers` itself is a host array of n_layers
+ * entries, read during the call.  n_layers is 1 .. EA_MAX_PREFILL_LAYERS
+ * (more: EA_ERR_UNSUPPORTED); the workspace is
+ * ea_prefill_layers_workspace_size(...) bytes (0: invalid sizes, or
+ * B * n_layers above 65535).  Every layer is checked as ea_hybrid_attn_prefill
+ * checks its arguments before anything is enqueued; device-side conditions
+ * are reported by ea_check_errors(workspace).
+ */
+#define EA_MAX_PREFILL_LAYERS 48
+
+typedef struct {
+    const void *Q;
+    const void *K;
+    const void *V;
+    void *O;
+    float *LSE;
+    const uint8_t *m;
+    const uint8_t *block_mask;
+} ea_prefill_layer;
+
+size_t ea_prefill_layers_workspace_size(int n_layers, int B, int S, int Hq, int Hkv, int d);
+
+ea_status ea_hybrid_attn_prefill_layers(const ea_prefill_layer *layers, int n_layers,
+                                        const int64_t q_str[4], const int64_t kv_str[4],
+                                        const int64_t o_str[4], int B, int S, int Hq, int Hkv,
+                                        int d, float scale, int sink, int window, int block_size,
+                                        void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * ea_hybrid_attn_prefill_noalloc - ea_hybrid_attn_prefill for callers that
  * cannot provide a workspace, e.g. an engine whose device memory is owned by
  * its own allocator and that forbids allocations once it is running, or a

@@ -37,6 +37,7 @@ EXPORTS = ("ea_status_string", "ea_route", "ea_route_layers", "ea_prefill_worksp
            "ea_prefill_plan", "ea_prefill_attend", "ea_hybrid_attn_prefill_noalloc",
            "ea_prefill_host_buffer_size", "ea_hybrid_attn_prefill_host",
            "ea_prefill_varlen_workspace_size", "ea_hybrid_attn_prefill_varlen",
+           "ea_prefill_layers_workspace_size", "ea_hybrid_attn_prefill_layers",
            "ea_decode_workspace_size",
            "ea_hybrid_attn_decode", "ea_hybrid_attn_decode_paged", "ea_xa_workspace_size",
            "ea_xa_estimate", "ea_sparsity_ratios", "ea_check_errors")
@@ -51,6 +52,15 @@ class EAError(RuntimeError):
 class _Mlp(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int), ("dims", ctypes.POINTER(ctypes.c_int)),
                 ("W", ctypes.POINTER(ctypes.c_void_p)), ("b", ctypes.POINTER(ctypes.c_void_p))]
+
+
+class _PrefillLayer(ctypes.Structure):
+    _fields_ = [("Q", ctypes.c_void_p), ("K", ctypes.c_void_p), ("V", ctypes.c_void_p),
+                ("O", ctypes.c_void_p), ("LSE", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("block_mask", ctypes.c_void_p)]
+
+
+MAX_PREFILL_LAYERS = 48
 
 
 class _Policy(ctypes.Structure):
@@ -97,6 +107,11 @@ def lib():
         L.ea_hybrid_attn_prefill_host.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P,
                                                   i32, i32, P, i32, P, sz, i32, P]
         L.ea_hybrid_attn_prefill_host.restype = ctypes.c_int
+        L.ea_prefill_layers_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        L.ea_prefill_layers_workspace_size.restype = sz
+        L.ea_hybrid_attn_prefill_layers.argtypes = [P, i32, P, P, P, i32, i32, i32, i32, i32, f32,
+                                                    i32, i32, i32, P, sz, P]
+        L.ea_hybrid_attn_prefill_layers.restype = ctypes.c_int
         L.ea_prefill_varlen_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
         L.ea_prefill_varlen_workspace_size.restype = sz
         L.ea_hybrid_attn_prefill_varlen.argtypes = [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32,
@@ -305,6 +320,65 @@ def ea_hybrid_attn_prefill_noalloc(Q, K, V, m, *, sink, window, block_mask=None,
         _ptr(visited_bitmap), _stream(stream))
     _check("ea_hybrid_attn_prefill_noalloc", st)
     return O, LSE
+
+
+def ea_prefill_layers_workspace_size(n_layers, B, S, Hq, Hkv, d=128):
+    return int(lib().ea_prefill_layers_workspace_size(n_layers, B, S, Hq, Hkv, d))
+
+
+def prefill_layers_workspace(n_layers, B, S, Hq, Hkv, d=128, device="cuda"):
+    n = ea_prefill_layers_workspace_size(n_layers, B, S, Hq, Hkv, d)
+    if n == 0:
+        raise ValueError("unsupported multi-layer prefill sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def ea_hybrid_attn_prefill_layers(Qs, Ks, Vs, ms, *, sink, window, block_masks=None, scale=None,
+                                  Os=None, LSEs=None, workspace=None, stream=None, want_lse=True):
+    """Several layers (same shapes and strides) in one planner + one launch.
+    Qs/Ks/Vs/ms: lists of per-layer CUDA tensors as for ea_hybrid_attn_prefill;
+    block_masks: None or a list (entries may be None).  Returns (Os, LSEs)."""
+    L = len(Qs)
+    if not (len(Ks) == len(Vs) == len(ms) == L) or L < 1:
+        raise ValueError("one Q, K, V and m per layer")
+    for t, nm in ((Qs, "Q"), (Ks, "K"), (Vs, "V")):
+        for x in t:
+            _dev(x, nm, torch.bfloat16)
+    for x in ms:
+        _dev(x, "m", torch.uint8)
+    B, S, Hq, d = Qs[0].shape
+    Hkv = Ks[0].shape[2]
+    for l in range(L):
+        if (Qs[l].shape != Qs[0].shape or Ks[l].shape != Ks[0].shape or Vs[l].shape != Ks[0].shape or
+                Qs[l].stride() != Qs[0].stride() or Ks[l].stride() != Ks[0].stride() or
+                Vs[l].stride() != Ks[0].stride()):
+            raise ValueError("every layer must have the same shapes and strides")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if Os is None:
+        Os = [torch.empty_like(Qs[0]) for _ in range(L)]
+    if LSEs is None:
+        LSEs = [torch.empty(B, Hq, S, dtype=torch.float32, device=Qs[0].device) if want_lse else None
+                for _ in range(L)]
+    bms = list(block_masks) if block_masks is not None else [None] * L
+    for bm in bms:
+        if bm is not None:
+            _dev(bm, "block_mask", torch.uint8)
+            if not bm.is_contiguous():
+                raise ValueError("block_mask must be contiguous")
+    if workspace is None:
+        workspace = prefill_layers_workspace(L, B, S, Hq, Hkv, d, Qs[0].device)
+    arr = (_PrefillLayer * L)()
+    for l in range(L):
+        arr[l] = _PrefillLayer(Qs[l].data_ptr(), Ks[l].data_ptr(), Vs[l].data_ptr(), Os[l].data_ptr(),
+                               LSEs[l].data_ptr() if LSEs[l] is not None else None, ms[l].data_ptr(),
+                               bms[l].data_ptr() if bms[l] is not None else None)
+    st = lib().ea_hybrid_attn_prefill_layers(
+        ctypes.cast(arr, ctypes.c_void_p), L, _strides(Qs[0]), _strides(Ks[0]), _strides(Os[0]), B, S,
+        Hq, Hkv, d, float(scale), int(sink), int(window), TILE, _ptr(workspace), workspace.numel(),
+        _stream(stream))
+    _check("ea_hybrid_attn_prefill_layers", st)
+    return Os, LSEs
 
 
 def ea_prefill_host_buffer_size(B, S, Hq, Hkv, d=128, with_block_mask=False):

@@ -51,17 +51,24 @@ constexpr int D = EA_HEAD_DIM;
 constexpr int kTileBytes = T * D * 2;        // one 128 x 128 bf16 tile
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column swizzled TMA box of 128 rows
 
+// Layers of one launch (a multi-layer prefill: every layer has the same shapes
+// and strides; its rows are numbered layer by layer).
+constexpr int kMaxLayers = EA_MAX_PREFILL_LAYERS;
+
 struct PrefillArgs {
-    __nv_bfloat16 *O;
+    __nv_bfloat16 *O[kMaxLayers];
+    const uint8_t *m[kMaxLayers];
+    const uint8_t *block_mask[kMaxLayers];
+    float *LSE[kMaxLayers];
+    int n_layers;
+    uint32_t rows_per_layer;     // rows of one layer (B * Hkv * nB for fixed-length batches)
+    int sort_by_layer;           // planner: queue layer by layer (longest first within a layer)
     int64_t o_sb, o_ss, o_sh;
-    float *LSE;
     int64_t lse_sb, lse_sh;      // LSE[b * lse_sb + qh * lse_sh + token]
     int64_t lse_elems;           // LSE elements (bounds-checked builds)
     int64_t mask_elems;          // block-mask bytes, -1: mask_off[B] (bounds-checked builds)
     int64_t visited_bits;        // bits of the visited bitmap (bounds-checked builds)
     int o_v8;                    // every O row starts 32-byte aligned: 256-bit stores
-    const uint8_t *m;
-    const uint8_t *block_mask;
     uint32_t *visited;
     int32_t *costs;
     uint32_t *items;
@@ -86,7 +93,7 @@ struct PrefillArgs {
 // token in the tensors' token dimension, tma_b its batch coordinate, mask_row
 // the offset of the row's block-mask entries.
 struct RowInfo {
-    int b, h, qb, tok0, S, nB, tma_b;
+    int layer, b, h, qb, tok0, S, nB, tma_b;
     int64_t mask_row;
 };
 
@@ -99,6 +106,7 @@ __device__ __forceinline__ int64_t mask_limit(const PrefillArgs &a)
 // Fields of a variable-length row once b, h and qb are known.
 __device__ __forceinline__ void varlen_row_fields(const PrefillArgs &a, RowInfo &x)
 {
+    x.layer = 0;
     x.tok0 = a.cu_seqlens[x.b];
     x.S = a.cu_seqlens[x.b + 1] - x.tok0;
     x.nB = (x.S + T - 1) / T;
@@ -106,9 +114,14 @@ __device__ __forceinline__ void varlen_row_fields(const PrefillArgs &a, RowInfo 
     x.mask_row = a.mask_off[x.b] + (static_cast<int64_t>(x.h) * x.nB + x.qb) * x.nB;
 }
 
-// A row of a fixed-length batch: rows are [b][h][qb].
+// A row of a fixed-length batch: rows are [layer][b][h][qb].
 __device__ __forceinline__ void decode_row_dense(int row, const PrefillArgs &a, RowInfo &x)
 {
+    x.layer = 0;
+    if (a.n_layers > 1) {
+        x.layer = static_cast<int>(static_cast<uint32_t>(row) / a.rows_per_layer);
+        row -= x.layer * static_cast<int>(a.rows_per_layer);
+    }
     x.qb = row % a.nB;
     const int bh = row / a.nB;
     x.h = bh % a.Hkv;
@@ -222,7 +235,8 @@ __global__ void plan_costs_kernel(PrefillArgs a)
     if (a.cu_seqlens && lane == 0)
         a.row_desc[warp] = make_int2(x.b, (x.h << 16) | x.qb);
     const int qb = x.qb;
-    const int mode = a.m[x.b * a.Hkv + x.h];
+    const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
+    const uint8_t *bmask = a.block_mask[x.layer];
     int n = 0;
     if (mode == EA_FULL) {
         n = qb + 1;
@@ -230,8 +244,8 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         int n_sink, kb_lo;
         ssa_tiles(qb, a.sink, a.window, n_sink, kb_lo);
         n = n_sink + (qb - kb_lo + 1);
-    } else if (mode == EA_BLOCK && a.block_mask) {
-        const uint8_t *row = a.block_mask + x.mask_row;
+    } else if (mode == EA_BLOCK && bmask) {
+        const uint8_t *row = bmask + x.mask_row;
         for (int kb = lane; kb <= qb; kb += 32)
             if (in_bounds(x.mask_row + kb, mask_limit(a), &a.hdr->error))
                 n += row[kb] != 0;
@@ -246,16 +260,27 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         a.costs[warp] = n;
 }
 
-// One CTA: counting sort of the planned rows (cost >= 0) by visited-tile
-// count, longest first; each row contributes its npairs items back to back.
-// The order among rows of equal cost is unspecified (every item is computed
-// the same way whatever the order, so results do not depend on it).  Also
-// resets the work queue head.
+// Sort key of a planned row: longest first, and for a multi-layer launch in
+// layer order first (key layer * (nB + 1) + nB - cost), so that one layer's
+// K/V tiles stay in L2 while its items run and the next layer's longest items
+// follow without a drain.  Keys of rows outside the plan: -1.
+__device__ __forceinline__ int plan_key(uint32_t r, int cost, const PrefillArgs &a)
+{
+    if (cost < 0)
+        return -1;
+    const int layer = a.sort_by_layer ? static_cast<int>(r / a.rows_per_layer) : 0;
+    return layer * (a.nB + 1) + (a.nB - cost);
+}
+
+// One CTA: counting sort of the planned rows (cost >= 0) by key, ascending;
+// each row contributes its npairs items back to back.  The order among rows of
+// equal key is unspecified (every item is computed the same way whatever the
+// order, so results do not depend on it).  Also resets the work queue head.
 __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
 {
-    extern __shared__ int hist[];  // [nB + 2]
+    extern __shared__ int hist[];  // [nbins + 1]
     __shared__ int scan_tmp[1024];
-    const int nbins = a.nB + 1;    // costs 0..nB
+    const int nbins = (a.sort_by_layer ? a.n_layers : 1) * (a.nB + 1);
     const int tid = threadIdx.x;
     for (int c = tid; c < nbins; c += blockDim.x)
         hist[c] = 0;
@@ -265,20 +290,22 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
         n_planned = 0;
     __syncthreads();
     int mine = 0;
-    for (uint32_t r = tid; r < a.n_rows; r += blockDim.x)
-        if (a.costs[r] >= 0) {
-            atomicAdd(&hist[a.costs[r]], 1);
+    for (uint32_t r = tid; r < a.n_rows; r += blockDim.x) {
+        const int k = plan_key(r, a.costs[r], a);
+        if (k >= 0) {
+            atomicAdd(&hist[k], 1);
             ++mine;
         }
+    }
     atomicAdd(&n_planned, mine);
     __syncthreads();
-    // Exclusive scan in descending cost order: start[c] = #rows with cost > c.
-    // Bin c is visited at position nbins - 1 - c; each thread scans a segment.
+    // Exclusive scan over the keys: start[k] = #rows with a smaller key; each
+    // thread scans a segment of bins.
     const int per = (nbins + blockDim.x - 1) / blockDim.x;
     const int lo = tid * per, hi = min(lo + per, nbins);
     int local = 0;
     for (int p = lo; p < hi; ++p)
-        local += hist[nbins - 1 - p];
+        local += hist[p];
     scan_tmp[tid] = local;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {
@@ -289,28 +316,27 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
     }
     int run = scan_tmp[tid] - local;
     for (int p = lo; p < hi; ++p) {
-        const int c = nbins - 1 - p;
-        const int cnt = hist[c];
-        hist[c] = run;
+        const int cnt = hist[p];
+        hist[p] = run;
         run += cnt;
     }
     __syncthreads();
     // Scatter by every warp, 32 rows at a time: the lanes of a warp with the
-    // same cost take consecutive slots, their first lane claims them for the
+    // same key take consecutive slots, their first lane claims them for the
     // group with one shared-memory atomic.
     {
         const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
         const unsigned lt = (1u << lane) - 1u;
         for (uint32_t base = warp * 32u; base < a.n_rows; base += 32u * nwarps) {
             const uint32_t r = base + lane;
-            const int c = r < a.n_rows ? a.costs[r] : -1;
-            const bool valid = c >= 0;
+            const int k = r < a.n_rows ? plan_key(r, a.costs[r], a) : -1;
+            const bool valid = k >= 0;
             const unsigned active = __ballot_sync(0xffffffffu, valid);
-            const unsigned peers = __match_any_sync(0xffffffffu, c) & active;
+            const unsigned peers = __match_any_sync(0xffffffffu, k) & active;
             const int leader = peers ? __ffs(peers) - 1 : 0;
             int start = 0;
             if (valid && lane == leader)
-                start = atomicAdd(&hist[c], __popc(peers));
+                start = atomicAdd(&hist[k], __popc(peers));
             start = __shfl_sync(0xffffffffu, start, leader);
             if (valid) {
                 const int pos = start + __popc(peers & lt);
@@ -600,9 +626,15 @@ __device__ __forceinline__ bool pwait1(uint64_t *bar, uint32_t parity, const Pai
     }
 }
 
-template <bool kVarlen>
-__device__ __forceinline__ void pair_producer(const CUtensorMap *tm_q, const CUtensorMap *tm_k,
-                                              const CUtensorMap *tm_v, const PrefillArgs &a,
+// The TMA tensor maps of the launch's layers (one entry for single-layer
+// launches).
+template <int kL>
+struct TmapTable {
+    CUtensorMap q[kL], k[kL], v[kL], o[kL];
+};
+
+template <bool kVarlen, int kL>
+__device__ __forceinline__ void pair_producer(const TmapTable<kL> &tm, const PrefillArgs &a,
                                               PairSmem &sm, const PairCtx &c, int lane)
 {
     uint32_t *err = c.err;
@@ -647,7 +679,10 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tm_q, const CUt
         const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
         if (N == 0)
             continue;
-        const int mode = a.m[x.b * a.Hkv + x.h];
+        const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
+        const CUtensorMap *tm_q = &tm.q[kL == 1 ? 0 : x.layer];
+        const CUtensorMap *tm_k = &tm.k[kL == 1 ? 0 : x.layer];
+        const CUtensorMap *tm_v = &tm.v[kL == 1 ? 0 : x.layer];
         // this CTA's query tile
         const int qbuf = q_it & 1;
         if (!pwait(&sm.q_empty[qbuf], ((q_it >> 1) & 1) ^ 1, c))
@@ -672,7 +707,7 @@ __device__ __forceinline__ void pair_producer(const CUtensorMap *tm_q, const CUt
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         BlockScan scan;
         if (mode == EA_BLOCK)
-            scan.init(a.block_mask + x.mask_row, mask_limit(a) - x.mask_row, err, x.qb + 1, lane);
+            scan.init(a.block_mask[x.layer] + x.mask_row, mask_limit(a) - x.mask_row, err, x.qb + 1, lane);
         for (int n = 0; n < N && ok; ++n, ++jt) {
             const int kb = mode == EA_BLOCK ? scan.next(lane) : seq_kb(mode, n, n_sink, kb_lo);
             const uint32_t ks = jt % kKSlots, vs = jt % kVSlots;
@@ -805,9 +840,9 @@ __device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uin
 
 // Softmax warps: warpgroup wg, thread = query row r, columns 64 wg .. +63 of
 // every S tile of this CTA's head.
-template <bool kVarlen>
+template <bool kVarlen, int kL>
 __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm, uint32_t tmem,
-                                             int warp, const CUtensorMap *tm_o, const PairCtx &c)
+                                             int warp, const TmapTable<kL> &tm, const PairCtx &c)
 {
     uint32_t *err = c.err;
     const int wg = warp >> 2;
@@ -834,14 +869,14 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         bool store;
         const int qh = item_head(x, static_cast<int>(c.rank), a, store);
         const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
-        const int mode = a.m[x.b * a.Hkv + x.h];
+        const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
         int n_sink = 0, kb_lo = 0;
         if (mode == EA_SSA)
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
         bool diag_kept = false;
         if (mode == EA_BLOCK && N > 0)
             diag_kept = in_bounds(x.mask_row + x.qb, mask_limit(a), err) &&
-                        a.block_mask[x.mask_row + x.qb] != 0;
+                        a.block_mask[x.layer][x.mask_row + x.qb] != 0;
         const int i = x.qb * T + r;
         float m_run = NEG_INF, l_run = 0.f;
         bool ok = true;
@@ -984,8 +1019,8 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
                             in_bounds(qh, a.Hq, err);
         const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
-        __nv_bfloat16 *orow =
-            a.O + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss + qh * a.o_sh + 64 * wg;
+        __nv_bfloat16 *orow = a.O[e.layer] + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss +
+                              qh * a.o_sh + 64 * wg;
         // Fixed-length batches: each warp stages its 32 rows x 64 columns in
         // shared memory (128-byte swizzle, as the tensor map expects) and its
         // lane 0 stores them with TMA, which skips rows past S.  Variable-
@@ -1041,13 +1076,13 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
             fence_proxy_async_smem();     // the stage's writes -> the TMA unit
             __syncwarp();
             if (lane == 0) {
-                tma_store_4d(tm_o, wstage, 64 * wg, qh, x.qb * T + quad * 32, e.b);
+                tma_store_4d(&tm.o[kL == 1 ? 0 : e.layer], wstage, 64 * wg, qh, x.qb * T + quad * 32, e.b);
                 bulk_commit_group();
             }
         }
-        if (wg == 0 && row_ok && a.LSE &&
+        if (wg == 0 && row_ok && a.LSE[e.layer] &&
             in_bounds(e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i, a.lse_elems, err))
-            a.LSE[e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
+            a.LSE[e.layer][e.b * a.lse_sb + qh * a.lse_sh + e.tok0 + i] =
                 l_tot > 0.f ? (m_run + __log2f(l_tot)) * 0.69314718055994531f : NEG_INF;
         tc_fence_before();
     }
@@ -1060,12 +1095,9 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         bulk_wait_all();
 }
 
-template <bool kVarlen>
+template <bool kVarlen, int kL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
-    hybrid_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
-                          const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_o, const PrefillArgs a)
+    hybrid_prefill_kernel(const __grid_constant__ TmapTable<kL> tm, const PrefillArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     PairSmem &sm = *reinterpret_cast<PairSmem *>(
@@ -1099,11 +1131,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         tmem_alloc_pair(&sm.tmem_base, kTmemCols);
         tmem_relinquish_pair();
     }
-    if (warp == kPProducerWarp && lane == 0) {
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_o);
+    if (warp == kPProducerWarp && lane == 0 && kL == 1) {
+        tma_prefetch_desc(&tm.q[0]);
+        tma_prefetch_desc(&tm.k[0]);
+        tma_prefetch_desc(&tm.v[0]);
+        tma_prefetch_desc(&tm.o[0]);
     }
     tc_fence_before();
     __syncthreads();
@@ -1118,9 +1150,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     c.timeout_ns = a.wait_timeout_ns;
 
     if (warp < 8)
-        pair_softmax<kVarlen>(a, sm, tmem, warp, &tm_o, c);
+        pair_softmax<kVarlen, kL>(a, sm, tmem, warp, tm, c);
     else if (warp == kPProducerWarp)
-        pair_producer<kVarlen>(&tm_q, &tm_k, &tm_v, a, sm, c, lane);
+        pair_producer<kVarlen, kL>(tm, a, sm, c, lane);
     else if (warp == kPMmaWarp && rank == 0 && lane == 0)
         pair_mma<true>(a, sm, tmem, c);
     else if (warp == kPPvWarp && rank == 0 && lane == 0)
@@ -1171,8 +1203,9 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
         return EA_ERR_UNSUPPORTED;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     a = PrefillArgs{};
-    a.m = m;
-    a.block_mask = block_mask;
+    a.m[0] = m;
+    a.block_mask[0] = block_mask;
+    a.n_layers = 1;
     a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
     a.items = reinterpret_cast<uint32_t *>(ws + L.items);
     a.hdr = reinterpret_cast<ea_ws_header *>(ws);
@@ -1197,11 +1230,18 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
     a.mask_elems = block_mask ? static_cast<int64_t>(B) * Hkv * nB * nB : 0;
     a.visited_bits = static_cast<int64_t>(B) * Hkv * nB * nB;
     a.n_rows = static_cast<uint32_t>(n_rows);
+    a.rows_per_layer = static_cast<uint32_t>(n_rows);
     a.n_items = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * (qb_end - qb_begin) * npairs);
     a.wait_timeout_ns = EA_WAIT_TIMEOUT_NS;
     a.test_skip_load = -1;
     return EA_OK;
 }
+
+// Histogram bins the planner's sort may use (shared memory): a whole
+// single-layer plan at the longest length, or a multi-layer plan sorted by
+// layer while it fits (longer multi-layer plans are sorted by cost alone).
+constexpr int kMaxSortBins = 48 * 1024;
+static_assert(kMaxSortBins >= EA_MAX_SEQ / T + 2, "sort histogram");
 
 static bool g_attr_done[64] = {};
 static int g_max_clusters[64] = {};   // co-resident CTA pairs of the attention kernel, per device
@@ -1213,14 +1253,17 @@ static ea_status ensure_attributes()
         return EA_ERR_CUDA;
     if (dev < 64 && g_attr_done[dev])
         return EA_OK;
-    if (cudaFuncSetAttribute(hybrid_prefill_kernel<false>,
+    if (cudaFuncSetAttribute(hybrid_prefill_kernel<false, 1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPairSmemBytes)) != cudaSuccess ||
-        cudaFuncSetAttribute(hybrid_prefill_kernel<true>,
+        cudaFuncSetAttribute(hybrid_prefill_kernel<true, 1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPairSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(hybrid_prefill_kernel<false, kMaxLayers>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kPairSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(sizeof(int) * (EA_MAX_SEQ / T + 2))) != cudaSuccess)
+                             static_cast<int>(sizeof(int) * kMaxSortBins)) != cudaSuccess)
         return EA_ERR_CUDA;
     // How many CTA pairs fit on the device at once (one CTA per SM; an odd SM
     // count or pair placement rules can leave SMs out).
@@ -1237,7 +1280,7 @@ static ea_status ensure_attributes()
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaOccupancyMaxActiveClusters(&clusters, hybrid_prefill_kernel<false>, &cfg) !=
+        if (cudaOccupancyMaxActiveClusters(&clusters, hybrid_prefill_kernel<false, 1>, &cfg) !=
                 cudaSuccess ||
             clusters < 1)
             return EA_ERR_CUDA;
@@ -1286,8 +1329,8 @@ ea_status prefill_plan_range(int B, int S, int Hq, int Hkv, int d, const uint8_t
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
-static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const CUtensorMap &to, const PrefillArgs &a, void *stream);
+template <int kL>
+static ea_status launch_attend(const TmapTable<kL> &tm, const PrefillArgs &a, void *stream);
 
 ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void *O, float *LSE,
                                const int64_t q_str[4], const int64_t kv_str[4],
@@ -1312,28 +1355,28 @@ ea_status prefill_attend_range(const void *Q, const void *K, const void *V, void
             return EA_ERR_INVALID_ARG;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
         return EA_ERR_INVALID_ARG;
-    alignas(64) CUtensorMap tq, tk, tv, to;
-    if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, S, B, q_str, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tk, K, d, Hkv, S, B, kv_str, 64, T / 2, true) ||
-        !encode_tmap_bf16_4d(&tv, V, d, Hkv, S, B, kv_str, 64, T, true) ||
-        !encode_tmap_bf16_4d(&to, O, d, Hq, S, B, o_str, 64, 32, true))
+    TmapTable<1> tm;
+    if (!encode_tmap_bf16_4d(&tm.q[0], Q, d, Hq, S, B, q_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tm.k[0], K, d, Hkv, S, B, kv_str, 64, T / 2, true) ||
+        !encode_tmap_bf16_4d(&tm.v[0], V, d, Hkv, S, B, kv_str, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tm.o[0], O, d, Hq, S, B, o_str, 64, 32, true))
         return EA_ERR_INVALID_ARG;
-    a.O = static_cast<__nv_bfloat16 *>(O);
+    a.O[0] = static_cast<__nv_bfloat16 *>(O);
     a.o_sb = o_str[0];
     a.o_ss = o_str[1];
     a.o_sh = o_str[2];
     a.o_v8 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 && o_str[0] % 16 == 0 && o_str[1] % 16 == 0 &&
              o_str[2] % 16 == 0;
-    a.LSE = LSE;
+    a.LSE[0] = LSE;
     a.visited = visited_bitmap;
     a.scale_log2 = scale * 1.4426950408889634f;
-    return launch_attend(tq, tk, tv, to, a, stream);
+    return launch_attend(tm, a, stream);
 }
 
 // The persistent attention launch over a plan made with the same arguments:
 // as many CTA pairs as fit on the device (or as there are items).
-static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
-                               const CUtensorMap &to, const PrefillArgs &a_in, void *stream)
+template <int kL>
+static ea_status launch_attend(const TmapTable<kL> &tm, const PrefillArgs &a_in, void *stream)
 {
     ea_status s;
     if ((s = ensure_attributes()) != EA_OK)
@@ -1352,10 +1395,14 @@ static ea_status launch_attend(const CUtensorMap &tq, const CUtensorMap &tk, con
     const uint32_t clusters = static_cast<uint32_t>(g_max_clusters[dev]);
     const unsigned grid = 2u * (a.n_items < clusters ? (a.n_items > 0 ? a.n_items : 1u) : clusters);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (a.cu_seqlens)
-        hybrid_prefill_kernel<true><<<grid, kPThreads, kPairSmemBytes, st>>>(tq, tk, tv, to, a);
-    else
-        hybrid_prefill_kernel<false><<<grid, kPThreads, kPairSmemBytes, st>>>(tq, tk, tv, to, a);
+    if constexpr (kL == 1) {
+        if (a.cu_seqlens)
+            hybrid_prefill_kernel<true, 1><<<grid, kPThreads, kPairSmemBytes, st>>>(tm, a);
+        else
+            hybrid_prefill_kernel<false, 1><<<grid, kPThreads, kPairSmemBytes, st>>>(tm, a);
+    } else {
+        hybrid_prefill_kernel<false, kL><<<grid, kPThreads, kPairSmemBytes, st>>>(tm, a);
+    }
     return cudaGetLastError() == cudaSuccess ? EA_OK : EA_ERR_CUDA;
 }
 
@@ -1395,17 +1442,18 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     const int64_t q4[4] = {static_cast<int64_t>(total_tokens) * q_str[0], q_str[0], q_str[1], 1};
     const int64_t kv4[4] = {static_cast<int64_t>(total_tokens) * kv_str[0], kv_str[0], kv_str[1], 1};
     const int64_t o4[4] = {static_cast<int64_t>(total_tokens) * o_str[0], o_str[0], o_str[1], 1};
-    alignas(64) CUtensorMap tq, tk, tv, to;
-    if (!encode_tmap_bf16_4d(&tq, Q, d, Hq, total_tokens, 1, q4, 64, T, true) ||
-        !encode_tmap_bf16_4d(&tk, K, d, Hkv, total_tokens, 1, kv4, 64, T / 2, true) ||
-        !encode_tmap_bf16_4d(&tv, V, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
-        !encode_tmap_bf16_4d(&to, O, d, Hq, total_tokens, 1, o4, 64, 32, true))
+    TmapTable<1> tm;
+    if (!encode_tmap_bf16_4d(&tm.q[0], Q, d, Hq, total_tokens, 1, q4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tm.k[0], K, d, Hkv, total_tokens, 1, kv4, 64, T / 2, true) ||
+        !encode_tmap_bf16_4d(&tm.v[0], V, d, Hkv, total_tokens, 1, kv4, 64, T, true) ||
+        !encode_tmap_bf16_4d(&tm.o[0], O, d, Hq, total_tokens, 1, o4, 64, 32, true))
         return EA_ERR_INVALID_ARG;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     PrefillArgs a{};
-    a.m = m;
-    a.block_mask = block_mask;
+    a.m[0] = m;
+    a.block_mask[0] = block_mask;
+    a.n_layers = 1;
     a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
     a.items = reinterpret_cast<uint32_t *>(ws + L.items);
     a.hdr = reinterpret_cast<ea_ws_header *>(ws);
@@ -1421,13 +1469,14 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.qb_begin = 0;
     a.qb_end = a.nB;
     a.n_rows = static_cast<uint32_t>(L.rows);
+    a.rows_per_layer = static_cast<uint32_t>(L.rows);
     a.n_items = static_cast<uint32_t>(L.rows * npairs);
-    a.O = static_cast<__nv_bfloat16 *>(O);
+    a.O[0] = static_cast<__nv_bfloat16 *>(O);
     a.o_sb = 0;
     a.o_ss = o_str[0];
     a.o_sh = o_str[1];
     a.o_v8 = (reinterpret_cast<uintptr_t>(O) & 31u) == 0 && o_str[0] % 16 == 0 && o_str[1] % 16 == 0;
-    a.LSE = LSE;
+    a.LSE[0] = LSE;
     a.lse_sb = 0;
     a.lse_sh = total_tokens;
     a.lse_elems = static_cast<int64_t>(Hq) * total_tokens;
@@ -1455,7 +1504,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return EA_ERR_CUDA;
-    return launch_attend(tq, tk, tv, to, a, stream);
+    return launch_attend(tm, a, stream);
 }
 
 extern "C" ea_status ea_prefill_plan(int B, int S, int Hq, int Hkv, int d, const uint8_t *m,
@@ -1526,6 +1575,93 @@ extern "C" ea_status ea_hybrid_attn_prefill(const void *Q, const void *K, const 
     return ea_prefill_attend(Q, K, V, O, LSE, q_str, kv_str, o_str, B, S, Hq, Hkv, d, scale, m,
                              sink, window, block_mask, block_size, workspace, ws_bytes,
                              visited_bitmap, stream);
+}
+
+extern "C" size_t ea_prefill_layers_workspace_size(int n_layers, int B, int S, int Hq, int Hkv, int d)
+{
+    if (n_layers < 1 || n_layers > EA_MAX_PREFILL_LAYERS || B < 1 ||
+        static_cast<int64_t>(B) * n_layers > 65535)
+        return 0;
+    return ea_prefill_workspace_size(B * n_layers, S, Hq, Hkv, d);
+}
+
+extern "C" ea_status ea_hybrid_attn_prefill_layers(const ea_prefill_layer *layers, int n_layers,
+                                                   const int64_t q_str[4], const int64_t kv_str[4],
+                                                   const int64_t o_str[4], int B, int S, int Hq,
+                                                   int Hkv, int d, float scale, int sink, int window,
+                                                   int block_size, void *workspace, size_t ws_bytes,
+                                                   void *stream)
+{
+    if (!layers || n_layers < 1)
+        return EA_ERR_INVALID_ARG;
+    if (n_layers > EA_MAX_PREFILL_LAYERS)
+        return EA_ERR_UNSUPPORTED;
+    // every layer's arguments, as a single-layer call checks them
+    for (int l = 0; l < n_layers; ++l) {
+        const ea_prefill_layer &ly = layers[l];
+        const ea_status s = prefill_validate(ly.Q, ly.K, ly.V, ly.O, q_str, kv_str, o_str, B, S, Hq,
+                                             Hkv, d, scale, ly.m, sink, window, ly.block_mask,
+                                             block_size, workspace, ws_bytes);
+        if (s != EA_OK)
+            return s;
+    }
+    const size_t need = ea_prefill_layers_workspace_size(n_layers, B, S, Hq, Hkv, d);
+    if (need == 0)
+        return EA_ERR_UNSUPPORTED;
+    if (ws_bytes < need)
+        return EA_ERR_WORKSPACE;
+    PrefillArgs a;
+    ea_status s = prefill_common(B, S, Hq, Hkv, d, layers[0].m, sink, window, layers[0].block_mask,
+                                 block_size, workspace, ws_bytes, a);
+    if (s != EA_OK)
+        return s;
+    // rows of every layer, numbered layer by layer
+    const PrefillWs WL = prefill_ws_layout(B * n_layers, S, Hq, Hkv);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    a.costs = reinterpret_cast<int32_t *>(ws + WL.costs);
+    a.items = reinterpret_cast<uint32_t *>(ws + WL.items);
+    a.n_layers = n_layers;
+    a.rows_per_layer = static_cast<uint32_t>(static_cast<int64_t>(B) * Hkv * a.nB);
+    const int64_t rows = static_cast<int64_t>(n_layers) * a.rows_per_layer;
+    if (rows * a.npairs >= (int64_t(1) << 31))
+        return EA_ERR_UNSUPPORTED;
+    a.n_rows = static_cast<uint32_t>(rows);
+    a.n_items = static_cast<uint32_t>(rows * a.npairs);
+    a.sort_by_layer = static_cast<int64_t>(n_layers) * (a.nB + 1) + 1 <= kMaxSortBins;
+    a.visited = nullptr;
+    a.visited_bits = 0;
+    bool any_mask = false, v8 = o_str[0] % 16 == 0 && o_str[1] % 16 == 0 && o_str[2] % 16 == 0;
+    static thread_local TmapTable<kMaxLayers> tm;   // 24.5 KB: kept off the stack
+    for (int l = 0; l < n_layers; ++l) {
+        const ea_prefill_layer &ly = layers[l];
+        a.m[l] = ly.m;
+        a.block_mask[l] = ly.block_mask;
+        a.O[l] = static_cast<__nv_bfloat16 *>(ly.O);
+        a.LSE[l] = ly.LSE;
+        any_mask |= ly.block_mask != nullptr;
+        v8 = v8 && (reinterpret_cast<uintptr_t>(ly.O) & 31u) == 0;
+        if (!encode_tmap_bf16_4d(&tm.q[l], ly.Q, d, Hq, S, B, q_str, 64, T, true) ||
+            !encode_tmap_bf16_4d(&tm.k[l], ly.K, d, Hkv, S, B, kv_str, 64, T / 2, true) ||
+            !encode_tmap_bf16_4d(&tm.v[l], ly.V, d, Hkv, S, B, kv_str, 64, T, true) ||
+            !encode_tmap_bf16_4d(&tm.o[l], ly.O, d, Hq, S, B, o_str, 64, 32, true))
+            return EA_ERR_INVALID_ARG;
+    }
+    a.mask_elems = any_mask ? static_cast<int64_t>(B) * Hkv * a.nB * a.nB : 0;
+    a.o_sb = o_str[0];
+    a.o_ss = o_str[1];
+    a.o_sh = o_str[2];
+    a.o_v8 = v8;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if ((s = ensure_attributes()) != EA_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int warps_per_cta = 8;
+    plan_costs_kernel<<<static_cast<unsigned>(ceil_div(a.n_rows, warps_per_cta)), warps_per_cta * 32, 0,
+                        st>>>(a);
+    plan_sort_kernel<<<1, 1024, sizeof(int) * ((a.sort_by_layer ? n_layers : 1) * (a.nB + 1) + 1), st>>>(a);
+    if (cudaGetLastError() != cudaSuccess)
+        return EA_ERR_CUDA;
+    return launch_attend(tm, a, stream);
 }
 
 // ---------------------------------------------------------------------------

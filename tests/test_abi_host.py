@@ -40,6 +40,25 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_multi_layer_prefill_host_checks(L):
+    # workspace: the single-layer plan of B * n_layers rows; 1 .. 48 layers
+    assert L.ea_prefill_layers_workspace_size(36, 1, 4096, 32, 8, 128) == \
+        L.ea_prefill_workspace_size(36, 4096, 32, 8, 128)
+    assert L.ea_prefill_layers_workspace_size(0, 1, 4096, 32, 8, 128) == 0
+    assert L.ea_prefill_layers_workspace_size(49, 1, 4096, 32, 8, 128) == 0
+    assert L.ea_prefill_layers_workspace_size(2, 40000, 128, 32, 8, 128) == 0   # B * layers > 65535
+    s4 = (ctypes.c_int64 * 4)(32 * 128 * 256, 32 * 128, 128, 1)
+    k4 = (ctypes.c_int64 * 4)(8 * 128 * 256, 8 * 128, 128, 1)
+    # rejected before anything is enqueued (no GPU needed): no layers, too many, a null tensor
+    assert L.ea_hybrid_attn_prefill_layers(None, 1, s4, k4, s4, 1, 256, 32, 8, 128,
+                                           ctypes.c_float(0.1), 0, 64, 128, None, 0, None) == 1
+    arr = (ea._PrefillLayer * 49)()
+    assert L.ea_hybrid_attn_prefill_layers(ctypes.cast(arr, ctypes.c_void_p), 49, s4, k4, s4, 1, 256, 32,
+                                           8, 128, ctypes.c_float(0.1), 0, 64, 128, None, 0, None) == 2
+    assert L.ea_hybrid_attn_prefill_layers(ctypes.cast(arr, ctypes.c_void_p), 2, s4, k4, s4, 1, 256, 32,
+                                           8, 128, ctypes.c_float(0.1), 0, 64, 128, None, 0, None) == 1
+
+
 def test_status_strings(L):
     for code in range(7):
         s = L.ea_status_string(code)
