@@ -62,7 +62,8 @@ struct PrefillArgs {
     float *LSE[kMaxLayers];
     int n_layers;
     uint32_t rows_per_layer;     // rows of one layer (B * Hkv * nB for fixed-length batches)
-    int sort_by_layer;           // planner: queue layer by layer (longest first within a layer)
+    int sort_group;              // planner: 0 longest first; 1 layer by layer, 2 sequence by sequence
+    int n_sort_groups;           // groups of that order (1 for sort_group 0)
     int64_t o_sb, o_ss, o_sh;
     int64_t lse_sb, lse_sh;      // LSE[b * lse_sb + qh * lse_sh + token]
     int64_t lse_elems;           // LSE elements (bounds-checked builds)
@@ -114,11 +115,13 @@ __device__ __forceinline__ void varlen_row_fields(const PrefillArgs &a, RowInfo 
     x.mask_row = a.mask_off[x.b] + (static_cast<int64_t>(x.h) * x.nB + x.qb) * x.nB;
 }
 
-// A row of a fixed-length batch: rows are [layer][b][h][qb].
+// A row of a fixed-length batch: rows are [layer][b][h][qb] (the layer part
+// only when the launch may hold several).
+template <bool kMulti = true>
 __device__ __forceinline__ void decode_row_dense(int row, const PrefillArgs &a, RowInfo &x)
 {
     x.layer = 0;
-    if (a.n_layers > 1) {
+    if (kMulti && a.n_layers > 1) {
         x.layer = static_cast<int>(static_cast<uint32_t>(row) / a.rows_per_layer);
         row -= x.layer * static_cast<int>(a.rows_per_layer);
     }
@@ -166,11 +169,11 @@ __device__ __forceinline__ bool decode_row_search(int row, const PrefillArgs &a,
 // record, which keeps the search out of the warps' register budgets).  The
 // attention kernel is compiled separately for fixed- and variable-length
 // batches, so that the fixed-length one carries none of this.
-template <bool kVarlen>
+template <bool kVarlen, int kL>
 __device__ __forceinline__ void decode_row(int row, const PrefillArgs &a, RowInfo &x)
 {
     if (!kVarlen) {
-        decode_row_dense(row, a, x);
+        decode_row_dense<(kL > 1)>(row, a, x);
         return;
     }
     const int2 d = in_bounds(row, a.n_rows, &a.hdr->error) ? a.row_desc[row] : make_int2(0, 0);
@@ -260,16 +263,21 @@ __global__ void plan_costs_kernel(PrefillArgs a)
         a.costs[warp] = n;
 }
 
-// Sort key of a planned row: longest first, and for a multi-layer launch in
-// layer order first (key layer * (nB + 1) + nB - cost), so that one layer's
-// K/V tiles stay in L2 while its items run and the next layer's longest items
-// follow without a drain.  Keys of rows outside the plan: -1.
+// Sort key of a planned row: longest first, and for a multi-layer launch or a
+// variable-length batch in layer or sequence order first (key
+// group * (nB + 1) + nB - cost), so that one group's K/V tiles stay in L2 while
+// its items run and the next group's longest items follow without a drain.
+// Keys of rows outside the plan: -1.
 __device__ __forceinline__ int plan_key(uint32_t r, int cost, const PrefillArgs &a)
 {
     if (cost < 0)
         return -1;
-    const int layer = a.sort_by_layer ? static_cast<int>(r / a.rows_per_layer) : 0;
-    return layer * (a.nB + 1) + (a.nB - cost);
+    int group = 0;
+    if (a.sort_group == 1)
+        group = static_cast<int>(r / a.rows_per_layer);
+    else if (a.sort_group == 2)
+        group = a.row_desc[r].x;
+    return group * (a.nB + 1) + (a.nB - cost);
 }
 
 // One CTA: counting sort of the planned rows (cost >= 0) by key, ascending;
@@ -280,7 +288,7 @@ __global__ void __launch_bounds__(1024) plan_sort_kernel(PrefillArgs a)
 {
     extern __shared__ int hist[];  // [nbins + 1]
     __shared__ int scan_tmp[1024];
-    const int nbins = (a.sort_by_layer ? a.n_layers : 1) * (a.nB + 1);
+    const int nbins = a.n_sort_groups * (a.nB + 1);
     const int tid = threadIdx.x;
     for (int c = tid; c < nbins; c += blockDim.x)
         hist[c] = 0;
@@ -478,13 +486,15 @@ struct ItemInfo : RowInfo {
     int pair, row;
 };
 
-template <bool kVarlen>
+template <bool kVarlen, int kL>
 __device__ __forceinline__ ItemInfo decode_item(int item, const PrefillArgs &a)
 {
     ItemInfo x;
     x.pair = item % a.npairs;
     x.row = item / a.npairs;
-    decode_row<kVarlen>(x.row, a, x);
+    decode_row<kVarlen, kL>(x.row, a, x);
+    if (kL == 1)
+        x.layer = 0;
     return x;
 }
 
@@ -675,7 +685,7 @@ __device__ __forceinline__ void pair_producer(const TmapTable<kL> &tm, const Pre
         }
         if (item < 0)
             break;
-        const ItemInfo x = decode_item<kVarlen>(item, a);
+        const ItemInfo x = decode_item<kVarlen, kL>(item, a);
         const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
         if (N == 0)
             continue;
@@ -865,7 +875,7 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
             mbar_arrive_remote(lead_bar(&sm.item_empty[slot]));
         if (item < 0)
             break;
-        const ItemInfo x = decode_item<kVarlen>(item, a);
+        const ItemInfo x = decode_item<kVarlen, kL>(item, a);
         bool store;
         const int qh = item_head(x, static_cast<int>(c.rank), a, store);
         const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
@@ -1014,7 +1024,9 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         // the row's sequence, length and offsets, decoded again here so that
         // none of them stays live across the tile loop
         RowInfo e;
-        decode_row<kVarlen>(x.row, a, e);
+        decode_row<kVarlen, kL>(x.row, a, e);
+        if (kL == 1)
+            e.layer = 0;
         const bool row_ok = store && i < e.S &&
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
                             in_bounds(qh, a.Hq, err);
@@ -1206,6 +1218,7 @@ static ea_status prefill_common(int B, int S, int Hq, int Hkv, int d, const uint
     a.m[0] = m;
     a.block_mask[0] = block_mask;
     a.n_layers = 1;
+    a.n_sort_groups = 1;
     a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
     a.items = reinterpret_cast<uint32_t *>(ws + L.items);
     a.hdr = reinterpret_cast<ea_ws_header *>(ws);
@@ -1454,6 +1467,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.m[0] = m;
     a.block_mask[0] = block_mask;
     a.n_layers = 1;
+    a.n_sort_groups = 1;
     a.costs = reinterpret_cast<int32_t *>(ws + L.costs);
     a.items = reinterpret_cast<uint32_t *>(ws + L.items);
     a.hdr = reinterpret_cast<ea_ws_header *>(ws);
@@ -1492,6 +1506,11 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     a.total_tokens = total_tokens;
     a.wait_timeout_ns = EA_WAIT_TIMEOUT_NS;
     a.test_skip_load = -1;
+    // the queue sequence by sequence when the planner's histogram holds it
+    if (static_cast<int64_t>(B) * (a.nB + 1) + 1 <= kMaxSortBins) {
+        a.sort_group = 2;
+        a.n_sort_groups = B;
+    }
 
     ea_status s;
     if ((s = ensure_attributes()) != EA_OK)
@@ -1501,7 +1520,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_varlen(
     varlen_setup_kernel<<<1, 1024, 0, st>>>(a);
     plan_costs_kernel<<<static_cast<unsigned>(ceil_div(a.n_rows, warps_per_cta)),
                         warps_per_cta * 32, 0, st>>>(a);
-    plan_sort_kernel<<<1, 1024, sizeof(int) * (a.nB + 2), st>>>(a);
+    plan_sort_kernel<<<1, 1024, sizeof(int) * (a.n_sort_groups * (a.nB + 1) + 1), st>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return EA_ERR_CUDA;
     return launch_attend(tm, a, stream);
@@ -1627,7 +1646,10 @@ extern "C" ea_status ea_hybrid_attn_prefill_layers(const ea_prefill_layer *layer
         return EA_ERR_UNSUPPORTED;
     a.n_rows = static_cast<uint32_t>(rows);
     a.n_items = static_cast<uint32_t>(rows * a.npairs);
-    a.sort_by_layer = static_cast<int64_t>(n_layers) * (a.nB + 1) + 1 <= kMaxSortBins;
+    if (static_cast<int64_t>(n_layers) * (a.nB + 1) + 1 <= kMaxSortBins) {
+        a.sort_group = 1;
+        a.n_sort_groups = n_layers;
+    }
     a.visited = nullptr;
     a.visited_bits = 0;
     bool any_mask = false, v8 = o_str[0] % 16 == 0 && o_str[1] % 16 == 0 && o_str[2] % 16 == 0;
@@ -1658,7 +1680,7 @@ extern "C" ea_status ea_hybrid_attn_prefill_layers(const ea_prefill_layer *layer
     const int warps_per_cta = 8;
     plan_costs_kernel<<<static_cast<unsigned>(ceil_div(a.n_rows, warps_per_cta)), warps_per_cta * 32, 0,
                         st>>>(a);
-    plan_sort_kernel<<<1, 1024, sizeof(int) * ((a.sort_by_layer ? n_layers : 1) * (a.nB + 1) + 1), st>>>(a);
+    plan_sort_kernel<<<1, 1024, sizeof(int) * (a.n_sort_groups * (a.nB + 1) + 1), st>>>(a);
     if (cudaGetLastError() != cudaSuccess)
         return EA_ERR_CUDA;
     return launch_attend(tm, a, stream);
