@@ -1166,6 +1166,8 @@ def run_serial_sweep(args, dev):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     for S in args.serial_lengths:
+        clocks = ClockSampler(dev.index or 0)
+        clocks.start()
         Q, K, V = wl.qkv(B, S, Hq, Hkv, d, seed=0, device=dev)
         O = torch.empty_like(Q)
         LSE = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
@@ -1201,6 +1203,8 @@ def run_serial_sweep(args, dev):
                               "omega_msr_layer": n_sa / Hkv, "fused_ms": round(res["fused"], 4),
                               "serial_ms": round(res["serial"], 4),
                               "speedup": round(res["serial"] / res["fused"], 3)}), flush=True)
+        print(json.dumps({"comparison": "fused vs serial dispatch", "seq_len": S,
+                          "clocks": clocks.stop()}), flush=True)
         del Q, K, V, O, LSE
 
 
