@@ -31,12 +31,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "ea_device.cuh"
 #include "ea_internal.h"
 
 namespace ea {
 
 constexpr int kDecKeys = 64;                           // keys per tile
+constexpr int kDecSplitMaxKeys = 128;                  // units up to this many keys: P V in two parts
 constexpr int kDecStages = 6;
 constexpr int kDecHalfBytes = kDecKeys * 128;          // one 64-dim swizzled box: 8 KB
 constexpr int kDecTileBytes = 2 * kDecHalfBytes;       // K or V of one tile: 16 KB
@@ -307,6 +310,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(DecodeArgs a)
 // [v_begin, v_end), tile v at key 128 * list[v / 2] + 64 * (v % 2).
 struct ChunkInfo {
     int b, h, v_begin, v_end;
+    int kept;                 // the unit's kept keys (whole tiles of a BLOCK unit)
     KeySegs ks;
     int a_tiles, b_begin, n_tiles;
     int TA, TB;
@@ -323,9 +327,11 @@ __device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
     unit_keys(a, ci.b, ci.h, ci.ks);
     const int ns = a.unit_splits[u];
     ci.list = nullptr;
+    ci.kept = ci.ks.n;
     if (ci.ks.blk >= 0) {
         ci.list = a.blk_list + static_cast<int64_t>(u) * a.nBm;
         const int nt = block_tiles(a, u, ci.ks);
+        ci.kept = nt * kDecKeys;
         const int len = (nt + ns - 1) / ns;
         ci.v_begin = min(sp * len, nt);
         ci.v_end = min(ci.v_begin + len, nt);
@@ -544,6 +550,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (c < 0)
             break;
         const ChunkInfo ci = chunk_info(a, c);
+        // A unit that keeps few keys takes P V in two bf16 parts: with a handful
+        // of keys one probability's 2^-9 rounding error would reach O undiluted.
+        const bool split = ci.kept <= kDecSplitMaxKeys;
         // Q as the A operand: rows r < g are query heads, the rest zero
         uint32_t qa[8][2];   // per head-dim step j: (r, 16j + 2q..), (r, 16j + 8 + 2q..)
         {
@@ -565,89 +574,105 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 o[n][e] = 0.f;
         float m_run = NEG_INF, l_part = 0.f;   // row r statistics (l summed over the quad at the end)
 
-        for (int t = 0; t < ci.n_tiles; ++t) {
-            const int s = consumed % kDecStages;
-            if (!mbar_wait(&sm.full[s], (consumed / kDecStages) & 1, abort, &a.hdr->error))
-                return;  // timed out (error word set) or another warp did
-            ++consumed;
-            int key0, nv;
-            tile_rows(a, ci, t, key0, nv);
-            const uint32_t kb = smem_u32(sm.k[s]), vb = smem_u32(sm.v[s]);
-            const int kw = warp * 16;   // this warp's first key in the tile
+        // the tile loop, compiled twice: with P's remainder (rare units) and without
+        auto tiles = [&](auto split_tag) -> bool {
+            constexpr bool kSplit = decltype(split_tag)::value;
+            for (int t = 0; t < ci.n_tiles; ++t) {
+                const int s = consumed % kDecStages;
+                if (!mbar_wait(&sm.full[s], (consumed / kDecStages) & 1, abort, &a.hdr->error))
+                    return false;  // timed out (error word set) or another warp did
+                ++consumed;
+                int key0, nv;
+                tile_rows(a, ci, t, key0, nv);
+                const uint32_t kb = smem_u32(sm.k[s]), vb = smem_u32(sm.v[s]);
+                const int kw = warp * 16;   // this warp's first key in the tile
 
-            // S = Q K^T for keys kw..kw+15 (two 8-key blocks)
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
-                const int krow = kw + (lane >> 4) * 8 + (lane & 7);   // key this lane addresses
-                const int csel = (lane >> 3) & 1;                      // 0: first 8 dims, 1: next 8
+                // S = Q K^T for keys kw..kw+15 (two 8-key blocks)
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const int krow = kw + (lane >> 4) * 8 + (lane & 7);   // key this lane addresses
+                    const int csel = (lane >> 3) & 1;                      // 0: first 8 dims, 1: next 8
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t b00, b01, b10, b11;
-                    ldsm_x4(kb + sw_off(krow, 2 * j + csel), b00, b01, b10, b11);
-                    mma_bf16(sc[0], qa[j][0], 0u, qa[j][1], 0u, b00, b01);
-                    mma_bf16(sc[1], qa[j][0], 0u, qa[j][1], 0u, b10, b11);
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t b00, b01, b10, b11;
+                        ldsm_x4(kb + sw_off(krow, 2 * j + csel), b00, b01, b10, b11);
+                        mma_bf16(sc[0], qa[j][0], 0u, qa[j][1], 0u, b00, b01);
+                        mma_bf16(sc[1], qa[j][0], 0u, qa[j][1], 0u, b10, b11);
+                    }
                 }
-            }
-            // online softmax over this warp's 16 keys, row r
-            float x[4] = {sc[0][0] * a.scale_log2, sc[0][1] * a.scale_log2,
-                          sc[1][0] * a.scale_log2, sc[1][1] * a.scale_log2};
-            const int kcol[4] = {kw + 2 * qd, kw + 2 * qd + 1, kw + 8 + 2 * qd, kw + 9 + 2 * qd};
-            if (a.page_size && !ci.list) {
-                // aligned tile: keep key k iff (k < sink end or k >= window
-                // start) and k < L
-                const int L = ci.ks.w0 + (ci.ks.n - ci.ks.n0);
+                // online softmax over this warp's 16 keys, row r
+                float x[4] = {sc[0][0] * a.scale_log2, sc[0][1] * a.scale_log2,
+                              sc[1][0] * a.scale_log2, sc[1][1] * a.scale_log2};
+                const int kcol[4] = {kw + 2 * qd, kw + 2 * qd + 1, kw + 8 + 2 * qd, kw + 9 + 2 * qd};
+                if (a.page_size && !ci.list) {
+                    // aligned tile: keep key k iff (k < sink end or k >= window
+                    // start) and k < L
+                    const int L = ci.ks.w0 + (ci.ks.n - ci.ks.n0);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = key0 + kcol[e];
+                        if (!((k < ci.ks.n0 || k >= ci.ks.w0) && k < L))
+                            x[e] = NEG_INF;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (kcol[e] >= nv)
+                            x[e] = NEG_INF;
+                }
+                float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float m_new = fmaxf(m_run, mx);
+                if (m_new > m_run) {
+                    const float f = m_run == NEG_INF ? 0.f : ex2(m_run - m_new);
+                    l_part *= f;
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) {
+                        o[n][0] *= f;
+                        o[n][1] *= f;
+                    }
+                    m_run = m_new;
+                }
+                const float mb = m_run == NEG_INF ? 0.f : m_run;
+                float p[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int k = key0 + kcol[e];
-                    if (!((k < ci.ks.n0 || k >= ci.ks.w0) && k < L))
-                        x[e] = NEG_INF;
+                    p[e] = ex2(x[e] - mb);
+                    l_part += p[e];
                 }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (kcol[e] >= nv)
-                        x[e] = NEG_INF;
-            }
-            float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
-            if (m_new > m_run) {
-                const float f = m_run == NEG_INF ? 0.f : ex2(m_run - m_new);
-                l_part *= f;
-#pragma unroll
-                for (int n = 0; n < 16; ++n) {
-                    o[n][0] *= f;
-                    o[n][1] *= f;
+                const uint32_t pa0 = pack_bf16x2(p[0], p[1]);   // (r, keys 2q..)
+                const uint32_t pa2 = pack_bf16x2(p[2], p[3]);   // (r, keys 8 + 2q..)
+                uint32_t pr0 = 0u, pr2 = 0u;                     // P - bf16(P), rounded to bf16
+                if constexpr (kSplit) {
+                    pr0 = pack_bf16x2(p[0] - __uint_as_float(pa0 << 16), p[1] - __uint_as_float(pa0 & 0xffff0000u));
+                    pr2 = pack_bf16x2(p[2] - __uint_as_float(pa2 << 16), p[3] - __uint_as_float(pa2 & 0xffff0000u));
                 }
-                m_run = m_new;
-            }
-            const float mb = m_run == NEG_INF ? 0.f : m_run;
-            float p[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                p[e] = ex2(x[e] - mb);
-                l_part += p[e];
-            }
-            const uint32_t pa0 = pack_bf16x2(p[0], p[1]);   // (r, keys 2q..)
-            const uint32_t pa2 = pack_bf16x2(p[2], p[3]);   // (r, keys 8 + 2q..)
 
-            // O += P V: 16 head-dim blocks of 8, two per ldmatrix
-            {
-                const int vrow = kw + ((lane >> 3) & 1) * 8 + (lane & 7);
-                const int cadd = lane >> 4;
+                // O += P V: 16 head-dim blocks of 8, two per ldmatrix
+                {
+                    const int vrow = kw + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int cadd = lane >> 4;
 #pragma unroll
-                for (int n = 0; n < 16; n += 2) {
-                    uint32_t b00, b01, b10, b11;
-                    ldsm_x4_t(vb + sw_off(vrow, n + cadd), b00, b01, b10, b11);
-                    mma_bf16(o[n], pa0, 0u, pa2, 0u, b00, b01);
-                    mma_bf16(o[n + 1], pa0, 0u, pa2, 0u, b10, b11);
+                    for (int n = 0; n < 16; n += 2) {
+                        uint32_t b00, b01, b10, b11;
+                        ldsm_x4_t(vb + sw_off(vrow, n + cadd), b00, b01, b10, b11);
+                        mma_bf16(o[n], pa0, 0u, pa2, 0u, b00, b01);
+                        mma_bf16(o[n + 1], pa0, 0u, pa2, 0u, b10, b11);
+                        if constexpr (kSplit) {
+                            mma_bf16(o[n], pr0, 0u, pr2, 0u, b00, b01);
+                            mma_bf16(o[n + 1], pr0, 0u, pr2, 0u, b10, b11);
+                        }
+                    }
                 }
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&sm.empty[s]);
             }
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&sm.empty[s]);
-        }
+            return true;
+        };
+        if (!(split ? tiles(std::true_type{}) : tiles(std::false_type{})))
+            return;
 
         // per-warp results of the rows r < g -> shared memory, then merge warps
         l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);

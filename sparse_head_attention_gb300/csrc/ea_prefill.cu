@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "ea_device.cuh"
 #include "ea_internal.h"
@@ -220,6 +221,28 @@ __device__ __forceinline__ bool tile_is_full(int mode, int qb, int kb, int sink,
         return (kb + 1) * T <= sink || (qb - kb) * T + T - 1 < window;
     return true;
 }
+
+// Keys kept by the first (fewest-keys) query row of block qb, for a row with
+// N visited tiles: FULL keeps i + 1, SSA the sink keys up to i plus the keys of
+// the window not already counted, BLOCK whole kept tiles plus i + 1 - kb*T of
+// the diagonal.  Every later row of the block keeps at least as many.
+__device__ __forceinline__ int first_row_keys(int mode, int qb, int sink, int window, int N,
+                                              bool diag_kept)
+{
+    const int i = qb * T;
+    if (mode == EA_FULL)
+        return i + 1;
+    if (mode == EA_SSA) {
+        const int n_sk = i + 1 < sink ? i + 1 : sink;
+        const int w_lo = i - window + 1 > sink ? i - window + 1 : sink;
+        return n_sk + (i + 1 - w_lo > 0 ? i + 1 - w_lo : 0);
+    }
+    return diag_kept ? (N - 1) * T + 1 : N * T;
+}
+
+// Rows that keep at most one tile's worth of keys take the P V product in two
+// bf16 parts (P's rounding and the remainder), see pair_softmax.
+constexpr int kSplitMaxKeys = T;
 
 // ------------------------------------------------------------ planner
 // One warp per (b, KV head, q block) row: number of visited key tiles, or -1
@@ -476,6 +499,7 @@ struct __align__(1024) PairSmem {
     float red_max[2][2][T];        // [tile parity][warpgroup][row]
     float red_l[2][2][T];          // [item parity][warpgroup][row]
     int item[2];
+    int pv_split;                  // the current item's P V products include P's remainder
     uint32_t tmem_base;
     int abort;
 };
@@ -822,25 +846,44 @@ __device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uin
                     tc_commit_pair(&sm.q_empty[qbuf], kBothCtas);
             }
         } else {
-            for (int n = 0; n < N && ok; ++n) {
-                const uint32_t jj = j + n, b = jj % 3, vs = jj % kVSlots;
-                if (!pwait1(&sm.p_ready[b], (jj / 3) & 1, c) ||
-                    !pwait1(&sm.kv_full[vs], (jj / kVSlots) & 1, c)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t vaddr = smem_u32(sm.v[vs]);
-                const uint32_t tp = tmem + kColS + 128 * b;
+            // the item's first P: rank 0's softmax wrote the split flag before it
+            if (!pwait1(&sm.p_ready[j % 3], (j / 3) & 1, c))
+                break;
+            const bool split = *reinterpret_cast<volatile int *>(&sm.pv_split) != 0;
+            // the tile loop, compiled twice: with the remainder products and without
+            auto tiles = [&](auto split_tag) {
+                constexpr bool kSplit = decltype(split_tag)::value;
+                for (int n = 0; n < N && ok; ++n) {
+                    const uint32_t jj = j + n, b = jj % 3, vs = jj % kVSlots;
+                    if ((n > 0 && !pwait1(&sm.p_ready[b], (jj / 3) & 1, c)) ||
+                        !pwait1(&sm.kv_full[vs], (jj / kVSlots) & 1, c)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t vaddr = smem_u32(sm.v[vs]);
+                    const uint32_t tp = tmem + kColS + 128 * b;
 #pragma unroll
-                for (int k = 0; k < T / 16; ++k)
-                    tc_mma_ts_pair(tmem + kColO, tp + (k < 4 ? 8 * k : 64 + 8 * (k - 4)),
-                                   sdesc_sw128(vaddr + k * 2048, kHalf, 1024), kIdescPV2,
-                                   (n > 0 || k > 0) ? 1u : 0u);
-                tc_commit_pair(&sm.v_empty[vs], kBothCtas);
-                if (n == N - 1)
-                    tc_commit_pair(&sm.o_done, kBothCtas);
-            }
+                    for (int k = 0; k < T / 16; ++k)
+                        tc_mma_ts_pair(tmem + kColO, tp + (k < 4 ? 8 * k : 64 + 8 * (k - 4)),
+                                       sdesc_sw128(vaddr + k * 2048, kHalf, 1024), kIdescPV2,
+                                       (n > 0 || k > 0) ? 1u : 0u);
+                    // few-key rows: the remainder P - bf16(P), 32 columns further on
+                    if constexpr (kSplit) {
+#pragma unroll
+                        for (int k = 0; k < T / 16; ++k)
+                            tc_mma_ts_pair(tmem + kColO, tp + (k < 4 ? 32 + 8 * k : 96 + 8 * (k - 4)),
+                                           sdesc_sw128(vaddr + k * 2048, kHalf, 1024), kIdescPV2, 1u);
+                    }
+                    tc_commit_pair(&sm.v_empty[vs], kBothCtas);
+                    if (n == N - 1)
+                        tc_commit_pair(&sm.o_done, kBothCtas);
+                }
+            };
+            if (split)
+                tiles(std::true_type{});
+            else
+                tiles(std::false_type{});
         }
         j += N;
     }
@@ -887,126 +930,172 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         if (mode == EA_BLOCK && N > 0)
             diag_kept = in_bounds(x.mask_row + x.qb, mask_limit(a), err) &&
                         a.block_mask[x.layer][x.mask_row + x.qb] != 0;
+        // Rows that keep few keys (the first query blocks, small sink and
+        // window, a lone diagonal block) take P V in two bf16 parts: with a
+        // handful of keys one probability's 2^-9 rounding error reaches O
+        // undiluted, and would add up to 2^-9 |O| to the output's own rounding.
+        const bool split = N > 0 && first_row_keys(mode, x.qb, a.sink, a.window, N, diag_kept) <= kSplitMaxKeys;
+        if (warp == 0 && lane == 0 && c.rank == 0)
+            sm.pv_split = split ? 1 : 0;   // read by the PV issuer after this item's first P
         const int i = x.qb * T + r;
         float m_run = NEG_INF, l_run = 0.f;
         bool ok = true;
 
-        for (int n = 0; n < N; ++n) {
-            const uint32_t jj = j + n;
-            const uint32_t b = jj % 3;
-            int kb;
-            if (mode == EA_BLOCK)
-                kb = (n == N - 1 && diag_kept) ? x.qb : -1;  // only the diagonal needs its index
-            else
-                kb = seq_kb(mode, n, n_sink, kb_lo);
-            if (!pwait(&sm.s_full[b], (jj / 3) & 1, c)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t tS = tmem + lane_base + kColS + 128 * b + 64 * wg;
-            uint32_t s[64];
-            tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-            tmem_wait_ld();
-
-            // mask edge tiles only: key j0 + c is kept when c <= hi (causal)
-            // and, for SSA, when c < sk (sink) or c > lo (inside the window);
-            // one keep word per 32 columns, built from three prefix masks
-            const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
-            if (edge) {
-                const int j0 = kb * T;
-                const int hi = i - j0;
-                int sk = -1, lo = -1;
-                if (mode == EA_SSA) {
-                    sk = a.sink - j0;
-                    lo = i - a.window - j0;
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int co = 64 * wg + 32 * q;
-                    const uint32_t w = low_bits(hi + 1 - co) & (low_bits(sk - co) | ~low_bits(lo + 1 - co));
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc)
-                        if (!((w >> cc) & 1u))
-                            s[32 * q + cc] = __float_as_uint(NEG_INF);
-                }
-            }
-            // partial row max over this warpgroup's 64 columns (eight 3-input
-            // chains), then the row's max with the other warpgroup's
-            float mxa[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                mxa[k] = max3f(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]), NEG_INF);
-#pragma unroll
-            for (int cc = 16; cc < 64; cc += 16)
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    mxa[k] = max3f(mxa[k], __uint_as_float(s[cc + 2 * k]), __uint_as_float(s[cc + 2 * k + 1]));
-            const float pm = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
-                                   fmaxf(mxa[6], mxa[7]));
-            sm.red_max[jj & 1][wg][r] = pm;
-            named_bar_sync(bar_id, 64);
-            float mx = fmaxf(pm, sm.red_max[jj & 1][wg ^ 1][r]);
-            mx *= a.scale_log2;
-            const float m_new = fmaxf(m_run, mx);
-            float factor = 1.f;
-            bool rescale_o = false;
-            if (m_new > m_run + kRescaleThreshold) {
-                if (m_run > NEG_INF) {
-                    factor = ex2(m_run - m_new);
-                    l_run *= factor;
-                    rescale_o = n > 0;
-                }
-                m_run = m_new;
-            }
-            const float mb = m_run > NEG_INF ? m_run : 0.f;
-            // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
-            // the row sum in four packed accumulators, P packed to bf16 pairs
-            // in place (s[c/2] once s[c], s[c+1] are consumed)
-            const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-            const uint64_t nm2 = f2_pack(-mb, -mb);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 2) {
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])), sc2, nm2),
-                          x0, x1);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
-                s[cc >> 1] = pack_bf16x2(p0, p1);
-            }
-            float l0, l1, l2, l3;
-            f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
-            f2_unpack(f2_add(acc[2], acc[3]), l2, l3);
-            l_run += (l0 + l1) + (l2 + l3);
-
-            // O rescale: PV of the previous tile must have completed
-            if (__any_sync(0xffffffffu, rescale_o)) {
-                if (!pwait(&sm.v_empty[(jj - 1) % kVSlots], ((jj - 1) / kVSlots) & 1, c)) {
+        // the tile loop, compiled twice: with P's remainder (rare items) and without
+        auto tiles = [&](auto split_tag) {
+            constexpr bool kSplit = decltype(split_tag)::value;
+            for (int n = 0; n < N; ++n) {
+                const uint32_t jj = j + n;
+                const uint32_t b = jj % 3;
+                int kb;
+                if (mode == EA_BLOCK)
+                    kb = (n == N - 1 && diag_kept) ? x.qb : -1;  // only the diagonal needs its index
+                else
+                    kb = seq_kb(mode, n, n_sink, kb_lo);
+                if (!pwait(&sm.s_full[b], (jj / 3) & 1, c)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-#pragma unroll 1
-                for (int ch = 0; ch < 2; ++ch) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + ch * 32, o);
-                    tmem_wait_ld();
+                const uint32_t tS = tmem + lane_base + kColS + 128 * b + 64 * wg;
+                uint32_t s[64];
+                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tmem_wait_ld();
+
+                // mask edge tiles only: key j0 + c is kept when c <= hi (causal)
+                // and, for SSA, when c < sk (sink) or c > lo (inside the window);
+                // one keep word per 32 columns, built from three prefix masks
+                const bool edge = kb >= 0 && !tile_is_full(mode, x.qb, kb, a.sink, a.window);
+                if (edge) {
+                    const int j0 = kb * T;
+                    const int hi = i - j0;
+                    int sk = -1, lo = -1;
+                    if (mode == EA_SSA) {
+                        sk = a.sink - j0;
+                        lo = i - a.window - j0;
+                    }
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc)
-                        o[cc] = __float_as_uint(__uint_as_float(o[cc]) * factor);
-                    tmem_st32(tO + ch * 32, o);
+                    for (int q = 0; q < 2; ++q) {
+                        const int co = 64 * wg + 32 * q;
+                        const uint32_t w = low_bits(hi + 1 - co) & (low_bits(sk - co) | ~low_bits(lo + 1 - co));
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc)
+                            if (!((w >> cc) & 1u))
+                                s[32 * q + cc] = __float_as_uint(NEG_INF);
+                    }
                 }
+                // partial row max over this warpgroup's 64 columns (eight 3-input
+                // chains), then the row's max with the other warpgroup's
+                float mxa[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mxa[k] = max3f(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]), NEG_INF);
+#pragma unroll
+                for (int cc = 16; cc < 64; cc += 16)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        mxa[k] = max3f(mxa[k], __uint_as_float(s[cc + 2 * k]), __uint_as_float(s[cc + 2 * k + 1]));
+                const float pm = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
+                                       fmaxf(mxa[6], mxa[7]));
+                sm.red_max[jj & 1][wg][r] = pm;
+                named_bar_sync(bar_id, 64);
+                float mx = fmaxf(pm, sm.red_max[jj & 1][wg ^ 1][r]);
+                mx *= a.scale_log2;
+                const float m_new = fmaxf(m_run, mx);
+                float factor = 1.f;
+                bool rescale_o = false;
+                if (m_new > m_run + kRescaleThreshold) {
+                    if (m_run > NEG_INF) {
+                        factor = ex2(m_run - m_new);
+                        l_run *= factor;
+                        rescale_o = n > 0;
+                    }
+                    m_run = m_new;
+                }
+                const float mb = m_run > NEG_INF ? m_run : 0.f;
+                // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
+                // the row sum in four packed accumulators, P packed to bf16 pairs
+                // in place (s[c/2] once s[c], s[c+1] are consumed)
+                const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+                const uint64_t nm2 = f2_pack(-mb, -mb);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2) {
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(s[cc]), __uint_as_float(s[cc + 1])), sc2, nm2),
+                              x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
+                    s[cc >> 1] = pack_bf16x2(p0, p1);
+                }
+                float l0, l1, l2, l3;
+                f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
+                f2_unpack(f2_add(acc[2], acc[3]), l2, l3);
+                l_run += (l0 + l1) + (l2 + l3);
+
+                // O rescale: PV of the previous tile must have completed
+                if (__any_sync(0xffffffffu, rescale_o)) {
+                    if (!pwait(&sm.v_empty[(jj - 1) % kVSlots], ((jj - 1) / kVSlots) & 1, c)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int ch = 0; ch < 2; ++ch) {
+                        uint32_t o[32];
+                        tmem_ld32(tO + ch * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc)
+                            o[cc] = __float_as_uint(__uint_as_float(o[cc]) * factor);
+                        tmem_st32(tO + ch * 32, o);
+                    }
+                }
+                if constexpr (kSplit) {
+                    // P again from S (same operations, same values), and its
+                    // remainder P - bf16(P) rounded to bf16 over the other 32 columns
+                    // (read by a second P V product; an error of 2^-9 of the
+                    // remainder, 2^-17 of P, is left)
+#pragma unroll 1
+                    for (int q = 1; q >= 0; --q) {   // columns 32..63 first: rem lands there
+                        uint32_t t[32], rem[16];
+                        tmem_ld32(tS + 32 * q, t);
+                        tmem_wait_ld();
+                        uint32_t w = 0xffffffffu;
+                        if (edge) {
+                            const int j0 = kb * T, co = 64 * wg + 32 * q;
+                            const int sk = mode == EA_SSA ? a.sink - j0 : -1;
+                            const int lo = mode == EA_SSA ? i - a.window - j0 : -1;
+                            w = low_bits(i - j0 + 1 - co) & (low_bits(sk - co) | ~low_bits(lo + 1 - co));
+                        }
+#pragma unroll
+                        for (int cc = 0; cc < 32; cc += 2) {
+                            const float s0 = (w >> cc) & 1u ? __uint_as_float(t[cc]) : NEG_INF;
+                            const float s1 = (w >> (cc + 1)) & 1u ? __uint_as_float(t[cc + 1]) : NEG_INF;
+                            float x0, x1;
+                            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
+                            const float p0 = ex2(x0), p1 = ex2(x1);
+                            const uint32_t hi = pack_bf16x2(p0, p1);
+                            rem[cc >> 1] = pack_bf16x2(p0 - __uint_as_float(hi << 16),
+                                                       p1 - __uint_as_float(hi & 0xffff0000u));
+                        }
+                        tmem_st16(tS + 32 + 16 * q, rem);
+                    }
+                }
+                // P (bf16 pairs) over the first 32 of this warpgroup's S columns
+                tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_remote(lead_bar(&sm.p_ready[b]));
             }
-            // P (bf16 pairs) over the first 32 of this warpgroup's S columns
-            tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive_remote(lead_bar(&sm.p_ready[b]));
-        }
+        };
+        if (split)
+            tiles(std::true_type{});
+        else
+            tiles(std::false_type{});
         if (!ok)
             break;
         j += N;

@@ -92,6 +92,17 @@ def qkv(B, S, Hq, Hkv, d, seed=0, device="cpu"):
     return Q, K, V
 
 
+def offset_values(B, S, Hkv, d, seed=0, lo=2.2, hi=3.8, device="cpu"):
+    """V [B, S, Hkv, d] bf16 with |v| uniform in [lo, hi) and one sign per
+    (b, KV head, dim) for all positions: any convex combination of a head's
+    values then has |O| in [lo, hi) too (a stress input for the output's
+    absolute error, which grows with |O|)."""
+    g = _gen(seed, device)
+    mag = lo + (hi - lo) * torch.rand((B, S, Hkv, d), generator=g, device=device)
+    sign = torch.where(torch.rand((B, 1, Hkv, d), generator=g, device=device) < 0.5, -1.0, 1.0)
+    return (mag * sign).to(torch.bfloat16)
+
+
 def routing_from_sa_heads(B: int, Hkv: int, sa_heads, fa_impl=FULL, sa_impl=SSA):
     """(r, m) uint8 [B, Hkv] for a fixed set of SA heads (same in every batch row)."""
     r = torch.zeros((B, Hkv), dtype=torch.uint8)

@@ -18,8 +18,9 @@ def pytest_collection_modifyitems(config, items):
 
 
 def pytest_terminal_summary(terminalreporter):
-    # The O tolerance departs from a flat 1e-2 by half a bf16 step (see
-    # gpu_helpers.assert_close): report how many compared elements used it.
+    # The O tolerance departs from a flat 1e-2 by half a bf16 step where
+    # |O| >= 4 (see gpu_helpers.assert_close): report how many compared
+    # elements used it.
     helpers = sys.modules.get("gpu_helpers")
     if helpers is None or not helpers.FLAT_EXCESS:
         return

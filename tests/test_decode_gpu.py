@@ -76,6 +76,26 @@ def test_block_heads_match_oracle(dev, num_splits):
     assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "splits=%d" % num_splits)
 
 
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_few_kept_keys_with_large_values(dev, num_splits):
+    # Units keeping 1 to 128 keys, |V| in [2.2, 3.8) with one sign per (head,
+    # dim): |O| stays in [2, 4), where correct rounding alone errs by up to
+    # 0.0078, and a P rounded to bf16 would add up to 2^-9 |O|.  Units of at
+    # most 128 keys take P V in two bf16 parts: every element within a flat 1e-2.
+    seqlens = [1, 2, 3, 5, 17, 64, 100, 128]
+    B, Hq, Hkv, Lmax, sink, window = len(seqlens), 8, 2, 128, 2, 3
+    cfg = wl.DecodeConfig("t", B=B, Hq=Hq, Hkv=Hkv, d=128, L=Lmax, sink=sink, window=window)
+    q, Kc, _, sl = wl.decode_inputs(cfg, seqlens=seqlens)
+    Vc = wl.offset_values(B, Lmax, Hkv, 128, seed=43)
+    modes = np.array([[FULL, SSA], [SSA, BLOCK], [BLOCK, FULL]] * 3, np.uint8)[:B]
+    bm = np.ones((B, Hkv, 1, 1), np.uint8)
+    O, LSE = run(dev, q, Kc, Vc, sl, modes, sink, window, num_splits, bm=bm)
+    Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=sink, window=window, block_mask=bm)
+    assert np.abs(Oref).min() >= 2.0
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
+                 "few keys, splits=%d" % num_splits, flat=True)
+
+
 def test_block_decode_equals_last_prefill_row_on_gpu(dev):
     B, S, Hq, Hkv = 1, 1500, 8, 2
     Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=14)

@@ -96,6 +96,37 @@ def test_block_masks_with_empty_rows(dev):
         oracle.visited(B, S, Hkv, np.array(modes, np.uint8), sink=64, window=300, block_mask=bm))
 
 
+FEW_KEY_CASES = [
+    # S, modes, sink, window: every query block's first row keeps at most 128 keys
+    (128, [[SSA, FULL]], 0, 3),      # FA rows keep 1..128 keys, SSA rows 1..3
+    (300, [[SSA, SSA]], 2, 2),       # two sink keys plus a window of 2
+    (300, [[BLOCK, SSA]], 1, 1),     # diagonal block only; sink + window of 1
+]
+
+
+@pytest.mark.parametrize("S,modes,sink,window", FEW_KEY_CASES)
+def test_few_kept_keys_with_large_values(dev, S, modes, sink, window):
+    # |V| in [2.2, 3.8) with one sign per (head, dim), so |O| stays in [2, 4),
+    # where a correctly rounded bf16 output errs by at most 2^-7 = 0.0078.
+    # With one to a few kept keys a P rounded to bf16 (2^-9 relative) would
+    # add up to 2^-9 |O| more and cross 1e-2 (an fp64 model of that arithmetic
+    # puts 464 to 1063 elements of these cases above it); rows keeping at most
+    # 128 keys take P V in two bf16 parts, which keeps every element within a
+    # flat 1e-2.
+    B, Hq, Hkv = 1, 4, 2
+    Q, K, _ = wl.qkv(B, S, Hq, Hkv, 128, seed=41)
+    V = wl.offset_values(B, S, Hkv, 128, seed=42)
+    nB = (S + 127) // 128
+    bm = np.zeros((B, Hkv, nB, nB), np.uint8)
+    bm[:, :, np.arange(nB), np.arange(nB)] = 1
+    O, LSE, _ = run(dev, Q, K, V, modes, sink, window, bm=bm)
+    Oref, Lref = oracle.prefill_full(Q, K, V, np.array(modes, np.uint8), sink=sink, window=window,
+                                     block_mask=bm)
+    assert np.abs(Oref).min() >= 2.0
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
+                 "few keys S=%d %s sink=%d window=%d" % (S, modes, sink, window), flat=True)
+
+
 def test_strided_views_and_concatenation(dev):
     # Q, K, V as views of one packed projection [B, S, Hq + 2 Hkv, d]; O written
     # into the first Hq heads of a wider buffer (eq. 3 concatenation in place).
