@@ -484,6 +484,21 @@ constexpr uint32_t kIdescPV2 = idesc_bf16_f32(256, 128, false, true);   // V is 
 constexpr uint16_t kBothCtas = 3;             // multicast mask: both CTAs of the pair
 constexpr float kRescaleThreshold = 8.0f;     // log2 units: rescale when max grows > 2^8
 
+// A queued item as rank 0's producer publishes it to both CTAs: the queue
+// entry and, read once from global memory there, what the consumers need of it.
+struct ItemMeta {
+    int item;        // queue entry (row * npairs + pair), or -1: the queue is drained
+    int info;        // visited tiles N | mode << 20 | diagonal kept << 22 | two-part P V << 23
+    int b, hq;       // batch row or sequence; KV head << 16 | query block
+    int tok0, len;   // the sequence's first token and length
+    int lp;          // layer << 16 | head pair
+    int row;         // planned row (item / npairs)
+};
+__device__ __forceinline__ int meta_n(int info) { return info & 0xFFFFF; }
+__device__ __forceinline__ int meta_mode(int info) { return (info >> 20) & 3; }
+__device__ __forceinline__ bool meta_diag(int info) { return (info >> 22) & 1; }
+__device__ __forceinline__ bool meta_split(int info) { return (info >> 23) & 1; }
+
 struct __align__(1024) PairSmem {
     uint8_t q[2][kTileBytes];      // this CTA's query tile, two items in flight
     uint8_t k[kKSlots][kHalf];     // this CTA's halves of the key tiles (64 keys)
@@ -496,10 +511,10 @@ struct __align__(1024) PairSmem {
     uint64_t o_done;
     uint64_t item_full[2], item_empty[2];
     uint64_t teardown;
+    uint64_t pv_issued;            // the PV issuer has issued an item's last product
     float red_max[2][2][T];        // [tile parity][warpgroup][row]
     float red_l[2][2][T];          // [item parity][warpgroup][row]
-    int item[2];
-    int pv_split;                  // the current item's P V products include P's remainder
+    ItemMeta meta[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -519,6 +534,57 @@ __device__ __forceinline__ ItemInfo decode_item(int item, const PrefillArgs &a)
     decode_row<kVarlen, kL>(x.row, a, x);
     if (kL == 1)
         x.layer = 0;
+    return x;
+}
+
+// The item's metadata, read from global memory (rank 0's producer, once per item).
+template <bool kVarlen, int kL>
+__device__ __forceinline__ ItemMeta make_meta(int item, const PrefillArgs &a, uint32_t *err)
+{
+    ItemMeta mt = {};
+    mt.item = item;
+    if (item < 0)
+        return mt;
+    const ItemInfo x = decode_item<kVarlen, kL>(item, a);
+    const int cost = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
+    const int N = cost > 0 ? cost : 0;
+    const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
+    bool diag_kept = false;
+    if (mode == EA_BLOCK && N > 0)
+        diag_kept = in_bounds(x.mask_row + x.qb, mask_limit(a), err) &&
+                    a.block_mask[x.layer][x.mask_row + x.qb] != 0;
+    // Rows that keep few keys (the first query blocks, small sink and window, a
+    // lone diagonal block) take P V in two bf16 parts: with a handful of keys
+    // one probability's 2^-9 rounding error reaches O undiluted, and would add
+    // up to 2^-9 |O| to the output's own rounding.
+    const bool split = N > 0 && first_row_keys(mode, x.qb, a.sink, a.window, N, diag_kept) <= kSplitMaxKeys;
+    mt.info = N | ((mode & 3) << 20) | (diag_kept ? 1 << 22 : 0) | (split ? 1 << 23 : 0);
+    mt.b = x.b;
+    mt.hq = (x.h << 16) | x.qb;
+    mt.tok0 = x.tok0;
+    mt.len = x.S;
+    mt.lp = (x.layer << 16) | x.pair;
+    mt.row = x.row;
+    return mt;
+}
+
+// An item's row from its metadata (no global memory, no division).  mask_row
+// is left for the producer to fill in where it needs it.
+template <bool kVarlen, int kL>
+__device__ __forceinline__ ItemInfo meta_item(const ItemMeta &mt, const PrefillArgs &a)
+{
+    ItemInfo x;
+    x.pair = mt.lp & 0xFFFF;
+    x.row = mt.row;
+    x.layer = kL == 1 ? 0 : static_cast<int>(static_cast<uint32_t>(mt.lp) >> 16);
+    x.b = mt.b;
+    x.h = static_cast<int>(static_cast<uint32_t>(mt.hq) >> 16);
+    x.qb = mt.hq & 0xFFFF;
+    x.tok0 = mt.tok0;
+    x.S = mt.len;
+    x.nB = kVarlen ? (x.S + T - 1) / T : a.nB;
+    x.tma_b = kVarlen ? 0 : x.b;
+    x.mask_row = 0;
     return x;
 }
 
@@ -680,40 +746,50 @@ __device__ __forceinline__ void pair_producer(const TmapTable<kL> &tm, const Pre
     for (int it = 0; ok; ++it) {
         const int slot = it & 1;
         const uint32_t par = (it >> 1) & 1;
-        int item = -1;
         if (lead) {
             if (!pwait(&sm.item_empty[slot], par ^ 1, c))
                 break;
             if (lane == 0) {
                 const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
-                item = x < n_items ? static_cast<int>(a.items[x]) : -1;
+                const int item = x < n_items ? static_cast<int>(a.items[x]) : -1;
                 // Every pair sees the empty queue exactly once; the last one
                 // resets the head so the same plan can feed another launch.
                 if (item < 0 && atomicAdd(&a.hdr->drained, 1u) == n_clusters - 1) {
                     a.hdr->work_counter = 0;
                     a.hdr->drained = 0;
                 }
-                sm.item[slot] = item;
-                st_cluster_u32(mapa_shared(smem_u32(&sm.item[slot]), 1), static_cast<uint32_t>(item));
+                // the item and its metadata into both CTAs' slots
+                const ItemMeta mt = make_meta<kVarlen, kL>(item, a, err);
+                sm.meta[slot] = mt;
+                const int *w = reinterpret_cast<const int *>(&mt);
+                const uint32_t peer = mapa_shared(smem_u32(&sm.meta[slot]), 1);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    st_cluster_u32(peer + 4 * k, static_cast<uint32_t>(w[k]));
                 mbar_arrive(&sm.item_full[slot]);
                 mbar_arrive_cluster(mapa_shared(smem_u32(&sm.item_full[slot]), 1));
             }
-            item = __shfl_sync(0xffffffffu, item, 0);
+            __syncwarp();
         } else {
             if (!pwait(&sm.item_full[slot], par, c, true))
                 break;
-            item = sm.item[slot];
+        }
+        const ItemMeta mt = sm.meta[slot];
+        if (!lead) {
             __syncwarp();
             if (lane == 0)
                 mbar_arrive_remote(lead_bar(&sm.item_empty[slot]));
         }
-        if (item < 0)
+        if (mt.item < 0)
             break;
-        const ItemInfo x = decode_item<kVarlen, kL>(item, a);
-        const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
+        const int N = meta_n(mt.info);
         if (N == 0)
             continue;
-        const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
+        const int mode = meta_mode(mt.info);
+        ItemInfo x = meta_item<kVarlen, kL>(mt, a);
+        if (mode == EA_BLOCK)
+            x.mask_row = (kVarlen ? a.mask_off[x.b] : static_cast<int64_t>(x.b) * a.Hkv * a.nB * a.nB) +
+                         (static_cast<int64_t>(x.h) * x.nB + x.qb) * x.nB;
         const CUtensorMap *tm_q = &tm.q[kL == 1 ? 0 : x.layer];
         const CUtensorMap *tm_k = &tm.k[kL == 1 ? 0 : x.layer];
         const CUtensorMap *tm_v = &tm.v[kL == 1 ? 0 : x.layer];
@@ -808,15 +884,22 @@ __device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uin
         const int slot = it & 1;
         if (!pwait1(&sm.item_full[slot], (it >> 1) & 1, c))
             break;
-        const int item = sm.item[slot];
+        const int item = sm.meta[slot].item, info = sm.meta[slot].info;
         mbar_arrive(&sm.item_empty[slot]);
         if (item < 0)
             break;
-        const int row = item / a.npairs;
-        const int N = in_bounds(row, a.n_rows, c.err) ? a.costs[row] : 0;
+        const int N = meta_n(info);
         if (N == 0)
             continue;
         if (kIsQK) {
+            // The previous item's last P V product is issued before this item's
+            // first Q K^T, so that it is not queued behind up to three S tiles
+            // of this item: the softmax waits for it before its epilogue.
+            // (q_it counts the items with tiles; the PV issuer completes phase
+            // q of pv_issued with item q's last product, and cannot complete
+            // phase q + 1 before this item's S exists.)
+            if (q_it > 0 && !pwait1(&sm.pv_issued, (q_it - 1) & 1, c))
+                break;
             const int qbuf = q_it & 1;
             if (!pwait1(&sm.q_full[qbuf], (q_it >> 1) & 1, c))
                 break;
@@ -846,16 +929,12 @@ __device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uin
                     tc_commit_pair(&sm.q_empty[qbuf], kBothCtas);
             }
         } else {
-            // the item's first P: rank 0's softmax wrote the split flag before it
-            if (!pwait1(&sm.p_ready[j % 3], (j / 3) & 1, c))
-                break;
-            const bool split = *reinterpret_cast<volatile int *>(&sm.pv_split) != 0;
             // the tile loop, compiled twice: with the remainder products and without
             auto tiles = [&](auto split_tag) {
                 constexpr bool kSplit = decltype(split_tag)::value;
                 for (int n = 0; n < N && ok; ++n) {
                     const uint32_t jj = j + n, b = jj % 3, vs = jj % kVSlots;
-                    if ((n > 0 && !pwait1(&sm.p_ready[b], (jj / 3) & 1, c)) ||
+                    if (!pwait1(&sm.p_ready[b], (jj / 3) & 1, c) ||
                         !pwait1(&sm.kv_full[vs], (jj / kVSlots) & 1, c)) {
                         ok = false;
                         break;
@@ -876,11 +955,13 @@ __device__ __forceinline__ void pair_mma(const PrefillArgs &a, PairSmem &sm, uin
                                            sdesc_sw128(vaddr + k * 2048, kHalf, 1024), kIdescPV2, 1u);
                     }
                     tc_commit_pair(&sm.v_empty[vs], kBothCtas);
-                    if (n == N - 1)
+                    if (n == N - 1) {
                         tc_commit_pair(&sm.o_done, kBothCtas);
+                        mbar_arrive(&sm.pv_issued);
+                    }
                 }
             };
-            if (split)
+            if (meta_split(info))
                 tiles(std::true_type{});
             else
                 tiles(std::false_type{});
@@ -912,31 +993,22 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const int slot = it & 1;
         if (!pwait(&sm.item_full[slot], (it >> 1) & 1, c, c.rank != 0))
             break;
-        const int item = sm.item[slot];
+        const ItemMeta mt = sm.meta[slot];
         __syncwarp();
         if (lane == 0)
             mbar_arrive_remote(lead_bar(&sm.item_empty[slot]));
-        if (item < 0)
+        if (mt.item < 0)
             break;
-        const ItemInfo x = decode_item<kVarlen, kL>(item, a);
+        const ItemInfo x = meta_item<kVarlen, kL>(mt, a);
         bool store;
         const int qh = item_head(x, static_cast<int>(c.rank), a, store);
-        const int N = in_bounds(x.row, a.n_rows, err) ? a.costs[x.row] : 0;
-        const int mode = a.m[x.layer][x.b * a.Hkv + x.h];
+        const int N = meta_n(mt.info);
+        const int mode = meta_mode(mt.info);
         int n_sink = 0, kb_lo = 0;
         if (mode == EA_SSA)
             ssa_tiles(x.qb, a.sink, a.window, n_sink, kb_lo);
-        bool diag_kept = false;
-        if (mode == EA_BLOCK && N > 0)
-            diag_kept = in_bounds(x.mask_row + x.qb, mask_limit(a), err) &&
-                        a.block_mask[x.layer][x.mask_row + x.qb] != 0;
-        // Rows that keep few keys (the first query blocks, small sink and
-        // window, a lone diagonal block) take P V in two bf16 parts: with a
-        // handful of keys one probability's 2^-9 rounding error reaches O
-        // undiluted, and would add up to 2^-9 |O| to the output's own rounding.
-        const bool split = N > 0 && first_row_keys(mode, x.qb, a.sink, a.window, N, diag_kept) <= kSplitMaxKeys;
-        if (warp == 0 && lane == 0 && c.rank == 0)
-            sm.pv_split = split ? 1 : 0;   // read by the PV issuer after this item's first P
+        const bool diag_kept = meta_diag(mt.info);
+        const bool split = meta_split(mt.info);   // P V in two bf16 parts (few kept keys)
         const int i = x.qb * T + r;
         float m_run = NEG_INF, l_run = 0.f;
         bool ok = true;
@@ -1110,12 +1182,7 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         sm.red_l[it & 1][wg][r] = l_run;
         named_bar_sync(bar_id, 64);
         const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
-        // the row's sequence, length and offsets, decoded again here so that
-        // none of them stays live across the tile loop
-        RowInfo e;
-        decode_row<kVarlen, kL>(x.row, a, e);
-        if (kL == 1)
-            e.layer = 0;
+        const RowInfo &e = x;   // the row's layer, sequence, length and offsets
         const bool row_ok = store && i < e.S &&
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
                             in_bounds(qh, a.Hq, err);
@@ -1224,6 +1291,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         }
         mbar_init(&sm.o_done, 1);
         mbar_init(&sm.teardown, 2);            // one commit from each MMA issuer
+        mbar_init(&sm.pv_issued, 1);           // the PV issuer, once per item with tiles
         sm.abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
