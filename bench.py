@@ -587,7 +587,70 @@ def run_decode(args, dev, peaks, flush):
                              ROOT, "sparse_head_attention_gb300", "csrc", "ea_decode.cu"))
                          if cfg.B == 32 else None,
                          "peak_source": peaks["source"]},
-            "gpu_launches_per_step": 3, "clocks": clk}
+            "gpu_launches_per_step": 3, "clocks": clk,
+            "small_batch": run_decode_small(args, dev, peaks) if cfg.B == 32 else None}
+
+
+def run_decode_small(args, dev, peaks):
+    """Decode at serving batch sizes B = 1 and 4 (the 128K cache, heads and
+    routing of the B = 32 line): the step through the public call, timed eager
+    (host argument handling and three launches inside the events) and replayed
+    from a CUDA graph (device time of the same launches), as a serving loop
+    that captures its decode step runs it."""
+    import dataclasses
+
+    import sparse_head_attention_gb300 as ea
+    from sparse_head_attention_gb300 import workloads as wl
+    out = {}
+    stream = torch.cuda.current_stream()
+    for B in (1, 4):
+        cfg = dataclasses.replace(wl.DECODE_128K, B=B, name="%s_b%d" % (wl.DECODE_128K.name, B))
+        q, Kc, Vc, sl = wl.decode_inputs(cfg, device=dev)
+        _, m_cpu = wl.routing_from_sa_heads(cfg.B, cfg.Hkv, cfg.sa_heads)
+        m = m_cpu.to(dev)
+        nbytes = decode_kept_bytes(cfg, m_cpu.numpy())
+        ws = ea.decode_workspace(cfg.B, cfg.Hq, cfg.Hkv, cfg.L, device=dev)
+        O = torch.empty_like(q)
+        LSE = torch.empty(cfg.B, cfg.Hq, dtype=torch.float32, device=dev)
+
+        def step():
+            ea.ea_hybrid_attn_decode(q, Kc, Vc, sl, m, sink=cfg.sink, window=cfg.window, O=O, LSE=LSE,
+                                     workspace=ws)
+
+        def timed(fn, n=200):
+            for _ in range(max(3, args.warmup)):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / n
+
+        t_eager = timed(step)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        t_graph = timed(g.replay)
+        if ea.ea_check_errors(ws) != 0:
+            raise RuntimeError("device error in the small-batch decode")
+        out["b%d" % B] = {
+            "kept_kv_bytes_per_step": nbytes,
+            "us_per_step_eager": round(t_eager * 1e3, 2),
+            "us_per_step_graph": round(t_graph * 1e3, 2),
+            "frac_eager": round(nbytes / (t_eager * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "frac_graph": round(nbytes / (t_graph * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+        del q, Kc, Vc, ws, g
+    out["timing"] = ("200 back-to-back steps between two events (the cache is larger than L2); "
+                     "eager: the Python call each step; graph: one captured call replayed")
+    return out
 
 
 def run_varlen(args, dev, peaks, flush):

@@ -719,18 +719,49 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
 }
 
-// One CTA per (q head, b): log-sum-exp merge of the unit's chunks.  Warp 0
-// computes the maximum and the weight sum of the partial LSEs in one online
-// pass (lanes over chunks, then a pairwise merge across lanes); then four
-// groups of 128 threads (one thread per head dimension) each sum the weighted
-// partial outputs of a quarter of the chunks with eight loads in flight, and
-// the four group sums are added in a fixed order.
+// One CTA per (q head, b): log-sum-exp merge of the unit's chunks.  Four
+// groups of 128 threads (one thread per head dimension) each take a quarter of
+// the chunks in one pass: a batch of partial LSEs and outputs is loaded at
+// once, the running maximum moves to the batch's maximum (one rescale per
+// batch) and the batch's weights exp(lse - max) are added to the running sum
+// and the weighted output.  The four groups' states are combined in a fixed
+// order.  (A separate pass for the maximum would put one more round trip to
+// memory on this short kernel's path.)
 constexpr int kMergeGroups = 4;
 
-__global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM) decode_merge_kernel(const DecodeArgs a)
+template <int K>
+__device__ __forceinline__ void merge_batch(const float (&l)[K], const float (&o)[K], float &m,
+                                            float &w, float &osum)
 {
-    __shared__ float stat[2];
-    __shared__ float part[kMergeGroups][EA_HEAD_DIM];
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const float LOG2E = 1.4426950408889634f;
+    float mb = l[0];
+#pragma unroll
+    for (int k = 1; k < K; ++k)
+        mb = fmaxf(mb, l[k]);
+    if (mb == NEG_INF)
+        return;                       // no kept key in any of these chunks
+    if (mb > m) {
+        if (m > NEG_INF) {
+            const float f = ex2((m - mb) * LOG2E);
+            w *= f;
+            osum *= f;
+        }
+        m = mb;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        const float e = ex2((l[k] - m) * LOG2E);   // 0 for an empty chunk (lse = -inf, o = 0)
+        w += e;
+        osum += e * o[k];
+    }
+}
+
+// (two CTAs per SM: a large batch has thousands of these short CTAs)
+__global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM, 2) decode_merge_kernel(const DecodeArgs a)
+{
+    __shared__ float gm[kMergeGroups], gw[kMergeGroups];
+    __shared__ float go[kMergeGroups][EA_HEAD_DIM];
     const float NEG_INF = -__int_as_float(0x7f800000);
     const float LOG2E = 1.4426950408889634f;
     const int qh = blockIdx.x, b = blockIdx.y;
@@ -743,64 +774,55 @@ __global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM) decode_merge_kerne
                    static_cast<int64_t>(a.B) * a.Hkv * a.max_splits, &a.hdr->error))
         ns = 0;
     const int64_t base = static_cast<int64_t>(first) * a.g + hh;
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        float m = NEG_INF, w = 0.f;      // running max and sum of exp(lse - m)
-        for (int s = lane; s < ns; s += 32) {
-            const float x = a.part_lse[base + static_cast<int64_t>(s) * a.g];
-            if (x == NEG_INF)
-                continue;
-            if (x > m) {
-                w = (m == NEG_INF ? 0.f : w * ex2((m - x) * LOG2E)) + 1.f;
-                m = x;
-            } else {
-                w += ex2((x - m) * LOG2E);
-            }
-        }
+    const int per = (ns + kMergeGroups - 1) / kMergeGroups;
+    const int s0 = min(grp * per, ns), s1 = min(s0 + per, ns);
+    float m = NEG_INF, w = 0.f, osum = 0.f;
+    int s = s0;
+    for (; s + 8 <= s1; s += 8) {
+        float l[8], o[8];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float w2 = __shfl_xor_sync(0xffffffffu, w, o);
-            const float M = fmaxf(m, m2);
-            w = (m == NEG_INF ? 0.f : w * ex2((m - M) * LOG2E)) +
-                (m2 == NEG_INF ? 0.f : w2 * ex2((m2 - M) * LOG2E));
-            m = M;
+        for (int k = 0; k < 8; ++k) {
+            const int64_t pidx = base + static_cast<int64_t>(s + k) * a.g;
+            l[k] = a.part_lse[pidx];
+            o[k] = a.part_o[pidx * EA_HEAD_DIM + dd];
         }
-        if (lane == 0) {
-            stat[0] = m;
-            stat[1] = w;
-        }
+        merge_batch(l, o, m, w, osum);
     }
-    __syncthreads();
-    const float M = stat[0], wsum = stat[1];
-    float osum = 0.f;
-    if (M > NEG_INF) {
-        const int per = (ns + kMergeGroups - 1) / kMergeGroups;
-        const int s0 = min(grp * per, ns), s1 = min(s0 + per, ns);
-        int s = s0;
-        for (; s + 8 <= s1; s += 8) {
-            float l[8], o[8];
+    for (; s + 4 <= s1; s += 4) {
+        float l[4], o[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                l[k] = a.part_lse[base + static_cast<int64_t>(s + k) * a.g];
-                o[k] = a.part_o[(base + static_cast<int64_t>(s + k) * a.g) * EA_HEAD_DIM + dd];
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                osum += ex2((l[k] - M) * LOG2E) * o[k];
+        for (int k = 0; k < 4; ++k) {
+            const int64_t pidx = base + static_cast<int64_t>(s + k) * a.g;
+            l[k] = a.part_lse[pidx];
+            o[k] = a.part_o[pidx * EA_HEAD_DIM + dd];
         }
-        for (; s < s1; ++s) {
-            const int64_t pidx = base + static_cast<int64_t>(s) * a.g;
-            osum += ex2((a.part_lse[pidx] - M) * LOG2E) * a.part_o[pidx * EA_HEAD_DIM + dd];
-        }
+        merge_batch(l, o, m, w, osum);
     }
-    part[grp][dd] = osum;
+    for (; s < s1; ++s) {
+        const int64_t pidx = base + static_cast<int64_t>(s) * a.g;
+        const float l[1] = {a.part_lse[pidx]}, o[1] = {a.part_o[pidx * EA_HEAD_DIM + dd]};
+        merge_batch(l, o, m, w, osum);
+    }
+    if (dd == 0) {
+        gm[grp] = m;
+        gw[grp] = w;
+    }
+    go[grp][dd] = osum;
     __syncthreads();
     if (grp == 0) {
-        float o = 0.f;
+        float M = NEG_INF;
 #pragma unroll
         for (int k = 0; k < kMergeGroups; ++k)
-            o += part[k][dd];
+            M = fmaxf(M, gm[k]);
+        float wsum = 0.f, o = 0.f;
+        if (M > NEG_INF)
+#pragma unroll
+            for (int k = 0; k < kMergeGroups; ++k)
+                if (gm[k] > NEG_INF) {
+                    const float f = ex2((gm[k] - M) * LOG2E);
+                    wsum += gw[k] * f;
+                    o += go[k][dd] * f;
+                }
         a.O[b * a.o_sb + qh * a.o_sh + dd] = __float2bfloat16_rn(wsum > 0.f ? o / wsum : 0.f);
         if (dd == 0 && a.LSE)
             a.LSE[static_cast<int64_t>(b) * a.Hq + qh] = wsum > 0.f ? M + __logf(wsum) : NEG_INF;
