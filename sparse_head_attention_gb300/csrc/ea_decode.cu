@@ -73,7 +73,17 @@ struct DecodeArgs {
     const int32_t *block_table;
     int64_t bt_stride;
     int page_size, num_pages;
+    // a single sequence (B * Hkv <= kSelfPlanUnits): every split CTA plans the
+    // step itself and takes chunks blockIdx.x + k * gridDim.x, with no planner
+    // launch and no queue
+    int self_plan;
 };
+
+// Up to this many units a step is planned inside the split kernel.  Measured
+// per step against the planner launch: B = 1 x 8 KV heads 36.9 -> 35.3 us; at
+// B = 4 and 8 the fixed chunk assignment balances worse than the queue (+1.4 %,
+// +4.6 %), so larger batches keep the planner.
+constexpr int kSelfPlanUnits = 8;
 
 struct __align__(1024) DecSmem {
     uint8_t k[kDecStages][kDecTileBytes];
@@ -86,6 +96,7 @@ struct __align__(1024) DecSmem {
     uint64_t chunk_full[2], chunk_empty[2];
     int chunk[2];  // chunk index handed from the producer to the compute warps (-1: none left)
     int abort;     // set by a timed-out wait; every warp then leaves without further barriers
+    int plan_first[kSelfPlanUnits], plan_ns[kSelfPlanUnits], plan_total;   // self-planned steps
 };
 
 // Kept keys of one (b, KV head) unit as at most two contiguous ranges:
@@ -317,15 +328,32 @@ struct ChunkInfo {
     const uint16_t *list;     // BLOCK unit: its kept blocks (NULL otherwise)
 };
 
-__device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c)
+__device__ __forceinline__ ChunkInfo chunk_info(const DecodeArgs &a, int c, const DecSmem &sm)
 {
     ChunkInfo ci;
-    const int code = a.chunks[c];
-    const int u = code >> kSplitBits, sp = code & ((1 << kSplitBits) - 1);
+    int u, sp, ns;
+    if (a.self_plan) {
+        // the last unit whose first chunk is <= c (every unit has one chunk at least)
+        int lo = 0, hi = a.B * a.Hkv - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.plan_first[mid] <= c)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        u = lo;
+        sp = c - sm.plan_first[u];
+        ns = sm.plan_ns[u];
+    } else {
+        const int code = a.chunks[c];
+        u = code >> kSplitBits;
+        sp = code & ((1 << kSplitBits) - 1);
+        ns = a.unit_splits[u];
+    }
     ci.b = u / a.Hkv;
     ci.h = u % a.Hkv;
     unit_keys(a, ci.b, ci.h, ci.ks);
-    const int ns = a.unit_splits[u];
     ci.list = nullptr;
     ci.kept = ci.ks.n;
     if (ci.ks.blk >= 0) {
@@ -433,6 +461,69 @@ __device__ __forceinline__ uint32_t sw_off(int row, int cb)
     return (cb >> 3) * kDecHalfBytes + row * 128 + (((cb & 7) ^ (row & 7)) << 4);
 }
 
+// A self-planned step (B * Hkv <= kSelfPlanUnits): warp 0 of every split CTA
+// computes the plan decode_plan_kernel would (the same chunk size, split
+// counts and chunk order, unit by unit), lane l taking units 2l and 2l + 1, into
+// shared memory; CTA 0 also stores each unit's first chunk and split count for
+// the merge kernel.
+__device__ __forceinline__ void self_plan(const DecodeArgs &a, DecSmem &sm, int lane)
+{
+    const int units = a.B * a.Hkv;
+    int w[2] = {0, 0};
+    bool bad = false;
+    long long mine = 0;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int u = 2 * lane + k;
+        if (u < units) {
+            bool ok;
+            w[k] = unit_work(a, u, ok);
+            bad |= !ok;
+            mine += w[k];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    const long long target = 4ll * (a.num_sms > 0 ? a.num_sms : 1);
+    long long chunk = (mine + target - 1) / target;
+    chunk = chunk < EA_DECODE_AUTO_CHUNK ? EA_DECODE_AUTO_CHUNK
+                                         : (chunk > EA_DECODE_MAX_CHUNK ? EA_DECODE_MAX_CHUNK : chunk);
+    int ns[2] = {0, 0};
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+        if (2 * lane + k < units) {
+            int n = a.num_splits > 0 ? a.num_splits : static_cast<int>((w[k] + chunk - 1) / chunk);
+            ns[k] = n < 1 ? 1 : (n > a.max_splits ? a.max_splits : n);
+        }
+    const int local = ns[0] + ns[1];
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    int first = incl - local;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int u = 2 * lane + k;
+        if (u < units) {
+            sm.plan_first[u] = first;
+            sm.plan_ns[u] = ns[k];
+            if (blockIdx.x == 0) {
+                a.unit_first[u] = first;
+                a.unit_splits[u] = ns[k];
+            }
+        }
+        first += ns[k];
+    }
+    if (lane == 31)
+        sm.plan_total = incl;
+    if (bad && blockIdx.x == 0)
+        raise_error(&a.hdr->error, EA_DEVERR_CHECK);
+}
+
 // Persistent: each CTA takes chunks from a queue (an atomic counter that the
 // planner resets), so CTAs that drew short chunks take more of them.
 // Warp w (of 4) owns keys [16w, 16w + 16) of every 64-key tile; the query
@@ -467,11 +558,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         fence_proxy_async_smem();
     }
     __syncthreads();
-    // The chunk list comes from the planner launched just before; every CTA is
-    // resident (one per SM) before the merge kernel may be scheduled.
+    if (a.self_plan) {
+        if (warp == 0)
+            self_plan(a, sm, lane);
+        __syncthreads();
+    }
+    // The chunk list comes from the planner launched just before (a self-planned
+    // step is launched without overlap); every CTA is resident (one per SM)
+    // before the merge kernel may be scheduled.
     griddep_wait();
     griddep_launch_dependents();
-    const int total = static_cast<int>(a.hdr->n_items);
+    const int total = a.self_plan ? sm.plan_total : static_cast<int>(a.hdr->n_items);
 
     if (warp == kDecWarps) {
         // ------------------------------------------------------------ producer
@@ -488,7 +585,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 return;
             int c = -1;
             if (lane == 0) {
-                const uint32_t x = atomicAdd(&a.hdr->work_counter, 1u);
+                const uint32_t x = a.self_plan ? blockIdx.x + static_cast<uint32_t>(it) * gridDim.x
+                                               : atomicAdd(&a.hdr->work_counter, 1u);
                 c = x < static_cast<uint32_t>(total) ? static_cast<int>(x) : -1;
                 sm.chunk[slot] = c;
                 mbar_arrive(&sm.chunk_full[slot]);
@@ -496,7 +594,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             c = __shfl_sync(0xffffffffu, c, 0);
             if (c < 0)
                 break;
-            const ChunkInfo ci = chunk_info(a, c);
+            const ChunkInfo ci = chunk_info(a, c, sm);
             int my_page = 0;
             for (int t = 0; t < ci.n_tiles; ++t) {
                 if (a.page_size && (t & 31) == 0) {
@@ -549,7 +647,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             mbar_arrive(&sm.chunk_empty[slot]);
         if (c < 0)
             break;
-        const ChunkInfo ci = chunk_info(a, c);
+        const ChunkInfo ci = chunk_info(a, c, sm);
         // A unit that keeps few keys takes P V in two bf16 parts: with a handful
         // of keys one probability's 2^-9 rounding error would reach O undiluted.
         const bool split = ci.kept <= kDecSplitMaxKeys;
@@ -830,7 +928,7 @@ __global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM, 2) decode_merge_ke
 }
 
 static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, const DecodeArgs &a,
-                                 int grid, cudaStream_t st)
+                                 int grid, cudaStream_t st, bool overlap)
 {
     const size_t smem = sizeof(DecSmem) + 1024;
     static bool attr_done[64] = {};   // the attribute is set once per device
@@ -855,7 +953,7 @@ static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, c
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = overlap ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, decode_split_kernel, tk, tv, a);
 }
 
@@ -976,10 +1074,15 @@ static ea_status decode_launch(const void *q, const void *Kc, const void *Vc, vo
     a.num_sms = sms;
     const int64_t max_chunks = static_cast<int64_t>(B) * Hkv * max_splits;
     const int grid = static_cast<int>(max_chunks < sms ? max_chunks : sms);
+    // Small batches plan inside the split kernel: no planner launch on their
+    // short critical path.  That launch then may not overlap its predecessor
+    // (the previous step's merge still reads the partials it overwrites).
+    a.self_plan = static_cast<int64_t>(B) * Hkv <= kSelfPlanUnits ? 1 : 0;
     if (block_mask)
         decode_blocks_kernel<<<static_cast<unsigned>(static_cast<int64_t>(B) * Hkv), kBlkThreads, 0, st>>>(a);
-    decode_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
-    const cudaError_t e = launch_decode(tk, tv, a, grid, st);
+    if (!a.self_plan)
+        decode_plan_kernel<<<1, kPlanThreads, 0, st>>>(a);
+    const cudaError_t e = launch_decode(tk, tv, a, grid, st, !a.self_plan);
     if (e != cudaSuccess)
         return EA_ERR_CUDA;
     if (launch_merge(a, Hq, B, st) != cudaSuccess)
