@@ -22,17 +22,23 @@
 //                   every S row: online softmax in fp32 (exp2 domain, lazy
 //                   rescale of O when the max grows by more than 2^8), P (bf16)
 //                   written back into TMEM over S; finally O / l and LSE.
-//        warp 8     TMA producer: this CTA's Q tile and K/V halves
-//        warp 9     rank 0: tcgen05 issuer, S = Q K^T (smem x smem) and
-//                   O += P V (P from TMEM, V from smem) into TMEM
+//        warp 8     TMA producer: this CTA's Q tile and K/V halves; rank 0's
+//                   also takes items from the queue and publishes each item's
+//                   metadata (visited tiles, mode, row fields) to both CTAs
+//        warp 9     rank 0: tcgen05 issuer of S = Q K^T (smem x smem)
+//        warp 10    rank 0: tcgen05 issuer of O += P V (P from TMEM, V from
+//                   smem), with a second product of P's bf16 remainder on
+//                   items whose rows keep few keys
 //      TMEM (each CTA): O (128 columns) + three S/P buffers (3 x 128), so the
 //      next tiles' S = Q K^T products run while the softmax works.
-//      Shared memory (each CTA): Q (2 x 32 KB, two items in flight), a 7-stage
-//      ring of 16 KB K/V halves, and the O tile on its way out (32 KB).
+//      Shared memory (each CTA): Q (2 x 32 KB, two items in flight), a 3-slot
+//      K ring and a 4-slot V ring of 16 KB halves, and the O tile on its way
+//      out (32 KB).
 //   Batches are either B sequences of one length S ([B][S][heads][d] tensors)
-//   or sequences of different lengths packed back to back (cu_seqlens); the
-//   attention kernel is compiled once for each, so that the fixed-length one
-//   carries none of the other's row decoding.
+//   or sequences of different lengths packed back to back (cu_seqlens), and a
+//   launch may hold up to 48 layers of one shape; the attention kernel is
+//   compiled for each of these, so that the fixed-length single-layer one
+//   carries none of the others' row decoding.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
