@@ -96,6 +96,23 @@ def test_few_kept_keys_with_large_values(dev, num_splits):
                  "few keys, splits=%d" % num_splits, flat=True)
 
 
+def test_single_sequence_planned_in_kernel_equals_planner(dev):
+    # B * Hkv <= 8 is planned inside the split kernel; the same sequence as row 0
+    # of a two-sequence batch goes through the planner launch.  Both plans use
+    # the 2048-key minimum chunk here, so the chunks, partials and merge are the
+    # same: the outputs must be bitwise equal (and match the oracle).
+    cfg = wl.DecodeConfig("t", B=2, Hq=32, Hkv=8, d=128, L=5000, sink=128, window=1000)
+    q, Kc, Vc, _ = wl.decode_inputs(cfg, seqlens=[5000, 5000])
+    q[1], Kc[1], Vc[1] = q[0], Kc[0], Vc[0]
+    modes = np.array([[FULL, SSA, SSA, FULL, SSA, SSA, SSA, SSA]] * 2, np.uint8)
+    sl2 = torch.tensor([5000, 5000], dtype=torch.int32)
+    O2, L2 = run(dev, q, Kc, Vc, sl2, modes, cfg.sink, cfg.window)
+    O1, L1 = run(dev, q[:1], Kc[:1], Vc[:1], sl2[:1], modes[:1], cfg.sink, cfg.window)
+    assert torch.equal(O1[0], O2[0]) and torch.equal(L1[0], L2[0])
+    Oref, Lref = oracle.decode(q[:1], Kc[:1], Vc[:1], sl2[:1], modes[:1], sink=cfg.sink, window=cfg.window)
+    assert_close(O1.float().cpu().numpy(), L1.cpu().numpy(), Oref, Lref, "single sequence")
+
+
 def test_block_decode_equals_last_prefill_row_on_gpu(dev):
     B, S, Hq, Hkv = 1, 1500, 8, 2
     Q, K, V = wl.qkv(B, S, Hq, Hkv, 128, seed=14)
