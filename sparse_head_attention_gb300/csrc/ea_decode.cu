@@ -872,7 +872,8 @@ __global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM, 2) decode_merge_ke
                    static_cast<int64_t>(a.B) * a.Hkv * a.max_splits, &a.hdr->error))
         ns = 0;
     const int64_t base = static_cast<int64_t>(first) * a.g + hh;
-    const int per = (ns + kMergeGroups - 1) / kMergeGroups;
+    const int groups = blockDim.x / EA_HEAD_DIM;   // 1 for many (b, head) rows, else kMergeGroups
+    const int per = (ns + groups - 1) / groups;
     const int s0 = min(grp * per, ns), s1 = min(s0 + per, ns);
     float m = NEG_INF, w = 0.f, osum = 0.f;
     int s = s0;
@@ -911,12 +912,13 @@ __global__ void __launch_bounds__(kMergeGroups * EA_HEAD_DIM, 2) decode_merge_ke
         float M = NEG_INF;
 #pragma unroll
         for (int k = 0; k < kMergeGroups; ++k)
-            M = fmaxf(M, gm[k]);
+            if (k < groups)
+                M = fmaxf(M, gm[k]);
         float wsum = 0.f, o = 0.f;
         if (M > NEG_INF)
 #pragma unroll
             for (int k = 0; k < kMergeGroups; ++k)
-                if (gm[k] > NEG_INF) {
+                if (k < groups && gm[k] > NEG_INF) {
                     const float f = ex2((gm[k] - M) * LOG2E);
                     wsum += gw[k] * f;
                     o += go[k][dd] * f;
@@ -959,14 +961,18 @@ static cudaError_t launch_decode(const CUtensorMap &tk, const CUtensorMap &tv, c
 
 // The merge kernel, launched so that its CTAs may be scheduled while the split
 // kernel finishes (it waits for the split kernel before reading anything).
+// With more (b, head) rows than two per SM, one group of 128 threads per row
+// (the rows fill the GPU, and a row's chunks are few); otherwise four groups
+// share a row's chunks.
 static cudaError_t launch_merge(const DecodeArgs &a, int Hq, int B, cudaStream_t st)
 {
+    const int groups = static_cast<int64_t>(B) * Hq >= 2ll * a.num_sms ? 1 : kMergeGroups;
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(Hq, B);
-    cfg.blockDim = dim3(kMergeGroups * EA_HEAD_DIM);
+    cfg.blockDim = dim3(groups * EA_HEAD_DIM);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;
