@@ -390,7 +390,7 @@ def run_ours(args, rank, world, dev):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms, 3), "estimator": "median of %d steps" % n_e2e,
                "call": "ea_hybrid_attn_prefill_host (chunked copies overlapped with the attention, "
-                       "%s chunks)" % (args.e2e_chunks or "8"),
+                       "%s chunks)" % (args.e2e_chunks or "10"),
                "serial_ms_per_step": round(s_ms, 3)}
         del hQ, hK, hV, dQ, dK, dV, buf
 

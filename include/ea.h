@@ -363,7 +363,10 @@ size_t ea_prefill_host_buffer_size(int B, int S, int Hq, int Hkv, int d, int wit
  *                and folds every device error word into the workspace at its
  *                start, so ea_check_errors(device_buffer, stream) reads them
  *                afterwards.
- *   n_chunks     0 = automatic (8, at most nB); otherwise 1 <= n_chunks <= 64
+ *   n_chunks     0 = automatic (10, at most nB); otherwise 1 <= n_chunks <= 64.
+ *                The chunks shrink toward the end of the sequence (chunk c ends
+ *                near nB * (1 - (1 - (c + 1) / n_chunks)^1.25) query blocks),
+ *                each holding at least one query block
  *                and <= nB.
  *   stream       the call's work is ordered after earlier work on `stream`,
  *                and later work on `stream` is ordered after all of it

@@ -7,6 +7,7 @@
 // chunks of whole query blocks and run as a three-stage pipeline:
 //
 //   up stream       Q/K/V rows of chunk c                  -> event in[c]
+//   (chunks shrink toward the end of the sequence, see chunk_bounds)
 //   compute stream  wait in[c]; plan + attention over chunk c's query blocks
 //                                                          -> event out[c]
 //   down stream     wait out[c]; O / LSE rows of chunk c back to the host
@@ -20,6 +21,7 @@
 // host: ordering is by events only.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "ea_internal.h"
@@ -27,7 +29,27 @@
 namespace ea {
 
 constexpr int kMaxChunks = 64;
-constexpr int kAutoChunks = 8;
+constexpr int kAutoChunks = 10;
+
+// Query-block boundaries of the chunks: chunk c ends near
+// nB * (1 - (1 - (c + 1) / n)^1.25), so that the chunks shrink toward the end.
+// Under a causal mask the last query blocks carry the most work, and what
+// remains after the last upload is the last chunk's attention and download:
+// the smaller that chunk, the shorter the tail.  (32K Llama-shaped layer,
+// median step: 8 equal chunks 3.02 ms, 10 equal 3.00 ms; 10 shrinking with
+// exponent 1.2 / 1.25-1.3 / 1.4: 2.92 / 2.92 / 2.94 ms; 12 with 1.2: 2.92 ms.)
+// Every chunk holds at least one query block.
+static void chunk_bounds(int nB, int n, int *qb)
+{
+    qb[0] = 0;
+    for (int c = 1; c < n; ++c) {
+        int v = static_cast<int>(nB * (1.0 - std::pow(1.0 - static_cast<double>(c) / n, 1.25)));
+        v = v > qb[c - 1] + 1 ? v : qb[c - 1] + 1;
+        v = v < nB - (n - c) ? v : nB - (n - c);
+        qb[c] = v;
+    }
+    qb[n] = nB;
+}
 
 // Device buffer layout (every part 256-byte aligned): the two planner
 // workspaces first.
@@ -212,9 +234,11 @@ extern "C" ea_status ea_hybrid_attn_prefill_host(const void *Q_host, const void 
                         cudaMemcpyHostToDevice, R.up) != cudaSuccess)
         return fail(EA_ERR_CUDA);
 
+    int bounds[kMaxChunks + 1];
+    chunk_bounds(nB, n_chunks, bounds);
     for (int c = 0; c < n_chunks; ++c) {
-        const int qb0 = static_cast<int>(static_cast<int64_t>(c) * nB / n_chunks);
-        const int qb1 = static_cast<int>(static_cast<int64_t>(c + 1) * nB / n_chunks);
+        const int qb0 = bounds[c];
+        const int qb1 = bounds[c + 1];
         const int r0 = qb0 * EA_TILE;
         const int r1 = qb1 * EA_TILE < S ? qb1 * EA_TILE : S;
         if (copy_rows(dQ, Q_host, row_q, B, S, r0, r1, cudaMemcpyHostToDevice, R.up) ||
