@@ -1178,16 +1178,23 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
             break;
         j += N;
 
-        // epilogue: O / l -> bf16, LSE = ln(2^m * l)
+        // epilogue: O / l -> bf16, LSE = ln(2^m * l).  What needs no O (the
+        // row-sum exchange, the stage's release by the previous item's store)
+        // comes first, while the item's last P V product completes.
+        sm.red_l[it & 1][wg][r] = l_run;
+        named_bar_sync(bar_id, 64);
+        const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
+        if (!kVarlen && store) {
+            if (lane == 0)
+                bulk_wait_read_all();     // the previous item's store has read the stage
+            __syncwarp();
+        }
         if (N > 0) {
             if (!pwait(&sm.o_done, o_cnt & 1, c))
                 break;
             ++o_cnt;
             tc_fence_after();
         }
-        sm.red_l[it & 1][wg][r] = l_run;
-        named_bar_sync(bar_id, 64);
-        const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
         const RowInfo &e = x;   // the row's layer, sequence, length and offsets
         const bool row_ok = store && i < e.S &&
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
@@ -1203,11 +1210,6 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const bool staged = !kVarlen && store;
         const int wrow = r & 31;
         uint8_t *wstage = sm.ostage + warp * (kTileBytes / 8);
-        if (staged) {
-            if (lane == 0)
-                bulk_wait_read_all();     // the previous item's store has read the stage
-            __syncwarp();
-        }
 #pragma unroll 1
         for (int ch = 0; ch < 2; ++ch) {
             uint32_t o[32];
