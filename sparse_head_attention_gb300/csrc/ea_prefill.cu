@@ -1210,17 +1210,20 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const bool staged = !kVarlen && store;
         const int wrow = r & 31;
         uint8_t *wstage = sm.ostage + warp * (kTileBytes / 8);
-#pragma unroll 1
-        for (int ch = 0; ch < 2; ++ch) {
-            uint32_t o[32];
-            if (N > 0) {
-                tmem_ld32(tO + ch * 32, o);
-                tmem_wait_ld();
-            } else {
+        // both halves of this warp's O columns in one round trip to TMEM
+        uint32_t oo[2][32];
+        if (N > 0) {
+            tmem_ld32(tO, oo[0]);
+            tmem_ld32(tO + 32, oo[1]);
+            tmem_wait_ld();
+        } else {
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc)
-                    o[cc] = 0u;
-            }
+            for (int cc = 0; cc < 32; ++cc)
+                oo[0][cc] = oo[1][cc] = 0u;
+        }
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t (&o)[32] = oo[ch];
             uint32_t w[16];
 #pragma unroll
             for (int cc = 0; cc < 16; ++cc)
