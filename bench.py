@@ -662,7 +662,7 @@ def run_varlen(args, dev, peaks, flush):
     from sparse_head_attention_gb300 import workloads as wl
     cfg = wl.LLAMA_32K
     rng = np.random.default_rng(11)
-    lens = [int(x) for x in rng.integers(256, 8193, size=128)]
+    lens = [int(x) for x in rng.integers(256, 8193, size=128)][:args.varlen_seqs]
     total = sum(lens)
     Q = wl.randn_bf16((total, cfg.Hq, cfg.d), seed=21, device=dev)
     K = wl.randn_bf16((total, cfg.Hkv, cfg.d), seed=22, device=dev)
@@ -704,7 +704,7 @@ def run_varlen(args, dev, peaks, flush):
     if ea.ea_check_errors(ws) != 0:
         raise RuntimeError("device error in the variable-length prefill")
     ms = statistics.median(x.elapsed_time(y) for x, y in ts)
-    return {"workload": "128 sequences of 256..8192 tokens (%d in all), 32/8 heads, 2 FA + 6 SSA" % total,
+    return {"workload": "%d sequences of 256..8192 tokens (%d in all), 32/8 heads, 2 FA + 6 SSA" % (len(lens), total),
             "ms_per_step": round(ms, 4),
             "useful_tflops": round(useful / (ms * 1e-3) / 1e12, 1),
             "visited_tile_tflops": round(tile / (ms * 1e-3) / 1e12, 1),
@@ -1301,6 +1301,8 @@ def main():
     ap.add_argument("--serial-sweep", action="store_true",
                     help="fused single launch vs Serial Dispatch (Algorithm 1(a)) sweep instead of the benchmark")
     ap.add_argument("--serial-lengths", type=int, nargs="+", default=[16384, 32768, 65536, 131072])
+    ap.add_argument("--varlen-seqs", type=int, default=128,
+                    help="the first N sequences of the variable-length batch (a smaller case for ncu)")
     ap.add_argument("--decode-batch", type=int, default=32,
                     help="decode batch (32 is the benchmark workload; smaller for profiling)")
     args = ap.parse_args()
