@@ -163,3 +163,37 @@ def test_xa_ssa_estimation_prefill_and_decode_replayed(dev):
             assert torch.equal(a_, b_), seed
     for ws in (xws, pws, dws):
         check_no_device_error(ws)
+
+
+def test_several_layers_in_one_launch_replayed(dev):
+    # ea_hybrid_attn_prefill_layers inside a graph: the layers' pointers and
+    # tensor maps travel as kernel parameters, so a replay with new values in
+    # the same buffers equals an eager call
+    L, B, S, Hq, Hkv = 3, 1, 700, 8, 2
+    Qs, Ks, Vs = [], [], []
+    for l in range(L):
+        Q, K, V = (t.to(dev) for t in wl.qkv(B, S, Hq, Hkv, 128, seed=500 + l))
+        Qs.append(Q), Ks.append(K), Vs.append(V)
+    ms = [torch.tensor([[FULL, SSA]], dtype=torch.uint8, device=dev) for _ in range(L)]
+    Os = [torch.empty_like(q) for q in Qs]
+    LSEs = [torch.empty(B, Hq, S, dtype=torch.float32, device=dev) for _ in range(L)]
+    ws = ea.prefill_layers_workspace(L, B, S, Hq, Hkv, device=dev)
+
+    def step():
+        ea.ea_hybrid_attn_prefill_layers(Qs, Ks, Vs, ms, sink=16, window=200, Os=Os, LSEs=LSEs,
+                                         workspace=ws)
+
+    g = capture(step)
+    for seed in (510, 511):
+        for l in range(L):
+            Qs[l].copy_(wl.randn_bf16(Qs[l].shape, seed=seed + l, device=dev))
+            ms[l].copy_(torch.tensor([[SSA, FULL]] if (seed + l) % 2 else [[FULL, SSA]],
+                                     dtype=torch.uint8))
+        g.replay()
+        torch.cuda.synchronize()
+        got = [(o.clone(), s.clone()) for o, s in zip(Os, LSEs)]
+        step()
+        torch.cuda.synchronize()
+        for l in range(L):
+            assert torch.equal(got[l][0], Os[l]) and torch.equal(got[l][1], LSEs[l]), (seed, l)
+    check_no_device_error(ws)
