@@ -39,7 +39,7 @@
 namespace ea {
 
 constexpr int kDecKeys = 64;                           // keys per tile
-constexpr int kDecSplitMaxKeys = 128;                  // units up to this many keys: P V in two parts
+constexpr int kDecSplitMaxKeys = 512;                  // units up to this many keys: P V in two parts
 constexpr int kDecStages = 6;
 constexpr int kDecHalfBytes = kDecKeys * 128;          // one 64-dim swizzled box: 8 KB
 constexpr int kDecTileBytes = 2 * kDecHalfBytes;       // K or V of one tile: 16 KB

@@ -246,9 +246,16 @@ __device__ __forceinline__ int first_row_keys(int mode, int qb, int sink, int wi
     return diag_kept ? (N - 1) * T + 1 : N * T;
 }
 
-// Rows that keep at most one tile's worth of keys take the P V product in two
-// bf16 parts (P's rounding and the remainder), see pair_softmax.
-constexpr int kSplitMaxKeys = T;
+// Rows that keep at most this many keys take the P V product in two bf16 parts
+// (P's rounding and the remainder), see pair_softmax.  A row whose weight sits
+// on a few keys carries each probability's 2^-9 rounding error almost whole
+// into O; with V of a large common offset (|v| in [2.2, 3.8), one sign per
+// dimension) query blocks whose first row keeps 129-512 keys still put elements
+// up to 1.4e-3 above a flat 1e-2 when only rows of at most 128 keys were split
+// (24 of 150 random configurations).  At 512 keys none did; the 32K layer's cost is nil (its
+// rows keep more keys past the first query blocks), a batch of 128 sequences
+// of 256-8192 tokens pays about 1 %.
+constexpr int kSplitMaxKeys = 4 * T;
 
 // ------------------------------------------------------------ planner
 // One warp per (b, KV head, q block) row: number of visited key tiles, or -1

@@ -81,7 +81,7 @@ def test_few_kept_keys_with_large_values(dev, num_splits):
     # Units keeping 1 to 128 keys, |V| in [2.2, 3.8) with one sign per (head,
     # dim): |O| stays in [2, 4), where correct rounding alone errs by up to
     # 0.0078, and a P rounded to bf16 would add up to 2^-9 |O|.  Units of at
-    # most 128 keys take P V in two bf16 parts: every element within a flat 1e-2.
+    # most 512 keys take P V in two bf16 parts: every element within a flat 1e-2.
     seqlens = [1, 2, 3, 5, 17, 64, 100, 128]
     B, Hq, Hkv, Lmax, sink, window = len(seqlens), 8, 2, 128, 2, 3
     cfg = wl.DecodeConfig("t", B=B, Hq=Hq, Hkv=Hkv, d=128, L=Lmax, sink=sink, window=window)
@@ -211,3 +211,27 @@ def test_block_decode_at_the_longest_cache(dev):
     Oref, Lref = oracle.decode(q.cpu(), Kc.cpu(), Vc.cpu(), sl.cpu(), m, sink=0, window=1,
                                block_mask=bm)
     assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "Lmax=2^21")
+
+
+def test_random_configurations_offset_values(dev):
+    # decode counterpart of the prefill's offset-value sweep: every element
+    # within a flat 1e-2 (units of up to 512 kept keys take P V in two parts)
+    rng = np.random.default_rng(4343)
+    for case in range(20):
+        B = int(rng.integers(1, 6))
+        Hkv = int(rng.integers(1, 4))
+        Hq = Hkv * int(rng.integers(1, 5))
+        Lmax = int(rng.integers(1, 3000))
+        sink, window = int(rng.integers(0, 300)), int(rng.integers(1, 1200))
+        seqlens = [int(rng.integers(1, Lmax + 1)) for _ in range(B)]
+        cfg = wl.DecodeConfig("t", B=B, Hq=Hq, Hkv=Hkv, d=128, L=Lmax, sink=sink, window=window)
+        q, Kc, _, sl = wl.decode_inputs(cfg, seqlens=seqlens)
+        Vc = wl.offset_values(B, Lmax, Hkv, 128, seed=7100 + case)
+        modes = rng.integers(0, 3, size=(B, Hkv)).astype(np.uint8)
+        bm = wl.block_mask(B, Hkv, Lmax, density=float(rng.uniform(0.1, 0.9)), seed=200 + case).numpy()
+        ns = int(rng.choice([0, 0, 1, 3, 9]))
+        O, LSE = run(dev, q, Kc, Vc, sl, modes, sink, window, ns, bm=bm)
+        Oref, Lref = oracle.decode(q, Kc, Vc, sl, modes, sink=sink, window=window, block_mask=bm)
+        assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
+                     "offset V, case %d (B=%d Hq=%d Hkv=%d Lmax=%d splits=%d)" % (case, B, Hq, Hkv, Lmax, ns),
+                     flat=True)

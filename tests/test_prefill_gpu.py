@@ -111,7 +111,7 @@ def test_few_kept_keys_with_large_values(dev, S, modes, sink, window):
     # With one to a few kept keys a P rounded to bf16 (2^-9 relative) would
     # add up to 2^-9 |O| more and cross 1e-2 (an fp64 model of that arithmetic
     # puts 464 to 1063 elements of these cases above it); rows keeping at most
-    # 128 keys take P V in two bf16 parts, which keeps every element within a
+    # 512 keys take P V in two bf16 parts, which keeps every element within a
     # flat 1e-2.
     B, Hq, Hkv = 1, 4, 2
     Q, K, _ = wl.qkv(B, S, Hq, Hkv, 128, seed=41)
@@ -343,3 +343,30 @@ def test_random_configurations_wider(dev):
         np.testing.assert_array_equal(
             bitmap_to_tiles(vis, B, Hkv, nB),
             oracle.visited(B, S, Hkv, modes, sink=sink, window=window, block_mask=bm), err_msg=what)
+
+
+def test_random_configurations_offset_values(dev):
+    # V with a large common offset (|v| in [2.2, 3.8), one sign per head
+    # dimension): the softmax average keeps |O| near 3, where the output's own
+    # rounding leaves least room under 1e-2, and each probability's rounding
+    # error reaches O with the offset's weight unless it averages out over many
+    # keys.  Every element must be within a flat 1e-2 (rows of up to 512 kept
+    # keys take P V in two bf16 parts).
+    rng = np.random.default_rng(4242)
+    for case in range(30):
+        B = int(rng.integers(1, 3))
+        S = int(rng.integers(1, 1200))
+        Hkv = int(rng.integers(1, 4))
+        Hq = Hkv * int(rng.integers(1, 6))
+        sink = int(rng.integers(0, 400))
+        window = int(rng.integers(1, 900))
+        modes = rng.integers(0, 3, size=(B, Hkv)).astype(np.uint8)
+        Q, K, _ = wl.qkv(B, S, Hq, Hkv, 128, seed=6000 + case)
+        V = wl.offset_values(B, S, Hkv, 128, seed=6500 + case)
+        bm = wl.block_mask(B, Hkv, S, density=float(rng.uniform(0.05, 0.9)), seed=case).numpy()
+        bm[rng.random(bm.shape) < 0.15] = 0
+        O, LSE, _ = run(dev, Q, K, V, modes, sink, window, bm=bm)
+        Oref, Lref = oracle.prefill_full(Q, K, V, modes, sink=sink, window=window, block_mask=bm)
+        assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
+                     "offset V, case %d (B=%d S=%d Hq=%d Hkv=%d sink=%d window=%d)"
+                     % (case, B, S, Hq, Hkv, sink, window), flat=True)
