@@ -527,6 +527,7 @@ struct __align__(1024) PairSmem {
     uint64_t pv_issued;            // the PV issuer has issued an item's last product
     float red_max[2][2][T];        // [tile parity][warpgroup][row]
     float red_l[2][2][T];          // [item parity][warpgroup][row]
+    float red_dl[2][2][T];         // the same for the normaliser's correction (see pair_softmax)
     ItemMeta meta[2];
     uint32_t tmem_base;
     int abort;
@@ -1023,7 +1024,7 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const bool diag_kept = meta_diag(mt.info);
         const bool split = meta_split(mt.info);   // P V in two bf16 parts (few kept keys)
         const int i = x.qb * T + r;
-        float m_run = NEG_INF, l_run = 0.f;
+        float m_run = NEG_INF, l_run = 0.f, dl_run = 0.f;
         bool ok = true;
 
         // the tile loop, compiled twice: with P's remainder (rare items) and without
@@ -1094,11 +1095,22 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
                     if (m_run > NEG_INF) {
                         factor = ex2(m_run - m_new);
                         l_run *= factor;
+                        dl_run *= factor;
                         rescale_o = n > 0;
                     }
                     m_run = m_new;
                 }
                 const float mb = m_run > NEG_INF ? m_run : 0.f;
+                if constexpr (!kSplit) {
+                    // The largest probability of this thread's columns enters O
+                    // rounded to bf16, and it is not 1 (exact) unless the lazy
+                    // running maximum is this tile's.  Its rounding error joins
+                    // the normaliser of O, so that a dominant key's weight stays
+                    // exact; the LSE keeps the unrounded sum.  (Same operations as
+                    // the loop below, so the same value.)
+                    const float pmx = ex2(fmaf(pm, a.scale_log2, -mb));
+                    dl_run += __uint_as_float(pack_bf16x2(pmx, 0.f) << 16) - pmx;
+                }
                 // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
                 // the row sum in four packed accumulators, P packed to bf16 pairs
                 // in place (s[c/2] once s[c], s[c+1] are consumed)
@@ -1189,8 +1201,11 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         // row-sum exchange, the stage's release by the previous item's store)
         // comes first, while the item's last P V product completes.
         sm.red_l[it & 1][wg][r] = l_run;
+        sm.red_dl[it & 1][wg][r] = dl_run;
         named_bar_sync(bar_id, 64);
         const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
+        // O's normaliser: the sum of the probabilities as O received them
+        const float ln_tot = l_tot + (dl_run + sm.red_dl[it & 1][wg ^ 1][r]);
         if (!kVarlen && store) {
             if (lane == 0)
                 bulk_wait_read_all();     // the previous item's store has read the stage
@@ -1206,7 +1221,7 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const bool row_ok = store && i < e.S &&
                             in_bounds(e.tok0 + i, kVarlen ? a.total_tokens : a.S, err) &&
                             in_bounds(qh, a.Hq, err);
-        const float inv_l = l_tot > 0.f ? 1.f / l_tot : 0.f;
+        const float inv_l = ln_tot > 0.f ? 1.f / ln_tot : 0.f;
         __nv_bfloat16 *orow = a.O[e.layer] + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss +
                               qh * a.o_sh + 64 * wg;
         // Fixed-length batches: each warp stages its 32 rows x 64 columns in
