@@ -370,3 +370,33 @@ def test_random_configurations_offset_values(dev):
         assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref,
                      "offset V, case %d (B=%d S=%d Hq=%d Hkv=%d sink=%d window=%d)"
                      % (case, B, S, Hq, Hkv, sink, window), flat=True)
+
+
+
+
+def test_dominant_key_beyond_the_running_maximum(dev):
+    # Rows 600..1023 keep key 0 (score 0, the first tile's maximum), key 600,
+    # whose score is 5.005 higher (log2 units; within the lazy rescale's
+    # threshold, so the running maximum stays at key 0's score), and keys far
+    # below.  Key 600's probability 2^5.005 = 32.115 is rounded to 32.0 in bf16
+    # (-0.36 %) and carries 97 % of the weight; with v = -3.875 against key 0's
+    # +3.875 a copy of the kernel without the normaliser's correction is 0.0152
+    # off the oracle (an fp64 model of that arithmetic: 0.0151).  These query
+    # blocks keep more than 512 keys, so no remainder product applies; the
+    # normaliser takes the rounding of the tile's largest probability, which
+    # makes the weights exact: every element within a flat 1e-2.
+    S, d = 1024, 128
+    Q = torch.zeros(1, S, 1, d)
+    K = torch.zeros(1, S, 1, d)
+    V = torch.zeros(1, S, 1, d)
+    Q[0, :, 0, 0] = 1.0
+    K[0, 1:, 0, 0] = -128.0         # every other key far below
+    K[0, 600, 0, 0] = 39.25         # 39.25 / sqrt(128) * log2(e) = 5.005
+    V[0, 0, 0, :] = 3.875
+    V[0, 600, 0, :] = -3.875
+    Q, K, V = (t.to(torch.bfloat16) for t in (Q, K, V))
+    modes = [[FULL]]
+    O, LSE, _ = run(dev, Q, K, V, modes, 0, S)
+    Oref, Lref = oracle.prefill_full(Q, K, V, np.array(modes, np.uint8), sink=0, window=S)
+    assert_close(O.float().cpu().numpy(), LSE.cpu().numpy(), Oref, Lref, "dominant key", flat=True)
+    assert abs(float(O[0, 700, 0, 0]) + 3.64) < 0.05    # the dominant key's value does dominate
