@@ -1206,7 +1206,9 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const float l_tot = l_run + sm.red_l[it & 1][wg ^ 1][r];
         // O's normaliser: the sum of the probabilities as O received them
         const float ln_tot = l_tot + (dl_run + sm.red_dl[it & 1][wg ^ 1][r]);
-        if (!kVarlen && store) {
+        const int row0 = x.qb * T + quad * 32;   // the warp's first row in its sequence
+        const bool staged = store && (!kVarlen || row0 + 32 <= x.S);
+        if (staged) {
             if (lane == 0)
                 bulk_wait_read_all();     // the previous item's store has read the stage
             __syncwarp();
@@ -1224,12 +1226,11 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
         const float inv_l = ln_tot > 0.f ? 1.f / ln_tot : 0.f;
         __nv_bfloat16 *orow = a.O[e.layer] + e.b * a.o_sb + static_cast<int64_t>(e.tok0 + i) * a.o_ss +
                               qh * a.o_sh + 64 * wg;
-        // Fixed-length batches: each warp stages its 32 rows x 64 columns in
-        // shared memory (128-byte swizzle, as the tensor map expects) and its
-        // lane 0 stores them with TMA, which skips rows past S.  Variable-
-        // length batches store directly: the rows past a sequence belong to
-        // the next one.
-        const bool staged = !kVarlen && store;
+        // A warp stages its 32 rows x 64 columns in shared memory (128-byte
+        // swizzle, as the tensor map expects) and its lane 0 stores them with
+        // TMA, which skips rows past S in a fixed-length batch.  In a variable-
+        // length batch the warp over a sequence's end stores its rows directly:
+        // the rows past the end belong to the next sequence.
         const int wrow = r & 31;
         uint8_t *wstage = sm.ostage + warp * (kTileBytes / 8);
         // both halves of this warp's O columns in one round trip to TMEM
@@ -1277,7 +1278,7 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
             fence_proxy_async_smem();     // the stage's writes -> the TMA unit
             __syncwarp();
             if (lane == 0) {
-                tma_store_4d(&tm.o[kL == 1 ? 0 : e.layer], wstage, 64 * wg, qh, x.qb * T + quad * 32, e.b);
+                tma_store_4d(&tm.o[kL == 1 ? 0 : e.layer], wstage, 64 * wg, qh, (kVarlen ? e.tok0 : 0) + row0, e.tma_b);
                 bulk_commit_group();
             }
         }

@@ -87,12 +87,15 @@ def test_strided_views_and_bad_sequence(dev):
     Q, K, V = qkv[:, :Hq], qkv[:, Hq:Hq + Hkv], qkv[:, Hq + Hkv:]
     cu = torch.tensor([0, 400, 1300, 1600], dtype=torch.int32, device=dev)
     m = torch.tensor([[FULL, SSA]] * 3, dtype=torch.uint8, device=dev)
-    O = torch.full((total, Hq + 3, 128), 7.0, dtype=torch.bfloat16, device=dev)[:, 1:1 + Hq]
+    wide = torch.full((total, Hq + 3, 128), 7.0, dtype=torch.bfloat16, device=dev)
+    O = wide[:, 1:1 + Hq]
     ws = ea.prefill_varlen_workspace(3, total, 500, Hq, Hkv, device=dev)
     _, LSE = ea.ea_hybrid_attn_prefill_varlen(Q, K, V, cu, m, max_seqlen=500, sink=16, window=200, O=O,
                                               workspace=ws)
     assert ea.ea_check_errors(ws) == 6            # sequence 1 (900 > 500) reported
     assert (O[400:1300].float() == 7.0).all()     # and not written
+    # the heads beside the view are untouched (staged stores write whole warps of rows)
+    assert (wide[:, 0].float() == 7.0).all() and (wide[:, 1 + Hq:].float() == 7.0).all()
     for b, (c0, L) in enumerate([(0, 400), (1300, 300)]):
         Ob, Lb = ea.ea_hybrid_attn_prefill(Q[c0:c0 + L][None], K[c0:c0 + L][None], V[c0:c0 + L][None],
                                            m[:1], sink=16, window=200)
