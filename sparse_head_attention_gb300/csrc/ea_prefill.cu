@@ -1113,10 +1113,15 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
                 }
                 // p = 2^(s * scale_log2 - mb): the affine part two lanes at a time,
                 // the row sum in four packed accumulators, P packed to bf16 pairs
-                // in place (s[c/2] once s[c], s[c+1] are consumed)
+                // in place (s[c/2] once s[c], s[c+1] are consumed).  Rows that
+                // keep few keys also take P's remainder P - bf16(P), rounded to
+                // bf16, which a second P V product reads 32 columns further on
+                // (an error of 2^-9 of the remainder, 2^-17 of P, is left); it
+                // goes to TMEM 16 columns at a time, over S already read.
                 const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
                 const uint64_t nm2 = f2_pack(-mb, -mb);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+                uint32_t rem[16];
 #pragma unroll
                 for (int cc = 0; cc < 64; cc += 2) {
                     float x0, x1;
@@ -1124,7 +1129,14 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
                               x0, x1);
                     const float p0 = ex2(x0), p1 = ex2(x1);
                     acc[(cc >> 1) & 3] = f2_add(acc[(cc >> 1) & 3], f2_pack(p0, p1));
-                    s[cc >> 1] = pack_bf16x2(p0, p1);
+                    const uint32_t hi = pack_bf16x2(p0, p1);
+                    s[cc >> 1] = hi;
+                    if constexpr (kSplit) {
+                        rem[(cc >> 1) & 15] = pack_bf16x2(p0 - __uint_as_float(hi << 16),
+                                                          p1 - __uint_as_float(hi & 0xffff0000u));
+                        if (((cc >> 1) & 15) == 15)
+                            tmem_st16(tS + 32 + ((cc >> 1) & ~15), rem);
+                    }
                 }
                 float l0, l1, l2, l3;
                 f2_unpack(f2_add(acc[0], acc[1]), l0, l1);
@@ -1147,37 +1159,6 @@ __device__ __forceinline__ void pair_softmax(const PrefillArgs &a, PairSmem &sm,
                         for (int cc = 0; cc < 32; ++cc)
                             o[cc] = __float_as_uint(__uint_as_float(o[cc]) * factor);
                         tmem_st32(tO + ch * 32, o);
-                    }
-                }
-                if constexpr (kSplit) {
-                    // P again from S (same operations, same values), and its
-                    // remainder P - bf16(P) rounded to bf16 over the other 32 columns
-                    // (read by a second P V product; an error of 2^-9 of the
-                    // remainder, 2^-17 of P, is left)
-#pragma unroll 1
-                    for (int q = 1; q >= 0; --q) {   // columns 32..63 first: rem lands there
-                        uint32_t t[32], rem[16];
-                        tmem_ld32(tS + 32 * q, t);
-                        tmem_wait_ld();
-                        uint32_t w = 0xffffffffu;
-                        if (edge) {
-                            const int j0 = kb * T, co = 64 * wg + 32 * q;
-                            const int sk = mode == EA_SSA ? a.sink - j0 : -1;
-                            const int lo = mode == EA_SSA ? i - a.window - j0 : -1;
-                            w = low_bits(i - j0 + 1 - co) & (low_bits(sk - co) | ~low_bits(lo + 1 - co));
-                        }
-#pragma unroll
-                        for (int cc = 0; cc < 32; cc += 2) {
-                            const float s0 = (w >> cc) & 1u ? __uint_as_float(t[cc]) : NEG_INF;
-                            const float s1 = (w >> (cc + 1)) & 1u ? __uint_as_float(t[cc + 1]) : NEG_INF;
-                            float x0, x1;
-                            f2_unpack(f2_fma(f2_pack(s0, s1), sc2, nm2), x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            const uint32_t hi = pack_bf16x2(p0, p1);
-                            rem[cc >> 1] = pack_bf16x2(p0 - __uint_as_float(hi << 16),
-                                                       p1 - __uint_as_float(hi & 0xffff0000u));
-                        }
-                        tmem_st16(tS + 32 + 16 * q, rem);
                     }
                 }
                 // P (bf16 pairs) over the first 32 of this warpgroup's S columns
