@@ -680,18 +680,20 @@ __device__ __forceinline__ uint32_t lead_bar(const uint64_t *bar)
 }
 
 // Bounded wait of the pair kernel, called by every lane of a warp; the result
-// is the same in all lanes.  It fails at once when the CTA is aborting
-// (checked first, so that no role passes another wait after an abort) and
-// after the timeout (raising EA_DEVERR_TIMEOUT and aborting both CTAs).
+// is the same in all lanes.  It fails at once when the CTA is aborting (the
+// flag is read with the barrier's first test, so that no role passes another
+// wait after an abort, and neither read waits for the other) and after the
+// timeout (raising EA_DEVERR_TIMEOUT and aborting both CTAs).
 // Acquire at CTA scope, or at cluster scope (`cl`) for the item hand-off from
 // the other CTA.
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, const PairCtx &c,
                                       bool cl = false)
 {
-    bool ok = false;
-    if (!*c.abort) {
-        const uint32_t a = smem_u32(bar);
-        ok = cl ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+    const int aborting = *c.abort;
+    const uint32_t a = smem_u32(bar);
+    bool ok = cl ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity);
+    ok = ok && !aborting;
+    if (!aborting) {
         if (!ok) {
             const uint64_t t0 = globaltimer_ns();
             while (true) {
@@ -719,10 +721,12 @@ __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, const Pair
 // The same for one thread (the MMA issuer).
 __device__ __forceinline__ bool pwait1(uint64_t *bar, uint32_t parity, const PairCtx &c)
 {
-    if (*c.abort)
-        return false;
+    const int aborting = *c.abort;
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity))
+    const bool done = mbar_try_wait(a, parity);
+    if (aborting)
+        return false;
+    if (done)
         return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
