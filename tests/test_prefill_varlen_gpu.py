@@ -47,6 +47,9 @@ def packed_inputs(lens, Hq, Hkv, seed, use_bm):
     ([128, 256, 127, 1], 12, 4, True),
     ([3000], 8, 2, True),
     ([5, 300, 0, 0, 2049, 17], 6, 2, False),
+    # lengths at 32-row boundaries: a warp's 32 rows either all inside the
+    # sequence (stored through shared memory and TMA) or crossing its end
+    ([160, 96, 32, 64, 224, 33, 31], 8, 2, True),
 ])
 def test_each_sequence_equals_its_own_prefill(dev, lens, Hq, Hkv, use_bm):
     sink, window = 64, 300
