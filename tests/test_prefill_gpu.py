@@ -61,6 +61,8 @@ SHAPES = [
     (1, 513, 4, 4, [[FULL, SSA, FULL, SSA]], 130, 129),          # one query head per KV head
     (1, 700, 8, 2, [[SSA, SSA]], 2000, 1),                       # sink covers everything
     (1, 640, 8, 2, [[SSA, FULL]], 128, 128),                     # tile-aligned sink / window
+    (1, 700, 16, 2, [[FULL, SSA]], 64, 300),                     # group size 8 (four head pairs)
+    (2, 450, 14, 2, [[SSA, FULL], [FULL, SSA]], 32, 200),        # group size 7 (last head paired with itself)
 ]
 
 
