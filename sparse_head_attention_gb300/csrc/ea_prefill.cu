@@ -463,19 +463,20 @@ __global__ void __launch_bounds__(1024) varlen_setup_kernel(PrefillArgs a)
 // P V product that read its P has completed (an mbarrier wait): no ordering
 // between MMAs into different accumulators is assumed.
 //
-// Roles (320 threads per CTA):
+// Roles (352 threads per CTA):
 //   warps 0-7  softmax.  Warpgroup w handles columns 64w .. 64w + 63 of every
 //              S row (one query row per thread); the two threads of a row
 //              exchange their partial row maxima through shared memory and a
 //              named barrier of their two warps.  P (bf16 pairs) is written
 //              over the warpgroup's own S columns.  Epilogue: O / l of the
-//              warpgroup's 64 head dims, stored by TMA (or directly for
-//              variable-length batches), and LSE.
+//              warpgroup's 64 head dims, stored by TMA (in a variable-length
+//              batch the warp whose rows cross the sequence's end stores them
+//              directly), and LSE.
 //   warp 8     TMA producer (both CTAs): this CTA's Q and its halves of the
 //              K/V tiles, tile by tile, into a 3-slot K ring and a 4-slot V
 //              ring; completion is reported to rank 0's barriers.  Rank 0's
-//              producer also takes items from the work queue and hands them to
-//              rank 1.
+//              producer also takes items from the work queue and publishes
+//              each item's metadata to both CTAs.
 //   warps 9, 10  rank 0, one thread each: the S = Q K^T issuer and the
 //              O += P V issuer; warp 9 of both ranks: the pair's TMEM allocation.
 // A tcgen05.mma holds its issuing thread for about its own execution time, so
